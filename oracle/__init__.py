@@ -1,0 +1,126 @@
+"""Float64 CPU oracle of the gated delta-rule layer (ctypes binding).
+
+TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the
+benchmark's CPU-baseline leg import this module; the product path never
+does.  It shares no code with the CUDA library.
+
+The arithmetic lives in ``gdn_oracle.c`` (plain C, double precision); see
+its header for what each function follows ("Qwen3.5-9B-npu" model card,
+section "How it works": the per-token recurrence, the chunkwise form,
+token_valid padding and the block-doubling triangular inverse).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libgdn_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler (portable flags, no FMA contraction)."""
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+                               "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        lib.gdn_oracle_recurrent.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, I, I]
+        lib.gdn_oracle_recurrent.restype = I
+        lib.gdn_oracle_chunked.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, I, I, I, I]
+        lib.gdn_oracle_chunked.restype = I
+        lib.gdn_oracle_tril_inverse.argtypes = [I, P, P, I]
+        lib.gdn_oracle_tril_inverse.restype = I
+        _lib = lib
+    return _lib
+
+
+def _f32(x):
+    return None if x is None else np.ascontiguousarray(x, np.float32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _prep(q, k, v, g, beta, state_in, cu_seqlens, pairs):
+    q, k, v, g, beta, state_in = map(_f32, (q, k, v, g, beta, state_in))
+    T, hk, dk = q.shape
+    _, hv, dv = v.shape
+    assert k.shape == (T, hk, dk) and v.shape[0] == T
+    assert g.shape == (T, hv) and beta.shape == (T, hv)
+    cu = np.ascontiguousarray(cu_seqlens, np.int32)
+    n = len(cu) - 1
+    assert cu[0] == 0 and cu[-1] == T and np.all(np.diff(cu) >= 0)
+    if state_in is not None:
+        assert state_in.shape == (n, hv, dk, dv)
+    pr = None if pairs is None else np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
+    o = np.zeros((T, hv, dv), np.float64)
+    s_out = np.zeros((n, hv, dk, dv), np.float64)
+    return q, k, v, g, beta, state_in, cu, pr, o, s_out, (n, hk, hv, dk, dv)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def recurrent(q, k, v, g, beta, state_in, cu_seqlens,
+              pairs: Optional[Sequence[Tuple[int, int]]] = None,
+              threads: Optional[int] = None):
+    """Per-token gated delta rule in float64.
+
+    Returns (o [T, Hv, dv], state_out [N, Hv, dk, dv]) as float64.  With
+    `pairs`, only those (sequence, v-head) chains are computed; the other
+    entries of both outputs stay zero.
+    """
+    q, k, v, g, beta, s_in, cu, pr, o, s_out, (n, hk, hv, dk, dv) = \
+        _prep(q, k, v, g, beta, state_in, cu_seqlens, pairs)
+    rc = _load().gdn_oracle_recurrent(
+        n, hk, hv, dk, dv, _ptr(cu), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s_in),
+        _ptr(o), _ptr(s_out), _ptr(pr), 0 if pr is None else len(pr),
+        threads or default_threads())
+    if rc:
+        raise RuntimeError("gdn_oracle_recurrent failed (%d)" % rc)
+    return o, s_out
+
+
+def chunked(q, k, v, g, beta, state_in, cu_seqlens, chunk: int, solve: str = "forward",
+            pairs: Optional[Sequence[Tuple[int, int]]] = None,
+            threads: Optional[int] = None):
+    """Chunkwise-parallel closed form in float64 (solve: "forward" or "doubling")."""
+    q, k, v, g, beta, s_in, cu, pr, o, s_out, (n, hk, hv, dk, dv) = \
+        _prep(q, k, v, g, beta, state_in, cu_seqlens, pairs)
+    rc = _load().gdn_oracle_chunked(
+        n, hk, hv, dk, dv, _ptr(cu), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s_in),
+        _ptr(o), _ptr(s_out), _ptr(pr), 0 if pr is None else len(pr), int(chunk),
+        {"forward": 0, "doubling": 1}[solve], threads or default_threads())
+    if rc:
+        raise RuntimeError("gdn_oracle_chunked failed (%d)" % rc)
+    return o, s_out
+
+
+def tril_inverse(Nm: np.ndarray, method: str = "forward") -> np.ndarray:
+    """(I + tril(Nm, -1))^-1 in float64 by forward substitution or block doubling."""
+    Nm = np.ascontiguousarray(Nm, np.float64)
+    n = Nm.shape[0]
+    X = np.zeros((n, n), np.float64)
+    rc = _load().gdn_oracle_tril_inverse(n, _ptr(Nm), _ptr(X), {"forward": 0, "doubling": 1}[method])
+    if rc:
+        raise RuntimeError("gdn_oracle_tril_inverse failed")
+    return X
