@@ -1,0 +1,182 @@
+"""Python binding of libgdn, the gated delta-rule layer for GB300 (sm_103a).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels of
+``libgdn.so`` (built in-tree by ``build.py``).  The functions carry the C-ABI's
+names (include/gdn.h) and take torch CUDA tensors, which supply device memory
+and the current stream; there is no CPU path.  If the library has not been
+built, importing works but every call raises ``GdnUnavailable``.
+
+Layer ("Qwen3.5-9B-npu" model card, section "How it works"): per head a state
+S [dk, dv] evolves per token by S <- S exp(g_t); kv = S^T k_t;
+S <- S + k_t (x) ((v_t - kv) beta_t); o_t = S^T q_t.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgdn.so")
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIAS, GDN_ERR_WORKSPACE, \
+    GDN_ERR_CUDA = range(6)
+GDN_F32, GDN_BF16 = 0, 1
+GDN_OP_PREFILL, GDN_OP_DECODE, GDN_OP_VERIFY = 0, 1, 2
+
+EXPORTS = ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_block",
+           "gdn_workspace_size", "gdn_status_string")
+
+
+class GdnUnavailable(RuntimeError):
+    """libgdn.so is missing or cannot be loaded."""
+
+
+class GdnError(RuntimeError):
+    """A libgdn entry point returned a status other than GDN_OK."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s" % (what, gdn_status_string(status)))
+
+
+class GdnShape(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+                ("chunk", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgdn.so (raises GdnUnavailable if it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise GdnUnavailable("libgdn.so not built (run gated_deltanet_linear_05_gb300/build.py)")
+        try:
+            L = ctypes.CDLL(LIB_PATH)
+        except OSError as e:
+            raise GdnUnavailable("cannot load libgdn.so: %s" % e)
+        P, S = ctypes.c_void_p, ctypes.c_size_t
+        for name in ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_block"):
+            f = getattr(L, name)
+            f.argtypes = [ctypes.POINTER(GdnShape), P, P, P, P, P, P, P, P, P, P, S, P]
+            f.restype = ctypes.c_int
+        L.gdn_workspace_size.argtypes = [ctypes.POINTER(GdnShape), ctypes.c_int]
+        L.gdn_workspace_size.restype = ctypes.c_size_t
+        L.gdn_status_string.argtypes = [ctypes.c_int]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def gdn_status_string(status: int) -> str:
+    return lib().gdn_status_string(int(status)).decode()
+
+
+def make_shape(num_seqs: int, total_tokens: int, num_k_heads: int, num_v_heads: int,
+               dk: int = 128, dv: int = 128, chunk: int = 64, dtype: int = GDN_BF16) -> GdnShape:
+    return GdnShape(num_seqs, total_tokens, num_k_heads, num_v_heads, dk, dv, chunk, dtype)
+
+
+def gdn_workspace_size(shape: GdnShape, op: int) -> int:
+    n = lib().gdn_workspace_size(ctypes.byref(shape), int(op))
+    if n == ctypes.c_size_t(-1).value:
+        raise GdnError(GDN_ERR_INVALID_ARG, "gdn_workspace_size")
+    return n
+
+
+# ------------------------------------------------------------------ torch marshalling
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _shape_of(q, v, state_out, cu_seqlens, chunk: int) -> GdnShape:
+    T, hk, dk = q.shape
+    hv, dv = v.shape[1], v.shape[2]
+    n = state_out.shape[0] if state_out is not None else (len(cu_seqlens) - 1)
+    return make_shape(n, T, hk, hv, dk, dv, chunk, _dtype_code(q))
+
+
+def _check_tensors(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("libgdn takes contiguous CUDA tensors")
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _workspace(shape: GdnShape, op: int, device, workspace):
+    need = gdn_workspace_size(shape, op)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        torch = _torch()
+        workspace = torch.empty(need + 256, dtype=torch.uint8, device=device)
+    base = workspace.data_ptr()
+    aligned = (base + 255) & ~255
+    return aligned, workspace.numel() - (aligned - base)
+
+
+def _call(name, op, q, k, v, g, beta, state_in, state_out, cu_seqlens, o, chunk,
+          workspace, stream):
+    _check_tensors(q, k, v, g, beta, state_in, state_out, cu_seqlens, o, workspace)
+    shape = _shape_of(q, v, state_out, cu_seqlens, chunk)
+    ws_ptr, ws_bytes = _workspace(shape, op, q.device, workspace)
+    st = getattr(lib(), name)(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                              _ptr(beta), _ptr(state_in), _ptr(state_out), _ptr(cu_seqlens),
+                              _ptr(o), ws_ptr, ws_bytes, _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, name)
+    return o, state_out
+
+
+def gdn_prefill_chunked(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,
+                        chunk: int = 64, workspace=None, stream=None):
+    """Chunkwise-parallel prompt pass.  Tensors as in include/gdn.h:
+    q, k [T, Hk, 128]; v [T, Hv, 128]; g, beta [T, Hv] fp32; state_in (or None),
+    state_out [N, Hv, 128, 128] fp32; cu_seqlens [N+1] int32.  Returns (o, state_out)."""
+    if o is None:
+        o = _torch().empty_like(v)
+    return _call("gdn_prefill_chunked", GDN_OP_PREFILL, q, k, v, g, beta, state_in, state_out,
+                 cu_seqlens, o, chunk, workspace, stream)
+
+
+def gdn_verify_block(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,
+                     chunk: int = 16, workspace=None, stream=None):
+    """Draft-verify block from the snapshot state_in (left unchanged)."""
+    if o is None:
+        o = _torch().empty_like(v)
+    return _call("gdn_verify_block", GDN_OP_VERIFY, q, k, v, g, beta, state_in, state_out,
+                 cu_seqlens, o, chunk, workspace, stream)
+
+
+def gdn_decode_step(q, k, v, g, beta, state_in, state_out, cu_seqlens=None, o=None,
+                    stream=None):
+    """Token-by-token recurrence (cu_seqlens None: one token per sequence)."""
+    if o is None:
+        o = _torch().empty_like(v)
+    return _call("gdn_decode_step", GDN_OP_DECODE, q, k, v, g, beta, state_in, state_out,
+                 cu_seqlens, o, 64, None, stream)

@@ -1,0 +1,145 @@
+// Device helpers shared by the libgdn kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kD = 128;  // dk = dv = 128, the head size built
+
+// ------------------------------------------------------------------ dtype traits
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+  static __device__ __forceinline__ float load(const float *p) { return *p; }
+  static __device__ __forceinline__ void store(float *p, float x) { *p = x; }
+};
+template <>
+struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+    return __bfloat162float(*p);
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16 *p, float x) {
+    *p = __float2bfloat16_rn(x);
+  }
+};
+
+// ------------------------------------------------------------------ sequences
+
+// Token range [bos, eos) of sequence n, clamped to [0, total] so that a malformed
+// cu_seqlens can never move an access outside the buffers.
+__device__ __forceinline__ void seq_range(const int32_t *cu, int n, int total, int &bos,
+                                          int &eos) {
+  int a = cu[n], b = cu[n + 1];
+  a = min(max(a, 0), total);
+  b = min(max(b, a), total);
+  bos = a;
+  eos = b;
+}
+
+// ------------------------------------------------------------------ cp.async
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global->shared copy; src_bytes == 0 fills the destination with zeros.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)),
+               "l"(gmem), "r"(src_bytes));
+}
+// 4-byte global->shared copy; src_bytes == 0 writes a zero.
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(smem)),
+               "l"(gmem), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ------------------------------------------------------------------ tensor cores
+// mma.sync m16n8k16, bf16 inputs, fp32 accumulate.  Fragment ownership (lane l,
+// gid = l >> 2, tig = l & 3):
+//   A 16x16 (row-major): a0:(gid, 2tig..+1) a1:(gid+8, 2tig..) a2:(gid, 2tig+8..) a3:(gid+8, 2tig+8..)
+//   B 16x8  (k x n):     b0:(k=2tig..+1, n=gid) b1:(k=2tig+8..+9, n=gid)
+//   C 16x8:              c0,c1:(gid, 2tig..+1) c2,c3:(gid+8, 2tig..+1)
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *smem) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(smem)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *smem) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(smem)));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Swizzled tile of bf16 rows: row r holds ROWB bytes (a multiple of 16) split in
+// 16-byte granules.  Granule g of row r is stored at granule g ^ ((r / RPL) & MASK),
+// RPL = rows per 128-byte line, so that an ldmatrix read of eight consecutive rows at
+// one column touches eight different 16-byte bank groups.
+template <int ROWB>
+__device__ __forceinline__ int swz(int r, int byte_col) {
+  constexpr int GP = ROWB / 16;
+  constexpr int RPL = ROWB >= 128 ? 1 : 128 / ROWB;
+  constexpr int MASK = (GP >= 8 ? 8 : GP) - 1;
+  const int g = byte_col >> 4;
+  return r * ROWB + (((g ^ ((r / RPL) & MASK)) << 4) | (byte_col & 15));
+}
+
+// A-operand (16x16 at rows r0.., bf16 cols c0..) from a swizzled row-major tile.
+template <int ROWB>
+__device__ __forceinline__ void lda_tile(uint32_t (&a)[4], const char *base, int r0, int c0,
+                                         int lane) {
+  const int r = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int c = c0 + (lane >> 4) * 8;
+  ldsm_x4(a, base + swz<ROWB>(r, c * 2));
+}
+// Two B-operands (n-tiles n0 and n0+8, k 16 wide at k0) from a tile stored [n][k].
+// b[0], b[1]: n-tile n0 (k lo, k hi); b[2], b[3]: n-tile n0 + 8.
+template <int ROWB>
+__device__ __forceinline__ void ldb_nk(uint32_t (&b)[4], const char *base, int n0, int k0,
+                                       int lane) {
+  const int r = n0 + (lane & 7) + (lane >> 4) * 8;
+  const int c = k0 + ((lane >> 3) & 1) * 8;
+  ldsm_x4(b, base + swz<ROWB>(r, c * 2));
+}
+// Two B-operands (n-tiles n0 and n0+8, k 16 wide at k0) from a tile stored [k][n].
+template <int ROWB>
+__device__ __forceinline__ void ldb_kn(uint32_t (&b)[4], const char *base, int k0, int n0,
+                                       int lane) {
+  const int r = k0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int c = n0 + (lane >> 4) * 8;
+  ldsm_x4_t(b, base + swz<ROWB>(r, c * 2));
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+}  // namespace gdn

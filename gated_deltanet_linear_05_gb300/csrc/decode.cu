@@ -1,0 +1,142 @@
+// Token-by-token gated delta rule (decode step), "Qwen3.5-9B-npu" model card,
+// section "How it works": the 1-token matrix form
+//     d = exp(g);  u = S^T k,  w = S^T q  (one pass over S);  delta = beta (v - d u)
+//     o = d w + (q.k) delta;   S' = d S + k delta^T
+// which equals the four-line per-token rule (decay, read, write, output from the
+// updated state).
+//
+// One CTA of 128 threads owns a quarter of one head's state: S[0:128, 32c:32c+32]
+// (value columns are independent: every reduction runs over the key index only).
+// Each thread keeps 8 rows x 4 columns of S in registers for the whole sequence, so
+// the state is read from HBM once and written once, with 128-bit accesses; per token
+// the column sums k^T S and q^T S are formed in one pass, reduced across the 4 rows a
+// warp covers by shuffles and across the 4 warps through shared memory.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kDecThreads = 128;
+constexpr int kDecCols = 32;  // value columns per CTA
+
+template <typename T>
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeParams p) {
+  const int quarter = blockIdx.x & 3;
+  const int nh = blockIdx.x >> 2;
+  const int n = nh / p.hv;
+  const int h = nh - n * p.hv;
+  const int kh = h / (p.hv / p.hk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rsub = lane >> 3;  // row within the warp's group of 4
+  const int cg = lane & 7;     // column group of 4
+  const int col0 = quarter * kDecCols + cg * 4;
+
+  int bos, eos;
+  if (p.cu_seqlens) {
+    seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
+  } else {
+    bos = n;
+    eos = n + 1;
+  }
+
+  __shared__ float s_q[kD], s_k[kD], s_v[kDecCols];
+  __shared__ float s_red[2][4][kDecCols];
+
+  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD;
+  float4 S[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int i = s * 16 + warp * 4 + rsub;
+    S[s] = p.state_in
+               ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + col0)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  const T *q = static_cast<const T *>(p.q);
+  const T *k = static_cast<const T *>(p.k);
+  const T *v = static_cast<const T *>(p.v);
+  T *o = static_cast<T *>(p.o);
+
+  for (int t = bos; t < eos; ++t) {
+    s_q[tid] = Elem<T>::load(q + ((size_t)t * p.hk + kh) * kD + tid);
+    s_k[tid] = Elem<T>::load(k + ((size_t)t * p.hk + kh) * kD + tid);
+    if (tid < kDecCols)
+      s_v[tid] = Elem<T>::load(v + ((size_t)t * p.hv + h) * kD + quarter * kDecCols + tid);
+    const float d = expf(p.g[(size_t)t * p.hv + h]);
+    const float b = p.beta[(size_t)t * p.hv + h];
+    __syncthreads();
+
+    // q.k: every warp forms it (4 products per lane, then a butterfly)
+    float qk = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) qk += s_q[lane * 4 + e] * s_k[lane * 4 + e];
+    qk = warp_sum(qk);
+
+    // partial column sums of S^T k and S^T q over this thread's 8 rows
+    float u[4] = {0.f, 0.f, 0.f, 0.f}, w[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const int i = s * 16 + warp * 4 + rsub;
+      const float ki = s_k[i], qi = s_q[i];
+      u[0] += S[s].x * ki; u[1] += S[s].y * ki; u[2] += S[s].z * ki; u[3] += S[s].w * ki;
+      w[0] += S[s].x * qi; w[1] += S[s].y * qi; w[2] += S[s].z * qi; w[3] += S[s].w * qi;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      u[e] += __shfl_xor_sync(0xffffffffu, u[e], 8);
+      u[e] += __shfl_xor_sync(0xffffffffu, u[e], 16);
+      w[e] += __shfl_xor_sync(0xffffffffu, w[e], 8);
+      w[e] += __shfl_xor_sync(0xffffffffu, w[e], 16);
+    }
+    if (rsub == 0) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s_red[0][warp][cg * 4 + e] = u[e];
+        s_red[1][warp][cg * 4 + e] = w[e];
+      }
+    }
+    __syncthreads();
+
+    float delta[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = cg * 4 + e;
+      const float uu = s_red[0][0][c] + s_red[0][1][c] + s_red[0][2][c] + s_red[0][3][c];
+      const float ww = s_red[1][0][c] + s_red[1][1][c] + s_red[1][2][c] + s_red[1][3][c];
+      delta[e] = b * (s_v[c] - d * uu);
+      if (warp == 0 && rsub == 0)
+        Elem<T>::store(o + ((size_t)t * p.hv + h) * kD + col0 + e, d * ww + qk * delta[e]);
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const float ki = s_k[s * 16 + warp * 4 + rsub];
+      S[s].x = d * S[s].x + ki * delta[0];
+      S[s].y = d * S[s].y + ki * delta[1];
+      S[s].z = d * S[s].z + ki * delta[2];
+      S[s].w = d * S[s].w + ki * delta[3];
+    }
+    __syncthreads();  // s_q / s_k / s_v / s_red are rewritten by the next token
+  }
+
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int i = s * 16 + warp * 4 + rsub;
+    *reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)i * kD + col0) = S[s];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream) {
+  const long long units = (long long)p.num_seqs * p.hv * 4;
+  if (units == 0) return cudaSuccess;
+  if (p.dtype == GDN_BF16)
+    decode_kernel<__nv_bfloat16><<<(unsigned)units, kDecThreads, 0, stream>>>(p);
+  else
+    decode_kernel<float><<<(unsigned)units, kDecThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,188 @@
+// C-ABI entry points of libgdn: host-side validation, workspace layout and launch.
+// Declarations and the argument contract: include/gdn.h.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+using gdn::ChunkParams;
+using gdn::DecodeParams;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gdn_status check_shape(const gdn_shape *s, bool needs_chunk) {
+  if (!s) return GDN_ERR_INVALID_ARG;
+  if (s->num_seqs < 0 || s->total_tokens < 0 || s->num_k_heads <= 0 || s->num_v_heads <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (s->num_v_heads % s->num_k_heads != 0) return GDN_ERR_INVALID_ARG;
+  if (s->dk != gdn::kD || s->dv != gdn::kD) return GDN_ERR_UNSUPPORTED;
+  if (s->qkv_dtype != GDN_F32 && s->qkv_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (needs_chunk && s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return GDN_ERR_UNSUPPORTED;
+  // grids are sized (sequences x v-heads x 8) in one dimension
+  if ((long long)s->num_seqs * s->num_v_heads * 8 > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+// [a, a+n) and [b, b+n) overlap without being identical
+bool partial_overlap(const void *a, const void *b, size_t n) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  if (x == y) return false;
+  return x < y + n && y < x + n;
+}
+
+struct Common {
+  const gdn_shape *s;
+  const void *q, *k, *v;
+  const float *g, *beta, *state_in;
+  float *state_out;
+  const int32_t *cu_seqlens;
+  void *o;
+};
+
+gdn_status check_buffers(const Common &c, bool cu_required) {
+  const gdn_shape *s = c.s;
+  if (s->total_tokens > 0) {
+    if (!c.q || !c.k || !c.v || !c.g || !c.beta || !c.o) return GDN_ERR_INVALID_ARG;
+    if (!aligned16(c.q) || !aligned16(c.k) || !aligned16(c.v) || !aligned16(c.o) ||
+        !aligned16(c.g) || !aligned16(c.beta))
+      return GDN_ERR_INVALID_ARG;
+  }
+  if (s->num_seqs > 0) {
+    if (!c.state_out || !aligned16(c.state_out)) return GDN_ERR_INVALID_ARG;
+    if (c.state_in && !aligned16(c.state_in)) return GDN_ERR_INVALID_ARG;
+    if (cu_required && !c.cu_seqlens) return GDN_ERR_INVALID_ARG;
+  }
+  if (c.cu_seqlens && (reinterpret_cast<uintptr_t>(c.cu_seqlens) & 3u)) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+size_t state_bytes(const gdn_shape *s) {
+  return (size_t)s->num_seqs * s->num_v_heads * s->dk * s->dv * sizeof(float);
+}
+
+gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes, void *stream) {
+  const gdn_shape *s = c.s;
+  ChunkParams p{};
+  p.num_seqs = s->num_seqs;
+  p.total_tokens = s->total_tokens;
+  p.hk = s->num_k_heads;
+  p.hv = s->num_v_heads;
+  p.chunk = s->chunk;
+  p.dtype = s->qkv_dtype;
+  p.q = c.q;
+  p.k = c.k;
+  p.v = c.v;
+  p.g = c.g;
+  p.beta = c.beta;
+  p.state_in = c.state_in;
+  p.state_out = c.state_out;
+  p.cu_seqlens = c.cu_seqlens;
+  p.o = c.o;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (s->qkv_dtype == GDN_F32) return cuda_status(gdn::launch_chunk_f32(p, st));
+  size_t off[4];
+  const size_t need = gdn::chunk_workspace_layout(s->total_tokens, s->num_v_heads, s->chunk, off);
+  if (need > 0 && (!workspace || workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return GDN_ERR_WORKSPACE;
+  char *ws = static_cast<char *>(workspace);
+  p.w_ws = ws + off[0];
+  p.u_ws = reinterpret_cast<float *>(ws + off[1]);
+  p.a_ws = ws + off[2];
+  p.g_ws = reinterpret_cast<float *>(ws + off[3]);
+  return cuda_status(gdn::launch_chunk_bf16(p, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_workspace_size(const gdn_shape *s, int op) {
+  if (op != GDN_OP_PREFILL && op != GDN_OP_DECODE && op != GDN_OP_VERIFY) return (size_t)-1;
+  const bool chunked = (op == GDN_OP_PREFILL || op == GDN_OP_VERIFY);
+  if (check_shape(s, chunked) != GDN_OK) return (size_t)-1;
+  if (!chunked || s->qkv_dtype == GDN_F32) return 0;
+  size_t off[4];
+  return gdn::chunk_workspace_layout(s->total_tokens, s->num_v_heads, s->chunk, off);
+}
+
+const char *gdn_status_string(gdn_status status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: null, misaligned or inconsistent argument";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: shape, dtype or block length not built";
+    case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS: state_in and state_out overlap in a way not allowed";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA call or kernel launch failed";
+  }
+  return "unknown gdn_status";
+}
+
+gdn_status gdn_prefill_chunked(const gdn_shape *shape, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const float *state_in, float *state_out,
+                               const int32_t *cu_seqlens, void *o, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+  gdn_status st = check_shape(shape, true);
+  if (st != GDN_OK) return st;
+  Common c{shape, q, k, v, g, beta, state_in, state_out, cu_seqlens, o};
+  if ((st = check_buffers(c, true)) != GDN_OK) return st;
+  if (state_in && partial_overlap(state_in, state_out, state_bytes(shape))) return GDN_ERR_ALIAS;
+  if (shape->num_seqs == 0) return GDN_OK;
+  return run_chunked(c, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_verify_block(const gdn_shape *shape, const void *q, const void *k,
+                            const void *v, const float *g, const float *beta,
+                            const float *state_in, float *state_out,
+                            const int32_t *cu_seqlens, void *o, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+  gdn_status st = check_shape(shape, true);
+  if (st != GDN_OK) return st;
+  Common c{shape, q, k, v, g, beta, state_in, state_out, cu_seqlens, o};
+  if ((st = check_buffers(c, true)) != GDN_OK) return st;
+  if (shape->num_seqs == 0) return GDN_OK;
+  if (!state_in) return GDN_ERR_INVALID_ARG;
+  const size_t n = state_bytes(shape);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(state_in), b = reinterpret_cast<uintptr_t>(state_out);
+  if (a < b + n && b < a + n) return GDN_ERR_ALIAS;
+  return run_chunked(c, workspace, workspace_bytes, stream);
+}
+
+gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k,
+                           const void *v, const float *g, const float *beta,
+                           const float *state_in, float *state_out,
+                           const int32_t *cu_seqlens, void *o, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  gdn_status st = check_shape(shape, false);
+  if (st != GDN_OK) return st;
+  Common c{shape, q, k, v, g, beta, state_in, state_out, cu_seqlens, o};
+  if ((st = check_buffers(c, false)) != GDN_OK) return st;
+  if (!cu_seqlens && shape->total_tokens != shape->num_seqs) return GDN_ERR_INVALID_ARG;
+  if (state_in && partial_overlap(state_in, state_out, state_bytes(shape))) return GDN_ERR_ALIAS;
+  if (shape->num_seqs == 0) return GDN_OK;
+  DecodeParams p{};
+  p.num_seqs = shape->num_seqs;
+  p.total_tokens = shape->total_tokens;
+  p.hk = shape->num_k_heads;
+  p.hv = shape->num_v_heads;
+  p.dtype = shape->qkv_dtype;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.g = g;
+  p.beta = beta;
+  p.state_in = state_in;
+  p.state_out = state_out;
+  p.cu_seqlens = cu_seqlens;
+  p.o = o;
+  return cuda_status(gdn::launch_decode(p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

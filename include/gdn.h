@@ -1,0 +1,147 @@
+/*
+ * libgdn: the gated delta-rule linear-attention layer on NVIDIA GB300 (sm_103a).
+ *
+ * The layer ("Qwen3.5-9B-npu" model card, section "How it works"): a per-head
+ * state S [dk x dv] (S[i][j]: i indexes the key, j the value) evolves per token
+ *
+ *     S <- S * exp(g_t)
+ *     kv = S^T k_t
+ *     S <- S + k_t (x) ((v_t - kv) * beta_t)
+ *     o_t = S^T q_t            (the output reads the updated state)
+ *
+ * Three entry points compute it:
+ *   gdn_prefill_chunked  prompt blocks in the chunkwise-parallel form of the same
+ *                        section (G = cumsum(g), strictly lower N, per-token deltas
+ *                        D = (I + N)^-1 diag(beta)(V - diag(exp G) K S0), block
+ *                        output O and carried state S_T);
+ *   gdn_decode_step      the token-by-token recurrence (the 1-token matrix form of
+ *                        that section: o = d q^T S + (q.k) delta, S' = d S + k delta^T);
+ *   gdn_verify_block     a prompt-lookup draft check from a state snapshot (section
+ *                        "New in v2", prompt lookup decoding: the state is snapshotted
+ *                        before the check, so the snapshot must stay untouched).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * Pointers are DEVICE pointers, row-major and contiguous, each 16-byte aligned
+ * (cu_seqlens: 4-byte aligned):
+ *     q, k          [total_tokens, Hk, dk]   qkv_dtype
+ *     v, o          [total_tokens, Hv, dv]   qkv_dtype
+ *     g, beta       [total_tokens, Hv]       float32 (g: log-decay, used as is)
+ *     state_in/out  [num_seqs, Hv, dk, dv]   float32
+ *     cu_seqlens    [num_seqs + 1]           int32, cu_seqlens[0] = 0, non-decreasing,
+ *                                            cu_seqlens[num_seqs] = total_tokens
+ * v-head h reads q/k head h / (Hv / Hk) (grouped heads; Hv % Hk == 0).
+ * Sequence n owns tokens [cu_seqlens[n], cu_seqlens[n+1]); blocks never cross a
+ * sequence boundary and a partly filled block behaves as if padded with g = 0,
+ * beta = 0 tokens (the page's token_valid rule), so the state after it is exactly
+ * the state after the sequence's last token.  A zero-length sequence copies its
+ * initial state to state_out.
+ * state_in == NULL means a zero initial state.  The library applies no 1/sqrt(dk)
+ * scale and no normalisation to q or k, and computes no gates: g and beta are inputs.
+ *
+ * Ownership and execution: the caller owns every buffer.  Calls enqueue work on
+ * `stream` (a cudaStream_t; NULL = the legacy default stream) and return without
+ * synchronising.  The library allocates no memory and keeps no state between calls;
+ * scratch memory, where an entry point needs it, is the caller's `workspace`
+ * (query its size with gdn_workspace_size).
+ *
+ * Errors: arguments are validated on the host before anything is launched; a bad
+ * argument returns its status and enqueues nothing.  A failed launch returns
+ * GDN_ERR_CUDA.  cu_seqlens lives on the device and is not read by the host: a
+ * malformed cu_seqlens (decreasing, or past total_tokens) cannot make a kernel read
+ * or write outside the buffers sized by `shape` (every range is clamped to
+ * [0, total_tokens]), but the results are then unspecified.  Faults raised later on
+ * the device surface at the caller's next synchronisation, as usual in CUDA.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,  /* null pointer, bad count, misaligned pointer   */
+  GDN_ERR_UNSUPPORTED = 2,  /* a shape, dtype or block length not built       */
+  GDN_ERR_ALIAS = 3,        /* state_in / state_out overlap not allowed       */
+  GDN_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required     */
+  GDN_ERR_CUDA = 5          /* a CUDA call or launch failed                   */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef enum { GDN_OP_PREFILL = 0, GDN_OP_DECODE = 1, GDN_OP_VERIFY = 2 } gdn_op;
+
+typedef struct {
+  int32_t num_seqs;      /* N >= 0                                                  */
+  int32_t total_tokens;  /* = cu_seqlens[N]; decode without cu_seqlens: = N         */
+  int32_t num_k_heads;   /* Hk: heads of q and k                                    */
+  int32_t num_v_heads;   /* Hv, a multiple of Hk: heads of v, g, beta, state and o  */
+  int32_t dk, dv;        /* head sizes; 128 and 128 are built                       */
+  int32_t chunk;         /* block length for prefill / verify: 16, 32 or 64        */
+  gdn_dtype qkv_dtype;   /* dtype of q, k, v and o: GDN_F32 or GDN_BF16             */
+} gdn_shape;
+
+/*
+ * Chunkwise-parallel prompt pass ("How it works", chunkwise form).
+ * Runs every sequence from state_in (or zero) through its tokens in blocks of
+ * shape->chunk, writes o for every token and the final state to state_out.
+ * state_out may equal state_in exactly (in-place update); any other overlap is
+ * GDN_ERR_ALIAS.  bf16 q/k/v: products on tensor cores with fp32 accumulation, the
+ * state kept in fp32.  f32 q/k/v: all arithmetic in fp32 on CUDA cores.
+ * workspace: at least gdn_workspace_size(shape, GDN_OP_PREFILL) bytes, 256-byte
+ * aligned (may be NULL when that size is 0); its contents on entry do not matter and
+ * are unspecified on return.
+ */
+gdn_status gdn_prefill_chunked(const gdn_shape *shape, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const float *state_in, float *state_out,
+                               const int32_t *cu_seqlens, void *o, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/*
+ * Token-by-token recurrence ("How it works", the per-token rule in its 1-token
+ * matrix form), one pass over each head's state per token.
+ * cu_seqlens == NULL: one token per sequence (total_tokens must equal num_seqs;
+ * token n belongs to sequence n) -- the decode step.  Otherwise each sequence runs
+ * through all its tokens in order.
+ * state_out may equal state_in exactly (in-place); other overlap is GDN_ERR_ALIAS.
+ * shape->chunk is ignored.  Needs no workspace (workspace may be NULL).
+ */
+gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k,
+                           const void *v, const float *g, const float *beta,
+                           const float *state_in, float *state_out,
+                           const int32_t *cu_seqlens, void *o, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * Draft-verify block ("New in v2", prompt lookup decoding): the chunkwise pass over
+ * each sequence's draft tokens, started from the snapshot state_in, which is left
+ * unchanged.  state_in must not be NULL and must not overlap state_out
+ * (GDN_ERR_ALIAS).  Writes per-token outputs o and the end-of-block state state_out.
+ * Draft blocks are normally at most shape->chunk tokens (one block per sequence);
+ * longer ones are processed in several blocks, as by gdn_prefill_chunked.
+ * workspace: gdn_workspace_size(shape, GDN_OP_VERIFY) bytes, as for prefill.
+ */
+gdn_status gdn_verify_block(const gdn_shape *shape, const void *q, const void *k,
+                            const void *v, const float *g, const float *beta,
+                            const float *state_in, float *state_out,
+                            const int32_t *cu_seqlens, void *o, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/* Workspace bytes `op` (a gdn_op) needs for `shape` (0 when none); (size_t)-1 for an
+ * invalid shape or op. */
+size_t gdn_workspace_size(const gdn_shape *shape, int op);
+
+/* Static, human-readable name of a status code. */
+const char *gdn_status_string(gdn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

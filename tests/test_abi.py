@@ -1,0 +1,113 @@
+"""The C-ABI library: it loads, exports every entry point the header declares, and
+rejects bad arguments on the host before launching anything.  No GPU needed: every
+call here fails validation (or is a pure query), so no kernel is ever launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_linear_05_gb300 as gdn
+from gated_deltanet_linear_05_gb300 import build as gdn_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    gdn_build.build()
+    return gdn.lib()
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:gdn_status|size_t|const char \*)\s*(gdn_\w+)\(", txt, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    assert set(_declared()) == set(gdn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert gdn.gdn_status_string(s).startswith(
+            ["GDN_OK", "GDN_ERR_INVALID_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_ALIAS",
+             "GDN_ERR_WORKSPACE", "GDN_ERR_CUDA"][s])
+
+
+def test_workspace_size(L):
+    sh = gdn.make_shape(8, 4096, 16, 32, chunk=64)
+    n = gdn.gdn_workspace_size(sh, gdn.GDN_OP_PREFILL)
+    rows = 4096 * 32
+    assert n >= rows * (128 * 2 + 128 * 4 + 64 * 2 + 4)
+    assert n == gdn.gdn_workspace_size(sh, gdn.GDN_OP_VERIFY)
+    assert gdn.gdn_workspace_size(sh, gdn.GDN_OP_DECODE) == 0
+    assert gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, chunk=16, dtype=gdn.GDN_F32),
+                                  gdn.GDN_OP_PREFILL) == 0
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, dk=64), gdn.GDN_OP_PREFILL)
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_workspace_size(sh, 7)
+
+
+# fake, well-aligned device addresses: every call below must fail validation first
+A = 0x10000000
+
+
+def _call(L, name, shape, q=A, k=A, v=A, g=A, beta=A, s_in=A + (1 << 24), s_out=A + (1 << 26),
+          cu=A, o=A, ws=None, ws_bytes=0):
+    fn = getattr(L, name)
+    return fn(ctypes.byref(shape) if shape is not None else None, q, k, v, g, beta, s_in, s_out,
+              cu, o, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("name", ["gdn_prefill_chunked", "gdn_verify_block", "gdn_decode_step"])
+def test_validation(L, name):
+    ok_shape = gdn.make_shape(2, 10, 1, 2, chunk=16)
+    assert _call(L, name, None) == gdn.GDN_ERR_INVALID_ARG
+    assert _call(L, name, gdn.make_shape(2, 10, 1, 2, dk=64)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _call(L, name, gdn.make_shape(2, 10, 2, 3)) == gdn.GDN_ERR_INVALID_ARG   # Hv % Hk
+    assert _call(L, name, gdn.make_shape(-1, 10, 1, 1)) == gdn.GDN_ERR_INVALID_ARG
+    assert _call(L, name, gdn.make_shape(2, 10, 1, 2, dtype=5)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _call(L, name, ok_shape, q=None) == gdn.GDN_ERR_INVALID_ARG
+    assert _call(L, name, ok_shape, o=None) == gdn.GDN_ERR_INVALID_ARG
+    assert _call(L, name, ok_shape, s_out=None) == gdn.GDN_ERR_INVALID_ARG
+    assert _call(L, name, ok_shape, v=A + 8) == gdn.GDN_ERR_INVALID_ARG            # misaligned
+    assert _call(L, name, ok_shape, s_in=A + 4) == gdn.GDN_ERR_INVALID_ARG
+    assert _call(L, name, ok_shape, cu=A + 2) == gdn.GDN_ERR_INVALID_ARG
+    # partial overlap of the two state buffers
+    assert _call(L, name, ok_shape, s_in=A, s_out=A + 4096) == gdn.GDN_ERR_ALIAS
+
+
+@pytest.mark.parametrize("name", ["gdn_prefill_chunked", "gdn_verify_block"])
+def test_chunked_validation(L, name):
+    assert _call(L, name, gdn.make_shape(2, 10, 1, 2, chunk=24)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _call(L, name, gdn.make_shape(2, 10, 1, 2, chunk=16), cu=None) == gdn.GDN_ERR_INVALID_ARG
+    sh = gdn.make_shape(2, 10, 1, 2, chunk=16)
+    need = gdn.gdn_workspace_size(sh, gdn.GDN_OP_PREFILL)
+    assert _call(L, name, sh, ws=None) == gdn.GDN_ERR_WORKSPACE
+    assert _call(L, name, sh, ws=A, ws_bytes=need - 1) == gdn.GDN_ERR_WORKSPACE
+    assert _call(L, name, sh, ws=A + 16, ws_bytes=need) == gdn.GDN_ERR_WORKSPACE  # not 256-aligned
+
+
+def test_verify_needs_a_separate_snapshot(L):
+    sh = gdn.make_shape(2, 10, 1, 2, chunk=16)
+    assert _call(L, "gdn_verify_block", sh, s_in=None) == gdn.GDN_ERR_INVALID_ARG
+    assert _call(L, "gdn_verify_block", sh, s_in=A, s_out=A) == gdn.GDN_ERR_ALIAS
+
+
+def test_decode_without_cu_seqlens_needs_one_token_per_sequence(L):
+    sh = gdn.make_shape(3, 4, 1, 1)
+    assert _call(L, "gdn_decode_step", sh, cu=None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(L):
+    sh = gdn.make_shape(0, 0, 1, 1, chunk=16)
+    for name in ("gdn_prefill_chunked", "gdn_verify_block", "gdn_decode_step"):
+        assert _call(L, name, sh, q=None, k=None, v=None, g=None, beta=None, s_in=None,
+                     s_out=None, cu=None, o=None) == gdn.GDN_OK

@@ -1,0 +1,219 @@
+"""GPU parity: libgdn's CUDA path against the float64 oracle on the same seeded inputs.
+
+Tolerances (max |x - ref| / rms(ref) over the whole tensor, o and the final state
+separately): 1e-4 for fp32 q/k/v, 2e-2 for bf16 q/k/v with fp32 g/beta/state.
+"""
+import numpy as np
+import pytest
+
+import gdn_inputs as gi
+import oracle
+from gdn_testlib import device_inputs, gpu_prefill, rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gated_deltanet_linear_05_gb300 import build
+    build.build()
+
+
+def _oracle(x, pairs=None):
+    return oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state0"],
+                            x["cu_seqlens"], pairs=pairs)
+
+
+def _check(o, s, o_ref, s_ref, dtype, what=""):
+    eo, es = rel_err(o, o_ref), rel_err(s, s_ref)
+    assert np.isfinite(o).all() and np.isfinite(s).all(), what
+    assert eo <= TOL[dtype], "%s o err %.3g" % (what, eo)
+    assert es <= TOL[dtype], "%s state err %.3g" % (what, es)
+    return eo, es
+
+
+# ------------------------------------------------------------------ chunked prefill
+
+def test_chunk_vs_sequential_fp32_T64_C16():
+    wl = gi.chunk_vs_sequential_fp32()
+    x = gi.make_inputs(wl)
+    o, s, _ = gpu_prefill(x, wl, state_in=False)
+    o_ref, s_ref = _oracle(x)
+    _check(o, s, o_ref, s_ref, "f32")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("lengths,hk,hv", [
+    ([1], 1, 1), ([2], 1, 1), ([15], 1, 2), ([16], 2, 2), ([17], 1, 1),
+    ([63, 64, 65], 1, 2), ([200, 3, 129], 2, 4), ([0, 70, 0, 1], 1, 1)])
+def test_prefill_small_shapes(dtype, chunk, lengths, hk, hv):
+    wl = gi.Workload("small", lengths, hk, hv, chunk=chunk, dtype=dtype, s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=len(lengths) + chunk)
+    o, s, _ = gpu_prefill(x, wl)
+    o_ref, s_ref = _oracle(x)
+    _check(o, s, o_ref, s_ref, dtype, "T=%s C=%d" % (lengths, chunk))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_prefill_zero_initial_state_and_in_place(dtype):
+    wl = gi.Workload("small", [37, 90], 2, 2, chunk=32, dtype=dtype, s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=7)
+    o_ref, s_ref = _oracle(x)
+    o, s, _ = gpu_prefill(x, wl, inplace=True)
+    _check(o, s, o_ref, s_ref, dtype, "in place")
+    x0 = dict(x, state0=None)
+    o_ref0, s_ref0 = _oracle(x0)
+    o0, s0, _ = gpu_prefill(x0, wl, state_in=False)
+    _check(o0, s0, o_ref0, s_ref0, dtype, "zero state")
+
+
+def test_prefill_slow_decay_bf16():
+    """g = -0.01 softplus(.): the state carries across many blocks."""
+    wl = gi.Workload("slow", [1000], 1, 2, chunk=64, dtype="bf16", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=11, gate_scale=0.01)
+    o, s, _ = gpu_prefill(x, wl)
+    o_ref, s_ref = _oracle(x)
+    _check(o, s, o_ref, s_ref, "bf16", "slow decay")
+
+
+def test_prefill_T4096_H16_full():
+    wl = gi.prefill_t4096_h16()
+    x = gi.make_inputs(wl)
+    o, s, _ = gpu_prefill(x, wl)
+    o_ref, s_ref = _oracle(x)
+    _check(o, s, o_ref, s_ref, "bf16", "T=4096")
+
+
+@pytest.mark.slow
+def test_varlen_N8_Hk16_Hv32_sampled():
+    wl = gi.varlen_8seq_hk16_hv32()
+    x = gi.make_inputs(wl)
+    o, s, _ = gpu_prefill(x, wl)
+    rng = np.random.default_rng(0)
+    pairs = [(n, int(h)) for n in range(8) for h in rng.choice(32, 2, replace=False)]
+    o_ref, s_ref = _oracle(x, pairs=pairs)
+    cu = x["cu_seqlens"]
+    for n, h in pairs:
+        sl = slice(cu[n], cu[n + 1])
+        _check(o[sl, h], s[n, h], o_ref[sl, h], s_ref[n, h], "bf16", "seq %d head %d" % (n, h))
+
+
+# ------------------------------------------------------------------ verify
+
+def test_verify_B128_H32_T16_full():
+    import torch
+    wl = gi.verify_b128_h32()
+    x = gi.make_inputs(wl)
+    d = device_inputs(x, "bf16")
+    snap = d["state0"].clone()
+    s_out = torch.empty_like(snap)
+    import gated_deltanet_linear_05_gb300 as gdn
+    o, s = gdn.gdn_verify_block(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
+                                d["cu_seqlens"], chunk=16)
+    torch.cuda.synchronize()
+    assert torch.equal(d["state0"], snap)  # the snapshot is untouched, bit for bit
+    o_ref, s_ref = _oracle(x)
+    _check(to_np(o), to_np(s), o_ref, s_ref, "bf16", "verify")
+
+
+# ------------------------------------------------------------------ decode
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_one_token_per_sequence(dtype):
+    import torch
+    import gated_deltanet_linear_05_gb300 as gdn
+    wl = gi.Workload("dec", [1] * 5, 1, 3, dtype=dtype, s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=2)
+    d = device_inputs(x, dtype)
+    s_out = torch.empty_like(d["state0"])
+    o, s = gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out)
+    torch.cuda.synchronize()
+    o_ref, s_ref = _oracle(x)
+    _check(to_np(o), to_np(s), o_ref, s_ref, dtype, "decode")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_token_loop_varlen(dtype):
+    """With cu_seqlens the decode kernel walks every sequence token by token."""
+    import torch
+    import gated_deltanet_linear_05_gb300 as gdn
+    wl = gi.Workload("loop", [40, 0, 3, 17], 2, 4, dtype=dtype, s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=5)
+    d = device_inputs(x, dtype)
+    s_out = torch.empty_like(d["state0"])
+    o, s = gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
+                               d["cu_seqlens"])
+    torch.cuda.synchronize()
+    o_ref, s_ref = _oracle(x)
+    _check(to_np(o), to_np(s), o_ref, s_ref, dtype, "decode loop")
+
+
+def test_decode_B32_H16_100_steps_in_place():
+    """100 consecutive in-place steps; the oracle runs the same 100 tokens per sequence
+    as one chain in float64."""
+    import torch
+    import gated_deltanet_linear_05_gb300 as gdn
+    wl = gi.decode_b32_h16()
+    steps = [gi.make_inputs(wl, step=s) for s in range(wl.steps)]
+    state = device_inputs(steps[0], "bf16")["state0"]
+    outs = []
+    for xs in steps:
+        d = device_inputs(xs, "bf16")
+        o, _ = gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], state, state)
+        outs.append(o)
+    torch.cuda.synchronize()
+    o_gpu = np.stack([to_np(o) for o in outs], axis=1)          # [N, steps, H, dv]
+    # oracle: sequence n = its 100 tokens in step order
+    cat = {}
+    for name in ("q", "k", "v", "g", "beta"):
+        cat[name] = np.stack([xs[name] for xs in steps], axis=1).reshape(
+            (wl.num_seqs * wl.steps,) + steps[0][name].shape[1:])
+    cu = np.arange(0, wl.num_seqs * wl.steps + 1, wl.steps, dtype=np.int32)
+    o_ref, s_ref = oracle.recurrent(cat["q"], cat["k"], cat["v"], cat["g"], cat["beta"],
+                                    steps[0]["state0"], cu)
+    o_ref = o_ref.reshape(wl.num_seqs, wl.steps, wl.num_v_heads, wl.dv)
+    _check(o_gpu, to_np(state), o_ref, s_ref, "bf16", "100 steps")
+
+
+# ------------------------------------------------------------------ self-consistency
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chunked_matches_gpu_decode_loop(dtype):
+    import torch
+    import gated_deltanet_linear_05_gb300 as gdn
+    wl = gi.Workload("cons", [64, 130, 16], 1, 2, chunk=16, dtype=dtype, s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=9)
+    o_c, s_c, d = gpu_prefill(x, wl)
+    s_out = torch.empty_like(d["state0"])
+    o_d, s_d = gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"],
+                                   s_out, d["cu_seqlens"])
+    torch.cuda.synchronize()
+    _check(o_c, s_c, to_np(o_d), to_np(s_d), dtype, "chunked vs decode loop")
+
+
+def test_chunk16_matches_chunk64_bf16():
+    wl = gi.Workload("c", [300, 77], 2, 2, dtype="bf16", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=4)
+    o16, s16, _ = gpu_prefill(x, wl, chunk=16)
+    o64, s64, _ = gpu_prefill(x, wl, chunk=64)
+    _check(o16, s16, o64, s64, "bf16", "C16 vs C64")
+
+
+def test_varlen_packed_matches_separate_runs_bf16():
+    lengths = [100, 5, 64]
+    wl = gi.Workload("v", lengths, 1, 2, chunk=64, dtype="bf16", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=3)
+    o, s, _ = gpu_prefill(x, wl)
+    cu = x["cu_seqlens"]
+    for n, L in enumerate(lengths):
+        a, b = cu[n], cu[n + 1]
+        xs = {k: x[k][a:b] for k in ("q", "k", "v", "g", "beta", "q_st", "k_st", "v_st")}
+        xs["state0"] = x["state0"][n:n + 1]
+        xs["cu_seqlens"] = np.array([0, L], np.int32)
+        wl1 = gi.Workload("v1", [L], 1, 2, chunk=64, dtype="bf16")
+        o1, s1, _ = gpu_prefill(xs, wl1)
+        np.testing.assert_array_equal(o1, o[a:b])
+        np.testing.assert_array_equal(s1[0], s[n])
