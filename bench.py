@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Benchmark of libgdn (gated delta-rule layer) on GB300; prints ONE JSON line.
+
+Headline: chunked prefill tokens/s on the single-sequence workload (B=1, H=16,
+T=4096, chunk 64, bf16 q/k/v, fp32 g/beta/state).  One step = one
+gdn_prefill_chunked call over that batch (the prompt path: block bookkeeping,
+cumsum, Grams, triangular solve, block output and state carry).  The same line
+carries the other rows of the path measured the same way: the decode step
+(32 x 16 heads, state GB/s), the draft-verify block (128 x 32 heads, T=16) and
+packed varlen prefill (8 sequences, Hk=16 / Hv=32).
+
+Timing: CUDA events on the launching stream, L2 flushed (a 512 MiB write)
+before every timed step and outside the events; decode rotates over 8 state
+sets (268 MB > 2x L2) so each step streams its state from HBM.
+
+--impl reference times the float64 CPU oracle (the reference arm of this build)
+on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s (%TC roofline); decode state GB/s (%HBM peak)"
+D = 128
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        j = json.load(open(p))
+        return {"hbm": float(j["hbm_gbs"]), "bf16": float(j["bf16_tflops"]),
+                "bf16_sustained": float(j["bf16_tflops_sustained"]), "source": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def prefill_work(lengths, hk, hv, chunk, s_qk=2, s_v=2):
+    """(flops, bytes) the method itself must do / move for a prefill batch."""
+    T = sum(lengths)
+    flops = T * (hk * 2 * chunk * D + hv * (6 * D * D + 2 * chunk * D))
+    byts = T * (hk * 2 * D * s_qk + hv * (2 * D * s_v + 8)) + len(lengths) * hv * 2 * D * D * 4
+    return flops, byts
+
+
+def decode_bytes(n, hv, hk, s=2):
+    """State read + write, q/k (per k-head), v, o, g, beta for one decode step."""
+    return n * hv * (2 * D * D * 4 + 2 * D * s + 8) + n * hk * 2 * D * s
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    """nvidia-smi samples (every 100 ms) while the timed regions run."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        mhz = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dev_inputs(x, torch, device):
+    import numpy as np
+
+    def t(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return {"q": t(x["q_st"]), "k": t(x["k_st"]), "v": t(x["v_st"]), "g": t(x["g"]),
+            "beta": t(x["beta"]), "state0": t(x["state0"]), "cu": t(x["cu_seqlens"])}
+
+
+def timed_steps(torch, fn, steps, warmup, flush=None):
+    """Per-step CUDA-event times (ms) on the current stream, L2 flushed between steps."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for i in range(steps):
+        if flush is not None:
+            flush(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def roofline(bound, achieved, peak, unit, traffic=None):
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gdn(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import gdn_inputs as gi
+    import gated_deltanet_linear_05_gb300 as gdn
+    from gated_deltanet_linear_05_gb300 import build as gdn_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    gdn_build.build()
+    gdn.lib()
+    pk = peaks()
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+
+    def flush(i):
+        flush_buf.fill_(i & 0xFF)
+
+    def barrier_max(ms):
+        if world > 1:
+            t = torch.tensor([ms], device=device)
+            dist.barrier()
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return ms
+
+    clocks = Clocks(local)
+    out = {}
+
+    # ---- headline: prefill B=1, H=16, T=4096, C=64
+    wl = gi.prefill_t4096_h16()
+    x = gi.make_inputs(wl)
+    d = dev_inputs(x, torch, device)
+    N, Hk, Hv, C = wl.num_seqs, wl.num_k_heads, wl.num_v_heads, wl.chunk
+    s_out = torch.empty_like(d["state0"])
+    o = torch.empty_like(d["v"])
+    shape = gdn.make_shape(N, wl.total_tokens, Hk, Hv, chunk=C)
+    ws = torch.empty(gdn.gdn_workspace_size(shape, gdn.GDN_OP_PREFILL) + 256, dtype=torch.uint8,
+                     device=device)
+
+    def step():
+        gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
+                                d["cu"], o, chunk=C, workspace=ws)
+
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    times = timed_steps(torch, step, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    ms = barrier_max(statistics.mean(times))
+    flops, byts = prefill_work(wl.lengths, Hk, Hv, C)
+    tok_s = world * wl.total_tokens / (ms * 1e-3)
+    gbs = byts / (ms * 1e-3) / 1e9
+    tfs = flops / (ms * 1e-3) / 1e12
+
+    # e2e through the C-ABI from pinned host buffers
+    host = {k: v.cpu().pin_memory() for k, v in d.items() if v is not None}
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    s_h = torch.empty(s_out.shape, dtype=s_out.dtype).pin_memory()
+    bufs = {k: torch.empty_like(v) for k, v in d.items() if v is not None}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = o_h.numel() * o_h.element_size() + s_h.numel() * s_h.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            bufs[k].copy_(v, non_blocking=True)
+        gdn.gdn_prefill_chunked(bufs["q"], bufs["k"], bufs["v"], bufs["g"], bufs["beta"],
+                                bufs["state0"], s_out, bufs["cu"], o, chunk=C, workspace=ws)
+        o_h.copy_(o, non_blocking=True)
+        s_h.copy_(s_out, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    e2e_times = timed_steps(torch, e2e_step, e2e_steps, 2, flush)
+    e2e_ms = barrier_max(statistics.mean(e2e_times))
+
+    if not args.no_extra:
+        out["decode"] = bench_decode(torch, gdn, gi, device, pk, args)
+        out["verify"] = bench_verify(torch, gdn, gi, device, pk, args, flush)
+        out["varlen"] = bench_varlen(torch, gdn, gi, device, pk, args, flush)
+    clk = clocks.stop()
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "num_seqs": N, "seq_len": wl.total_tokens,
+                   "num_k_heads": Hk, "num_v_heads": Hv, "dk": D, "dv": D, "chunk": C,
+                   "qkv": "bf16", "g_beta_state": "fp32",
+                   "l2": "flushed (512 MiB write) before every timed step",
+                   "parallelism": "dp%d (independent batches per GPU)" % world},
+        "roofline": roofline("hbm", gbs, pk["hbm"], "GB/s"),
+        "tensor": {"achieved": round(tfs, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                   "frac": round(tfs / pk["bf16"], 4), "algorithmic_flops": flops},
+        "algorithmic_bytes": byts,
+        "peaks_source": pk["source"],
+        "e2e": {"value": round(world * wl.total_tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    line.update(out)
+    line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+def bench_decode(torch, gdn, gi, device, pk, args):
+    """Decode step, 32 sequences x 16 heads; 8 state sets rotated (268 MB > 2x L2)."""
+    wl = gi.decode_b32_h16()
+    R, steps = 8, 100
+    sets = []
+    for r in range(R):
+        x = gi.make_inputs(wl, seed=r, step=0)
+        sets.append(dev_inputs(x, torch, device))
+    o = torch.empty_like(sets[0]["v"])
+
+    def one(i):
+        s = sets[i % R]
+        gdn.gdn_decode_step(s["q"], s["k"], s["v"], s["g"], s["beta"], s["state0"], s["state0"],
+                            None, o)
+
+    for i in range(2 * R):
+        one(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(steps):
+        one(i)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    # the same 100 steps on one state set (state stays in L2): context only
+    a.record()
+    for i in range(steps):
+        one(0)
+    b.record()
+    torch.cuda.synchronize()
+    ms_res = a.elapsed_time(b) / steps
+    byts = decode_bytes(wl.num_seqs, wl.num_v_heads, wl.num_k_heads)
+    state_b = wl.num_seqs * wl.num_v_heads * 2 * D * D * 4
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"workload": wl.name + "_x100steps", "us_per_step": round(ms * 1e3, 3),
+            "state_GBps": round(state_b / (ms * 1e-3) / 1e9, 1),
+            "roofline": roofline("hbm", gbs, pk["hbm"], "GB/s"),
+            "bytes_per_step": byts, "l2": "8 state sets rotated (268 MB)",
+            "us_per_step_l2_resident": round(ms_res * 1e3, 3), "gpu_launches": steps}
+
+
+def bench_verify(torch, gdn, gi, device, pk, args, flush):
+    wl = gi.verify_b128_h32()
+    x = gi.make_inputs(wl)
+    d = dev_inputs(x, torch, device)
+    s_out = torch.empty_like(d["state0"])
+    o = torch.empty_like(d["v"])
+    shape = gdn.make_shape(wl.num_seqs, wl.total_tokens, wl.num_k_heads, wl.num_v_heads, chunk=16)
+    ws = torch.empty(gdn.gdn_workspace_size(shape, gdn.GDN_OP_VERIFY) + 256, dtype=torch.uint8,
+                     device=device)
+
+    def step():
+        gdn.gdn_verify_block(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
+                             d["cu"], o, chunk=16, workspace=ws)
+
+    n = max(5, min(args.steps, 50))
+    ms = statistics.mean(timed_steps(torch, step, n, 3, flush))
+    flops, byts = prefill_work(wl.lengths, wl.num_k_heads, wl.num_v_heads, 16)
+    return {"workload": wl.name, "us_per_step": round(ms * 1e3, 2),
+            "tokens_per_s": round(wl.total_tokens / (ms * 1e-3), 1),
+            "roofline": roofline("hbm", byts / (ms * 1e-3) / 1e9, pk["hbm"], "GB/s"),
+            "algorithmic_bytes": byts, "gpu_launches": 2 * n}
+
+
+def bench_varlen(torch, gdn, gi, device, pk, args, flush):
+    wl = gi.varlen_8seq_hk16_hv32()
+    x = gi.make_inputs(wl)
+    d = dev_inputs(x, torch, device)
+    s_out = torch.empty_like(d["state0"])
+    o = torch.empty_like(d["v"])
+    shape = gdn.make_shape(wl.num_seqs, wl.total_tokens, wl.num_k_heads, wl.num_v_heads, chunk=64)
+    ws = torch.empty(gdn.gdn_workspace_size(shape, gdn.GDN_OP_PREFILL) + 256, dtype=torch.uint8,
+                     device=device)
+
+    def step():
+        gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
+                                d["cu"], o, chunk=64, workspace=ws)
+
+    n = max(5, min(args.steps, 30))
+    ms = statistics.mean(timed_steps(torch, step, n, 3, flush))
+    flops, byts = prefill_work(wl.lengths, wl.num_k_heads, wl.num_v_heads, 64)
+    return {"workload": wl.name, "lengths": wl.lengths, "us_per_step": round(ms * 1e3, 2),
+            "tokens_per_s": round(wl.total_tokens / (ms * 1e-3), 1),
+            "roofline": roofline("hbm", byts / (ms * 1e-3) / 1e9, pk["hbm"], "GB/s"),
+            "tensor_frac": round(flops / (ms * 1e-3) / 1e12 / pk["bf16"], 4),
+            "gpu_launches": 2 * n}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(threads):
+    """The prefill workload's inputs and a sample of (sequence, head) chains, one per thread."""
+    import gdn_inputs as gi
+    wl = gi.prefill_t4096_h16()
+    x = gi.make_inputs(wl)
+    chains = min(wl.num_v_heads, threads)
+    pairs = [(0, h) for h in range(chains)]
+    return wl, x, pairs
+
+
+def cpu_baseline(seconds):
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    wl, x, pairs = oracle_sample(threads)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state0"], x["cu_seqlens"],
+                         pairs=pairs, threads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 100:
+            break
+    tokens = reps * wl.total_tokens * len(pairs) / wl.num_v_heads
+    return {"value": round(tokens / el, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of the %d heads of %s (full T), %d repetitions, %.1f s, float64 per-token "
+                      "recurrence" % (len(pairs), wl.num_v_heads, wl.name, reps, el)}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    wl, x, pairs = oracle_sample(threads)
+
+    def step():
+        oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state0"], x["cu_seqlens"],
+                         pairs=pairs, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    # bound the whole run to about two minutes
+    t0 = time.perf_counter()
+    step()
+    one = time.perf_counter() - t0
+    steps = max(1, min(args.steps, int(120.0 / max(one, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    el = time.perf_counter() - t0
+    ms = el / steps * 1e3
+    tok_step = wl.total_tokens * len(pairs) / wl.num_v_heads
+    val = round(tok_step / (ms * 1e-3), 1)
+    sample = ("%d of the %d heads of %s (full T) per step, float64 per-token recurrence, %d steps"
+              % (len(pairs), wl.num_v_heads, wl.name, steps))
+    return {"metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "num_seqs": 1, "seq_len": wl.total_tokens,
+                       "num_k_heads": wl.num_k_heads, "num_v_heads": wl.num_v_heads, "dk": D,
+                       "dv": D, "chunk": wl.chunk, "sample": sample},
+            "impl": "reference",
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    line = run_reference(args) if args.impl == "reference" else run_gdn(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -44,7 +44,8 @@ class GdnShape(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
                 ("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
-                ("chunk", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32)]
+                ("chunk", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32),
+                ("o_fp32", ctypes.c_int32)]
 
 
 _lib = None
@@ -78,8 +79,9 @@ def gdn_status_string(status: int) -> str:
 
 
 def make_shape(num_seqs: int, total_tokens: int, num_k_heads: int, num_v_heads: int,
-               dk: int = 128, dv: int = 128, chunk: int = 64, dtype: int = GDN_BF16) -> GdnShape:
-    return GdnShape(num_seqs, total_tokens, num_k_heads, num_v_heads, dk, dv, chunk, dtype)
+               dk: int = 128, dv: int = 128, chunk: int = 64, dtype: int = GDN_BF16,
+               o_fp32: int = 0) -> GdnShape:
+    return GdnShape(num_seqs, total_tokens, num_k_heads, num_v_heads, dk, dv, chunk, dtype, o_fp32)
 
 
 def gdn_workspace_size(shape: GdnShape, op: int) -> int:
@@ -109,11 +111,16 @@ def _dtype_code(t) -> int:
     raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
 
 
-def _shape_of(q, v, state_out, cu_seqlens, chunk: int) -> GdnShape:
+def _shape_of(q, v, o, state_out, cu_seqlens, chunk: int) -> GdnShape:
+    """Shape from the tensors; o may be float32 while q/k/v are bf16 (o_fp32 = 1)."""
     T, hk, dk = q.shape
     hv, dv = v.shape[1], v.shape[2]
     n = state_out.shape[0] if state_out is not None else (len(cu_seqlens) - 1)
-    return make_shape(n, T, hk, hv, dk, dv, chunk, _dtype_code(q))
+    code = _dtype_code(q)
+    o_fp32 = int(code == GDN_BF16 and _dtype_code(o) == GDN_F32)
+    if code == GDN_F32 and _dtype_code(o) != GDN_F32:
+        raise TypeError("o must be float32 when q/k/v are float32")
+    return make_shape(n, T, hk, hv, dk, dv, chunk, code, o_fp32)
 
 
 def _check_tensors(*ts):
@@ -143,7 +150,7 @@ def _workspace(shape: GdnShape, op: int, device, workspace):
 def _call(name, op, q, k, v, g, beta, state_in, state_out, cu_seqlens, o, chunk,
           workspace, stream):
     _check_tensors(q, k, v, g, beta, state_in, state_out, cu_seqlens, o, workspace)
-    shape = _shape_of(q, v, state_out, cu_seqlens, chunk)
+    shape = _shape_of(q, v, o, state_out, cu_seqlens, chunk)
     ws_ptr, ws_bytes = _workspace(shape, op, q.device, workspace)
     st = getattr(lib(), name)(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                               _ptr(beta), _ptr(state_in), _ptr(state_out), _ptr(cu_seqlens),

@@ -11,16 +11,20 @@
 //   pass 1 (prep_kernel, every block of every head in parallel): G, the decay-masked
 //     Grams, T by exact block doubling in fp32 (16x16 diagonal blocks by forward
 //     substitution, then (D + C)^-1 = D^-1 - D^-1 C D^-1 on 16 -> 32 -> 64), and the
-//     products W, U on tensor cores (T split into a bf16 high and low part, so the
-//     product keeps ~16 mantissa bits of T).  Writes W (bf16), U (fp32), the masked
-//     causal A (bf16) and G (fp32) to the workspace, indexed by token.
+//     products W, U on tensor cores.  Writes W, U (fp32), the masked causal A and G
+//     (fp32) to the workspace, indexed by token.
 //   pass 2 (recur_kernel, one CTA per (sequence, v-head, DVB value columns)): walks the
 //     blocks of the sequence in order with the state block S[:, cols] in fp32 registers
 //     (read from state_in once, written to state_out once):
 //       D^T = U^T - S^T W^T,  O^T = exp(G) (S^T Q^T) + D^T A^T,
 //       S^T <- exp(G_T) S^T + (D^T diag(exp(G_T - G))) K
-//     all on mma.sync tensor cores with fp32 accumulation; the state is rounded to bf16
-//     only as an MMA operand.
+//     all on mma.sync tensor cores with fp32 accumulation.
+// Precision: q, k, v are bf16 inputs and enter the products exactly.  Every other MMA
+// operand (T, W, A, the state, D) is an fp32 value x carried as two bf16 numbers,
+// hi = bf16(x) and lo = bf16(x - hi), and a product x*y is formed as hi*hi + lo*hi +
+// hi*lo (or hi*y + lo*y when y is an input), which keeps ~16 significant bits: the
+// layer's outputs have heavy tails (max/rms above 10), so single-bf16 intermediates
+// would put errors of a few 1e-2 of the rms on the largest entries.
 // Decay factors between two tokens are always the exp of a difference of cumsums.  A
 // partly filled block is padded with g = 0, beta = 0, zero q/k/v rows (token_valid),
 // which leaves the state exactly as after the sequence's last token.
@@ -73,8 +77,10 @@ __global__ void __launch_bounds__(2 * C) prep_kernel(ChunkParams p, int slots) {
   const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
   const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
-  __nv_bfloat16 *w_ws = static_cast<__nv_bfloat16 *>(p.w_ws);
-  __nv_bfloat16 *a_ws = static_cast<__nv_bfloat16 *>(p.a_ws);
+  __nv_bfloat16 *w_hi = static_cast<__nv_bfloat16 *>(p.w_hi);
+  __nv_bfloat16 *w_lo = static_cast<__nv_bfloat16 *>(p.w_lo);
+  __nv_bfloat16 *a_hi = static_cast<__nv_bfloat16 *>(p.a_hi);
+  __nv_bfloat16 *a_lo = static_cast<__nv_bfloat16 *>(p.a_lo);
 
   int bos, eos;
   seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
@@ -172,11 +178,16 @@ __global__ void __launch_bounds__(2 * C) prep_kernel(ChunkParams p, int slots) {
               sN[t][j + 1] = (j + 1 < t) ? sm.B[t] * d1 * x1 : 0.f;
             } else if (t < L) {
               const float a0 = (j <= t) ? d0 * x0 : 0.f, a1 = (j + 1 <= t) ? d1 * x1 : 0.f;
-              *reinterpret_cast<uint32_t *>(a_ws + ((size_t)h * T + tok0 + t) * C + j) =
-                  pack_bf16(a0, a1);
+              uint32_t hi, lo;
+              split_bf16(a0, a1, hi, lo);
+              const size_t at = ((size_t)h * T + tok0 + t) * C + j;
+              *reinterpret_cast<uint32_t *>(a_hi + at) = hi;
+              *reinterpret_cast<uint32_t *>(a_lo + at) = lo;
             }
           } else if (prod == 1 && t < L) {
-            *reinterpret_cast<uint32_t *>(a_ws + ((size_t)h * T + tok0 + t) * C + j) = 0u;
+            const size_t at = ((size_t)h * T + tok0 + t) * C + j;
+            *reinterpret_cast<uint32_t *>(a_hi + at) = 0u;
+            *reinterpret_cast<uint32_t *>(a_lo + at) = 0u;
           }
         }
       }
@@ -290,12 +301,15 @@ __global__ void __launch_bounds__(2 * C) prep_kernel(ChunkParams p, int slots) {
             const int col = n0 + 8 * nt + 2 * tig;
             if (t < L) {
               const size_t row = ((size_t)h * T + tok0 + t) * kD + col;
-              if (isU)
+              if (isU) {
                 *reinterpret_cast<float2 *>(p.u_ws + row) =
                     make_float2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
-              else
-                *reinterpret_cast<uint32_t *>(w_ws + row) =
-                    pack_bf16(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+              } else {
+                uint32_t hi, lo;
+                split_bf16(acc[nt][2 * hr], acc[nt][2 * hr + 1], hi, lo);
+                *reinterpret_cast<uint32_t *>(w_hi + row) = hi;
+                *reinterpret_cast<uint32_t *>(w_lo + row) = lo;
+              }
             }
           }
         }
@@ -307,48 +321,61 @@ __global__ void __launch_bounds__(2 * C) prep_kernel(ChunkParams p, int slots) {
 
 // ================================================================== pass 2
 
-template <int C, int DVB>
+template <int C, int DVB, typename TO>
 struct RecSmem {
   struct Stage {
-    alignas(128) char W[C * kRowB];
+    alignas(128) char Wh[C * kRowB];
+    alignas(128) char Wl[C * kRowB];
     alignas(128) char Q[C * kRowB];
     alignas(128) char K[C * kRowB];
-    alignas(128) char A[C * 2 * C];
+    alignas(128) char Ah[C * 2 * C];
+    alignas(128) char Al[C * 2 * C];
     alignas(16) float U[C][DVB];
     alignas(16) float G[C];
   } st[2];
-  alignas(128) char S[DVB * kRowB];   // S^T as a bf16 operand, [DVB][128]
-  alignas(128) char D[DVB * 2 * C];   // D^T, [DVB][C]
-  alignas(128) char Dt[DVB * 2 * C];  // (diag(exp(G_T - G)) D)^T
-  alignas(16) __nv_bfloat16 O[C][DVB];
+  alignas(128) char Sh[DVB * kRowB];   // S^T as bf16 operands (hi, lo), [DVB][128]
+  alignas(128) char Sl[DVB * kRowB];
+  alignas(128) char Dh[DVB * 2 * C];   // D^T (hi, lo), [DVB][C]
+  alignas(128) char Dl[DVB * 2 * C];
+  alignas(128) char Th[DVB * 2 * C];   // (diag(exp(G_T - G)) D)^T (hi, lo)
+  alignas(128) char Tl[DVB * 2 * C];
+  alignas(16) TO O[C][DVB];            // output staging
   alignas(16) float S32[kD][DVB + 4];  // fp32 staging of the state block
 };
 
-template <int C, int DVB>
-__device__ __forceinline__ void load_stage(typename RecSmem<C, DVB>::Stage &st,
+template <int C, int DVB, typename TO>
+__device__ __forceinline__ void load_stage(typename RecSmem<C, DVB, TO>::Stage &st,
                                            const ChunkParams &p, int h, int kh, int blk,
                                            int tok0, int L) {
   constexpr int RB = 2 * C;
   const size_t T = (size_t)p.total_tokens;
   const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
-  const __nv_bfloat16 *w_ws = static_cast<const __nv_bfloat16 *>(p.w_ws);
-  const __nv_bfloat16 *a_ws = static_cast<const __nv_bfloat16 *>(p.a_ws);
+  const __nv_bfloat16 *w_hi = static_cast<const __nv_bfloat16 *>(p.w_hi);
+  const __nv_bfloat16 *w_lo = static_cast<const __nv_bfloat16 *>(p.w_lo);
+  const __nv_bfloat16 *a_hi = static_cast<const __nv_bfloat16 *>(p.a_hi);
+  const __nv_bfloat16 *a_lo = static_cast<const __nv_bfloat16 *>(p.a_lo);
   const int tid = threadIdx.x;
   for (int e = tid; e < C * 16; e += 128) {
     const int r = e >> 4, gr = e & 15;
     const bool ok = r < L;
     const size_t tok = (size_t)tok0 + (ok ? r : 0);
     const int nb = ok ? 16 : 0;
-    cp_async16(st.W + swz<kRowB>(r, gr * 16), w_ws + ((size_t)h * T + tok) * kD + gr * 8, nb);
-    cp_async16(st.Q + swz<kRowB>(r, gr * 16), q + (tok * p.hk + kh) * kD + gr * 8, nb);
-    cp_async16(st.K + swz<kRowB>(r, gr * 16), k + (tok * p.hk + kh) * kD + gr * 8, nb);
+    const int so = swz<kRowB>(r, gr * 16);
+    const size_t wrow = ((size_t)h * T + tok) * kD + gr * 8;
+    cp_async16(st.Wh + so, w_hi + wrow, nb);
+    cp_async16(st.Wl + so, w_lo + wrow, nb);
+    cp_async16(st.Q + so, q + (tok * p.hk + kh) * kD + gr * 8, nb);
+    cp_async16(st.K + so, k + (tok * p.hk + kh) * kD + gr * 8, nb);
   }
   for (int e = tid; e < C * (C / 8); e += 128) {
     const int r = e / (C / 8), gr = e % (C / 8);
     const bool ok = r < L;
     const size_t tok = (size_t)tok0 + (ok ? r : 0);
-    cp_async16(st.A + swz<RB>(r, gr * 16), a_ws + ((size_t)h * T + tok) * C + gr * 8, ok ? 16 : 0);
+    const int so = swz<RB>(r, gr * 16);
+    const size_t arow = ((size_t)h * T + tok) * C + gr * 8;
+    cp_async16(st.Ah + so, a_hi + arow, ok ? 16 : 0);
+    cp_async16(st.Al + so, a_lo + arow, ok ? 16 : 0);
   }
   for (int e = tid; e < C * (DVB / 4); e += 128) {
     const int r = e / (DVB / 4), gr = e % (DVB / 4);
@@ -363,10 +390,10 @@ __device__ __forceinline__ void load_stage(typename RecSmem<C, DVB>::Stage &st,
   }
 }
 
-template <int C, int DVB>
+template <int C, int DVB, typename TO>
 __global__ void __launch_bounds__(128) recur_kernel(ChunkParams p) {
   constexpr int NB = kD / DVB, MB = DVB / 16, TT = C / 16, RB = 2 * C;
-  using Smem = RecSmem<C, DVB>;
+  using Smem = RecSmem<C, DVB, TO>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -376,7 +403,7 @@ __global__ void __launch_bounds__(128) recur_kernel(ChunkParams p) {
   const int n = nh / p.hv;
   const int h = nh - n * p.hv;
   const int kh = h / (p.hv / p.hk);
-  __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+  TO *o = static_cast<TO *>(p.o);
 
   int bos, eos;
   seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
@@ -393,7 +420,7 @@ __global__ void __launch_bounds__(128) recur_kernel(ChunkParams p) {
   }
   for (int s = 0; s < 2; ++s) {
     if (s < nchunks)
-      load_stage<C, DVB>(sm.st[s], p, h, kh, blk, bos + s * C, min(C, eos - bos - s * C));
+      load_stage<C, DVB, TO>(sm.st[s], p, h, kh, blk, bos + s * C, min(C, eos - bos - s * C));
     cp_async_commit();
   }
   __syncthreads();
@@ -416,8 +443,10 @@ __global__ void __launch_bounds__(128) recur_kernel(ChunkParams p) {
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int j = 16 * m + gid + 8 * hr, i = 32 * warp + 8 * nt + 2 * tig;
-          *reinterpret_cast<uint32_t *>(sm.S + swz<kRowB>(j, 2 * i)) =
-              pack_bf16(Sa[m][nt][2 * hr], Sa[m][nt][2 * hr + 1]);
+          uint32_t hi, lo;
+          split_bf16(Sa[m][nt][2 * hr], Sa[m][nt][2 * hr + 1], hi, lo);
+          *reinterpret_cast<uint32_t *>(sm.Sh + swz<kRowB>(j, 2 * i)) = hi;
+          *reinterpret_cast<uint32_t *>(sm.Sl + swz<kRowB>(j, 2 * i)) = lo;
         }
   };
   write_state_operand();
@@ -434,27 +463,33 @@ __global__ void __launch_bounds__(128) recur_kernel(ChunkParams p) {
 
     float Op[MB][2][4];
     if (warp < TT) {
-      // P = S^T W^T and R = S^T Q^T for this warp's 16 tokens
-      float P[MB][2][4], R[MB][2][4];
+      // P = S^T W^T and R = S^T Q^T for this warp's 16 tokens (main and correction terms)
+      float P[MB][2][4], Pc[MB][2][4], R[MB][2][4], Rc[MB][2][4];
 #pragma unroll
       for (int m = 0; m < MB; ++m)
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) P[m][a][e] = R[m][a][e] = 0.f;
+          for (int e = 0; e < 4; ++e) P[m][a][e] = Pc[m][a][e] = R[m][a][e] = Rc[m][a][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
-        uint32_t bw[4], bq[4];
-        ldb_nk<kRowB>(bw, st.W, 16 * warp, 16 * ks, lane);
+        uint32_t bwh[4], bwl[4], bq[4];
+        ldb_nk<kRowB>(bwh, st.Wh, 16 * warp, 16 * ks, lane);
+        ldb_nk<kRowB>(bwl, st.Wl, 16 * warp, 16 * ks, lane);
         ldb_nk<kRowB>(bq, st.Q, 16 * warp, 16 * ks, lane);
 #pragma unroll
         for (int m = 0; m < MB; ++m) {
-          uint32_t a[4];
-          lda_tile<kRowB>(a, sm.S, 16 * m, 16 * ks, lane);
-          mma_bf16(P[m][0], a, bw[0], bw[1]);
-          mma_bf16(P[m][1], a, bw[2], bw[3]);
-          mma_bf16(R[m][0], a, bq[0], bq[1]);
-          mma_bf16(R[m][1], a, bq[2], bq[3]);
+          uint32_t ah[4], al[4];
+          lda_tile<kRowB>(ah, sm.Sh, 16 * m, 16 * ks, lane);
+          lda_tile<kRowB>(al, sm.Sl, 16 * m, 16 * ks, lane);
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
+            mma_bf16(P[m][a], ah, bwh[2 * a], bwh[2 * a + 1]);
+            mma_bf16(Pc[m][a], al, bwh[2 * a], bwh[2 * a + 1]);
+            mma_bf16(Pc[m][a], ah, bwl[2 * a], bwl[2 * a + 1]);
+            mma_bf16(R[m][a], ah, bq[2 * a], bq[2 * a + 1]);
+            mma_bf16(Rc[m][a], al, bq[2 * a], bq[2 * a + 1]);
+          }
         }
       }
       // D = U - W S (transposed), the exp(G)-scaled output part, and D scaled for the carry
@@ -467,13 +502,18 @@ __global__ void __launch_bounds__(128) recur_kernel(ChunkParams p) {
             const int j = 16 * m + gid + 8 * hr;
             const int t = 16 * warp + 8 * a + 2 * tig;
             const float g0 = (t < L) ? st.G[t] : gC, g1 = (t + 1 < L) ? st.G[t + 1] : gC;
-            const float d0 = st.U[t][j] - P[m][a][2 * hr];
-            const float d1 = st.U[t + 1][j] - P[m][a][2 * hr + 1];
-            Op[m][a][2 * hr] = expf(g0) * R[m][a][2 * hr];
-            Op[m][a][2 * hr + 1] = expf(g1) * R[m][a][2 * hr + 1];
-            *reinterpret_cast<uint32_t *>(sm.D + swz<RB>(j, 2 * t)) = pack_bf16(d0, d1);
-            *reinterpret_cast<uint32_t *>(sm.Dt + swz<RB>(j, 2 * t)) =
-                pack_bf16(d0 * expf(gC - g0), d1 * expf(gC - g1));
+            const float d0 = st.U[t][j] - (P[m][a][2 * hr] + Pc[m][a][2 * hr]);
+            const float d1 = st.U[t + 1][j] - (P[m][a][2 * hr + 1] + Pc[m][a][2 * hr + 1]);
+            Op[m][a][2 * hr] = expf(g0) * (R[m][a][2 * hr] + Rc[m][a][2 * hr]);
+            Op[m][a][2 * hr + 1] = expf(g1) * (R[m][a][2 * hr + 1] + Rc[m][a][2 * hr + 1]);
+            const int so = swz<RB>(j, 2 * t);
+            uint32_t hi, lo;
+            split_bf16(d0, d1, hi, lo);
+            *reinterpret_cast<uint32_t *>(sm.Dh + so) = hi;
+            *reinterpret_cast<uint32_t *>(sm.Dl + so) = lo;
+            split_bf16(d0 * expf(gC - g0), d1 * expf(gC - g1), hi, lo);
+            *reinterpret_cast<uint32_t *>(sm.Th + so) = hi;
+            *reinterpret_cast<uint32_t *>(sm.Tl + so) = lo;
           }
     }
     __syncthreads();
@@ -481,14 +521,20 @@ __global__ void __launch_bounds__(128) recur_kernel(ChunkParams p) {
     if (warp < TT) {
       // O^T += D^T A^T over the causal part of the block
       for (int ks = 0; ks <= warp; ++ks) {
-        uint32_t b[4];
-        ldb_nk<RB>(b, st.A, 16 * warp, 16 * ks, lane);
+        uint32_t bh[4], bl[4];
+        ldb_nk<RB>(bh, st.Ah, 16 * warp, 16 * ks, lane);
+        ldb_nk<RB>(bl, st.Al, 16 * warp, 16 * ks, lane);
 #pragma unroll
         for (int m = 0; m < MB; ++m) {
-          uint32_t a[4];
-          lda_tile<RB>(a, sm.D, 16 * m, 16 * ks, lane);
-          mma_bf16(Op[m][0], a, b[0], b[1]);
-          mma_bf16(Op[m][1], a, b[2], b[3]);
+          uint32_t ah[4], al[4];
+          lda_tile<RB>(ah, sm.Dh, 16 * m, 16 * ks, lane);
+          lda_tile<RB>(al, sm.Dl, 16 * m, 16 * ks, lane);
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
+            mma_bf16(Op[m][a], ah, bh[2 * a], bh[2 * a + 1]);
+            mma_bf16(Op[m][a], al, bh[2 * a], bh[2 * a + 1]);
+            mma_bf16(Op[m][a], ah, bl[2 * a], bl[2 * a + 1]);
+          }
         }
       }
 #pragma unroll
@@ -497,15 +543,16 @@ __global__ void __launch_bounds__(128) recur_kernel(ChunkParams p) {
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            sm.O[16 * warp + 8 * a + 2 * tig + (e & 1)][16 * m + gid + 8 * (e >> 1)] =
-                __float2bfloat16_rn(Op[m][a][e]);
+            Elem<TO>::store(&sm.O[16 * warp + 8 * a + 2 * tig + (e & 1)][16 * m + gid + 8 * (e >> 1)],
+                            Op[m][a][e]);
       __syncwarp();
-      constexpr int GPR = DVB * 2 / 16;  // 16-byte granules per output row
+      constexpr int EPG = 16 / sizeof(TO);        // elements per 16-byte granule
+      constexpr int GPR = DVB / EPG;              // granules per output row
       for (int e = lane; e < 16 * GPR; e += 32) {
         const int r = e / GPR, gi = e % GPR, t = 16 * warp + r;
         if (t < L)
-          *reinterpret_cast<uint4 *>(o + ((size_t)(tok0 + t) * p.hv + h) * kD + blk * DVB + gi * 8) =
-              *reinterpret_cast<const uint4 *>(&sm.O[t][gi * 8]);
+          *reinterpret_cast<uint4 *>(o + ((size_t)(tok0 + t) * p.hv + h) * kD + blk * DVB + gi * EPG) =
+              *reinterpret_cast<const uint4 *>(&sm.O[t][gi * EPG]);
       }
     }
 
@@ -518,24 +565,29 @@ __global__ void __launch_bounds__(128) recur_kernel(ChunkParams p) {
         for (int e = 0; e < 4; ++e) Sa[m][nt][e] *= egc;
 #pragma unroll
     for (int ks = 0; ks < TT; ++ks) {
-      uint32_t a[MB][4];
+      uint32_t ah[MB][4], al[MB][4];
 #pragma unroll
-      for (int m = 0; m < MB; ++m) lda_tile<RB>(a[m], sm.Dt, 16 * m, 16 * ks, lane);
+      for (int m = 0; m < MB; ++m) {
+        lda_tile<RB>(ah[m], sm.Th, 16 * m, 16 * ks, lane);
+        lda_tile<RB>(al[m], sm.Tl, 16 * m, 16 * ks, lane);
+      }
 #pragma unroll
       for (int np = 0; np < 2; ++np) {
         uint32_t b[4];
         ldb_kn<kRowB>(b, st.K, 16 * ks, 32 * warp + 16 * np, lane);
 #pragma unroll
         for (int m = 0; m < MB; ++m) {
-          mma_bf16(Sa[m][2 * np], a[m], b[0], b[1]);
-          mma_bf16(Sa[m][2 * np + 1], a[m], b[2], b[3]);
+          mma_bf16(Sa[m][2 * np], ah[m], b[0], b[1]);
+          mma_bf16(Sa[m][2 * np], al[m], b[0], b[1]);
+          mma_bf16(Sa[m][2 * np + 1], ah[m], b[2], b[3]);
+          mma_bf16(Sa[m][2 * np + 1], al[m], b[2], b[3]);
         }
       }
     }
     write_state_operand();
     __syncthreads();
     if (c + 2 < nchunks)
-      load_stage<C, DVB>(st, p, h, kh, blk, bos + (c + 2) * C, min(C, eos - bos - (c + 2) * C));
+      load_stage<C, DVB, TO>(st, p, h, kh, blk, bos + (c + 2) * C, min(C, eos - bos - (c + 2) * C));
     cp_async_commit();
   }
   cp_async_wait<0>();
@@ -556,9 +608,19 @@ __global__ void __launch_bounds__(128) recur_kernel(ChunkParams p) {
   }
 }
 
+template <int C, typename TO>
+cudaError_t launch_recur(const ChunkParams &p, long long heads, cudaStream_t stream) {
+  constexpr int DVB = 16;
+  const size_t s2 = sizeof(RecSmem<C, DVB, TO>);
+  cudaError_t err = cudaFuncSetAttribute(recur_kernel<C, DVB, TO>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+  if (err != cudaSuccess) return err;
+  recur_kernel<C, DVB, TO><<<(unsigned)(heads * (kD / DVB)), 128, s2, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int C>
 cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
-  constexpr int DVB = 16;
   int dev = 0, sms = 148;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -577,24 +639,22 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
-  const size_t s2 = sizeof(RecSmem<C, DVB>);
-  err = cudaFuncSetAttribute(recur_kernel<C, DVB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)s2);
-  if (err != cudaSuccess) return err;
-  recur_kernel<C, DVB><<<(unsigned)(heads * (kD / DVB)), 128, s2, stream>>>(p);
-  return cudaGetLastError();
+  return p.o_fp32 ? launch_recur<C, float>(p, heads, stream)
+                  : launch_recur<C, __nv_bfloat16>(p, heads, stream);
 }
 
 }  // namespace
 
-size_t chunk_workspace_layout(int total_tokens, int hv, int chunk, size_t off[4]) {
+size_t chunk_workspace_layout(int total_tokens, int hv, int chunk, size_t off[kWsRegions]) {
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t rows = (size_t)total_tokens * hv;
-  off[0] = 0;                                      // W  bf16 [Hv, T, 128]
-  off[1] = off[0] + up(rows * kD * 2);             // U  fp32 [Hv, T, 128]
-  off[2] = off[1] + up(rows * kD * 4);             // A  bf16 [Hv, T, chunk]
-  off[3] = off[2] + up(rows * (size_t)chunk * 2);  // G  fp32 [Hv, T]
-  return off[3] + up(rows * 4);
+  off[0] = 0;                                      // W hi  bf16 [Hv, T, 128]
+  off[1] = off[0] + up(rows * kD * 2);             // W lo  bf16 [Hv, T, 128]
+  off[2] = off[1] + up(rows * kD * 2);             // U     fp32 [Hv, T, 128]
+  off[3] = off[2] + up(rows * kD * 4);             // A hi  bf16 [Hv, T, chunk]
+  off[4] = off[3] + up(rows * (size_t)chunk * 2);  // A lo  bf16 [Hv, T, chunk]
+  off[5] = off[4] + up(rows * (size_t)chunk * 2);  // G     fp32 [Hv, T]
+  return off[5] + up(rows * 4);
 }
 
 cudaError_t launch_chunk_bf16(const ChunkParams &p, cudaStream_t stream) {

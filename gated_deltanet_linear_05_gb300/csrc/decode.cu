@@ -21,7 +21,7 @@ namespace {
 constexpr int kDecThreads = 128;
 constexpr int kDecCols = 32;  // value columns per CTA
 
-template <typename T>
+template <typename T, typename TO>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeParams p) {
   const int quarter = blockIdx.x & 3;
   const int nh = blockIdx.x >> 2;
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeParams p) {
   const T *q = static_cast<const T *>(p.q);
   const T *k = static_cast<const T *>(p.k);
   const T *v = static_cast<const T *>(p.v);
-  T *o = static_cast<T *>(p.o);
+  TO *o = static_cast<TO *>(p.o);
 
   for (int t = bos; t < eos; ++t) {
     s_q[tid] = Elem<T>::load(q + ((size_t)t * p.hk + kh) * kD + tid);
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeParams p) {
       const float ww = s_red[1][0][c] + s_red[1][1][c] + s_red[1][2][c] + s_red[1][3][c];
       delta[e] = b * (s_v[c] - d * uu);
       if (warp == 0 && rsub == 0)
-        Elem<T>::store(o + ((size_t)t * p.hv + h) * kD + col0 + e, d * ww + qk * delta[e]);
+        Elem<TO>::store(o + ((size_t)t * p.hv + h) * kD + col0 + e, d * ww + qk * delta[e]);
     }
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
@@ -132,10 +132,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeParams p) {
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream) {
   const long long units = (long long)p.num_seqs * p.hv * 4;
   if (units == 0) return cudaSuccess;
-  if (p.dtype == GDN_BF16)
-    decode_kernel<__nv_bfloat16><<<(unsigned)units, kDecThreads, 0, stream>>>(p);
+  if (p.dtype == GDN_BF16 && !p.o_fp32)
+    decode_kernel<__nv_bfloat16, __nv_bfloat16><<<(unsigned)units, kDecThreads, 0, stream>>>(p);
+  else if (p.dtype == GDN_BF16)
+    decode_kernel<__nv_bfloat16, float><<<(unsigned)units, kDecThreads, 0, stream>>>(p);
   else
-    decode_kernel<float><<<(unsigned)units, kDecThreads, 0, stream>>>(p);
+    decode_kernel<float, float><<<(unsigned)units, kDecThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -19,6 +19,7 @@ gdn_status check_shape(const gdn_shape *s, bool needs_chunk) {
   if (s->num_v_heads % s->num_k_heads != 0) return GDN_ERR_INVALID_ARG;
   if (s->dk != gdn::kD || s->dv != gdn::kD) return GDN_ERR_UNSUPPORTED;
   if (s->qkv_dtype != GDN_F32 && s->qkv_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (s->o_fp32 != 0 && s->o_fp32 != 1) return GDN_ERR_INVALID_ARG;
   if (needs_chunk && s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return GDN_ERR_UNSUPPORTED;
   // grids are sized (sequences x v-heads x 8) in one dimension
   if ((long long)s->num_seqs * s->num_v_heads * 8 > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
@@ -73,6 +74,7 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   p.hv = s->num_v_heads;
   p.chunk = s->chunk;
   p.dtype = s->qkv_dtype;
+  p.o_fp32 = s->o_fp32 != 0;
   p.q = c.q;
   p.k = c.k;
   p.v = c.v;
@@ -84,16 +86,18 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   p.o = c.o;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s->qkv_dtype == GDN_F32) return cuda_status(gdn::launch_chunk_f32(p, st));
-  size_t off[4];
+  size_t off[gdn::kWsRegions];
   const size_t need = gdn::chunk_workspace_layout(s->total_tokens, s->num_v_heads, s->chunk, off);
   if (need > 0 && (!workspace || workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return GDN_ERR_WORKSPACE;
   char *ws = static_cast<char *>(workspace);
-  p.w_ws = ws + off[0];
-  p.u_ws = reinterpret_cast<float *>(ws + off[1]);
-  p.a_ws = ws + off[2];
-  p.g_ws = reinterpret_cast<float *>(ws + off[3]);
+  p.w_hi = ws + off[0];
+  p.w_lo = ws + off[1];
+  p.u_ws = reinterpret_cast<float *>(ws + off[2]);
+  p.a_hi = ws + off[3];
+  p.a_lo = ws + off[4];
+  p.g_ws = reinterpret_cast<float *>(ws + off[5]);
   return cuda_status(gdn::launch_chunk_bf16(p, st));
 }
 
@@ -106,7 +110,7 @@ size_t gdn_workspace_size(const gdn_shape *s, int op) {
   const bool chunked = (op == GDN_OP_PREFILL || op == GDN_OP_VERIFY);
   if (check_shape(s, chunked) != GDN_OK) return (size_t)-1;
   if (!chunked || s->qkv_dtype == GDN_F32) return 0;
-  size_t off[4];
+  size_t off[gdn::kWsRegions];
   return gdn::chunk_workspace_layout(s->total_tokens, s->num_v_heads, s->chunk, off);
 }
 
@@ -173,6 +177,7 @@ gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k,
   p.hk = shape->num_k_heads;
   p.hv = shape->num_v_heads;
   p.dtype = shape->qkv_dtype;
+  p.o_fp32 = shape->o_fp32 != 0;
   p.q = q;
   p.k = k;
   p.v = v;

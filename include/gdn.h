@@ -25,7 +25,8 @@
  * Pointers are DEVICE pointers, row-major and contiguous, each 16-byte aligned
  * (cu_seqlens: 4-byte aligned):
  *     q, k          [total_tokens, Hk, dk]   qkv_dtype
- *     v, o          [total_tokens, Hv, dv]   qkv_dtype
+ *     v             [total_tokens, Hv, dv]   qkv_dtype
+ *     o             [total_tokens, Hv, dv]   qkv_dtype, or float32 when shape->o_fp32
  *     g, beta       [total_tokens, Hv]       float32 (g: log-decay, used as is)
  *     state_in/out  [num_seqs, Hv, dk, dv]   float32
  *     cu_seqlens    [num_seqs + 1]           int32, cu_seqlens[0] = 0, non-decreasing,
@@ -83,7 +84,10 @@ typedef struct {
   int32_t num_v_heads;   /* Hv, a multiple of Hk: heads of v, g, beta, state and o  */
   int32_t dk, dv;        /* head sizes; 128 and 128 are built                       */
   int32_t chunk;         /* block length for prefill / verify: 16, 32 or 64        */
-  gdn_dtype qkv_dtype;   /* dtype of q, k, v and o: GDN_F32 or GDN_BF16             */
+  gdn_dtype qkv_dtype;   /* dtype of q, k, v (and of o unless o_fp32): F32 or BF16  */
+  int32_t o_fp32;        /* 0: o has qkv_dtype; 1: o is float32 (the unrounded       */
+                         /* fp32 result; the bf16 o of the same call is exactly its  */
+                         /* round-to-nearest-even rounding)                          */
 } gdn_shape;
 
 /*

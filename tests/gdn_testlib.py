@@ -37,19 +37,32 @@ def to_np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def gpu_prefill(x, wl, chunk=None, state_in=True, inplace=False, verify=False):
-    """Run the chunked path (or verify) on the seeded inputs; returns (o, state_out, dev)."""
+def gpu_prefill(x, wl, chunk=None, state_in=True, inplace=False, verify=False, o_fp32=False):
+    """Run the chunked path (or verify) on the seeded inputs; returns (o, state_out, dev).
+
+    o_fp32: ask for the unrounded fp32 output even when q/k/v are bf16."""
     import torch
     import gated_deltanet_linear_05_gb300 as gdn
     d = device_inputs(x, wl.dtype)
     s_in = d["state0"] if state_in else None
     N, Hv = wl.num_seqs, wl.num_v_heads
     if inplace:
-        s_out = s_in
+        s_out = s_in.clone() if s_in is not None else None
+        s_in = s_out
     else:
         s_out = torch.full((N, Hv, wl.dk, wl.dv), float("nan"), device="cuda")
+    o = torch.full(d["v"].shape, float("nan"), device="cuda",
+                   dtype=torch.float32 if o_fp32 else d["v"].dtype)
     fn = gdn.gdn_verify_block if verify else gdn.gdn_prefill_chunked
-    o, s = fn(d["q"], d["k"], d["v"], d["g"], d["beta"], s_in, s_out, d["cu_seqlens"],
+    o, s = fn(d["q"], d["k"], d["v"], d["g"], d["beta"], s_in, s_out, d["cu_seqlens"], o,
               chunk=chunk or wl.chunk)
     torch.cuda.synchronize()
+    d["o_raw"] = o
     return to_np(o), to_np(s), d
+
+
+def half_ulp_bf16(x):
+    """Half the bf16 spacing at |x| (the largest rounding error of a stored bf16 value)."""
+    ax = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return np.where(ax > 0, 2.0 ** (e - 8), 0.0)
