@@ -25,7 +25,7 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_OP_PREFILL, GDN_OP_DECODE, GDN_OP_VERIFY = 0, 1, 2
 
 EXPORTS = ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_block",
-           "gdn_workspace_size", "gdn_status_string")
+           "gdn_workspace_size", "gdn_status_string", "gdn_prefill_chunked_noalloc")
 
 
 class GdnUnavailable(RuntimeError):
@@ -70,6 +70,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_workspace_size.restype = ctypes.c_size_t
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_status_string.restype = ctypes.c_char_p
+        # for callers that cannot allocate: scratch built into the library, no workspace
+        L.gdn_prefill_chunked_noalloc.argtypes = [ctypes.POINTER(GdnShape), P, P, P, P, P, P, P,
+                                                  P, P, P]
+        L.gdn_prefill_chunked_noalloc.restype = ctypes.c_int
         _lib = L
     return _lib
 

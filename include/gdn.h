@@ -137,6 +137,39 @@ gdn_status gdn_verify_block(const gdn_shape *shape, const void *q, const void *k
                             const int32_t *cu_seqlens, void *o, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/*
+ * Scratch size built into gdn_prefill_chunked_noalloc (64 MiB).
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * The chunked prompt pass for callers that cannot allocate device memory.  The
+ * paper has no counterpart to this entry point: it exists for the library's users.
+ *
+ * Who needs it: code that may not call cudaMalloc (or any allocator) at the point
+ * where it runs the layer -- for example a host runtime that hands out only
+ * pre-registered buffers, a plug-in inside another framework's memory pool, or a
+ * real-time path where an allocation could block or fail.  Such a caller still
+ * owns q, k, v, g, beta, the states, cu_seqlens and o, exactly as for
+ * gdn_prefill_chunked; only the scratch (the `workspace` there) comes from a fixed
+ * array of GDN_NOALLOC_SCRATCH_BYTES compiled into the library.  The array lives on
+ * every GPU where this entry point has run until the process exits.
+ *
+ * Same arguments and results as gdn_prefill_chunked, without workspace.  The request
+ * must fit: gdn_workspace_size(shape, GDN_OP_PREFILL) <= GDN_NOALLOC_SCRATCH_BYTES,
+ * else GDN_ERR_WORKSPACE is returned and nothing is launched (f32 q/k/v need no
+ * scratch and always fit).  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array: two calls whose work
+ * overlaps on the GPU (different streams, or different host threads) race on it and
+ * give wrong results, so order them.  No part of the array has to start at zero.
+ * It allocates nothing itself: no cudaMalloc, cudaFree or allocating library call.
+ */
+gdn_status gdn_prefill_chunked_noalloc(const gdn_shape *shape, const void *q, const void *k,
+                                       const void *v, const float *g, const float *beta,
+                                       const float *state_in, float *state_out,
+                                       const int32_t *cu_seqlens, void *o, void *stream);
+
 /* Workspace bytes `op` (a gdn_op) needs for `shape` (0 when none); (size_t)-1 for an
  * invalid shape or op. */
 size_t gdn_workspace_size(const gdn_shape *shape, int op);
