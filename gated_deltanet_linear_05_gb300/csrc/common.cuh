@@ -65,6 +65,49 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+// ------------------------------------------------------------------ mbarrier / bulk copy
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// Wait for the phase with the given parity to complete.  Bounded: gives up after about
+// 2^22 polls (far beyond any legitimate wait) and returns false, so that a lost
+// signal ends in wrong results and an error flag instead of a hung GPU.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done = 0;
+  for (int it = 0; it < (1 << 22) && !done; ++it) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  }
+  return done != 0;
+}
+// Bulk (TMA) copy global -> shared of `bytes` (multiple of 16, both ends 16-byte
+// aligned); completion is counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ------------------------------------------------------------------ tensor cores
 // mma.sync m16n8k16, bf16 inputs, fp32 accumulate.  Fragment ownership (lane l,
 // gid = l >> 2, tig = l & 3):
@@ -118,6 +161,14 @@ __device__ __forceinline__ void lda_tile(uint32_t (&a)[4], const char *base, int
   const int c = c0 + (lane >> 4) * 8;
   ldsm_x4(a, base + swz<ROWB>(r, c * 2));
 }
+// A-operand (16x16: rows m0.., k cols k0..) from a swizzled tile stored [k][m].
+template <int ROWB>
+__device__ __forceinline__ void lda_tile_t(uint32_t (&a)[4], const char *base, int m0, int k0,
+                                           int lane) {
+  const int r = k0 + (lane & 7) + (lane >> 4) * 8;
+  const int c = m0 + ((lane >> 3) & 1) * 8;
+  ldsm_x4_t(a, base + swz<ROWB>(r, c * 2));
+}
 // Two B-operands (n-tiles n0 and n0+8, k 16 wide at k0) from a tile stored [n][k].
 // b[0], b[1]: n-tile n0 (k lo, k hi); b[2], b[3]: n-tile n0 + 8.
 template <int ROWB>
@@ -134,6 +185,18 @@ __device__ __forceinline__ void ldb_kn(uint32_t (&b)[4], const char *base, int k
   const int r = k0 + (lane & 7) + ((lane >> 3) & 1) * 8;
   const int c = n0 + (lane >> 4) * 8;
   ldsm_x4_t(b, base + swz<ROWB>(r, c * 2));
+}
+
+// x0, x1 -> bf16 pair hi = bf16(x), lo = bf16(x - hi): together ~16 significant bits.
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+  hi = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+  lo = pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+}
+
+// Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
+__device__ __forceinline__ void bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float x) {

@@ -86,18 +86,15 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   p.o = c.o;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s->qkv_dtype == GDN_F32) return cuda_status(gdn::launch_chunk_f32(p, st));
-  size_t off[gdn::kWsRegions];
-  const size_t need = gdn::chunk_workspace_layout(s->total_tokens, s->num_v_heads, s->chunk, off);
+  const size_t need =
+      gdn::chunk_workspace_bytes(s->total_tokens, s->num_seqs, s->num_v_heads, s->chunk);
   if (need > 0 && (!workspace || workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return GDN_ERR_WORKSPACE;
   char *ws = static_cast<char *>(workspace);
-  p.w_hi = ws + off[0];
-  p.w_lo = ws + off[1];
-  p.u_ws = reinterpret_cast<float *>(ws + off[2]);
-  p.a_hi = ws + off[3];
-  p.a_lo = ws + off[4];
-  p.g_ws = reinterpret_cast<float *>(ws + off[5]);
+  p.nslots = s->total_tokens / s->chunk + s->num_seqs;
+  p.err = reinterpret_cast<int *>(ws);
+  p.slot_ws = ws + 256;
   return cuda_status(gdn::launch_chunk_bf16(p, st));
 }
 
@@ -110,8 +107,7 @@ size_t gdn_workspace_size(const gdn_shape *s, int op) {
   const bool chunked = (op == GDN_OP_PREFILL || op == GDN_OP_VERIFY);
   if (check_shape(s, chunked) != GDN_OK) return (size_t)-1;
   if (!chunked || s->qkv_dtype == GDN_F32) return 0;
-  size_t off[gdn::kWsRegions];
-  return gdn::chunk_workspace_layout(s->total_tokens, s->num_v_heads, s->chunk, off);
+  return gdn::chunk_workspace_bytes(s->total_tokens, s->num_seqs, s->num_v_heads, s->chunk);
 }
 
 const char *gdn_status_string(gdn_status status) {

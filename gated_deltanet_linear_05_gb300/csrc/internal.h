@@ -29,18 +29,32 @@ struct ChunkParams {
   float *state_out;
   const int32_t *cu_seqlens;
   void *o;
-  // workspace regions of the two-pass bf16 path (see chunk_bf16.cu); "hi"/"lo" are the
-  // bf16 high part and the bf16 rounding of the remainder of an fp32 value
-  void *w_hi, *w_lo;  // bf16 [Hv, T, 128]: W = (I+N)^-1 diag(beta e^G) K, per token row
-  float *u_ws;        // fp32 [Hv, T, 128]: U = (I+N)^-1 diag(beta) V
-  void *a_hi, *a_lo;  // bf16 [Hv, T, chunk]: row t of the block's decay-masked causal Q K^T
-  float *g_ws;        // fp32 [Hv, T]: in-block inclusive cumsum of g
+  // Workspace of the two-pass bf16 path (see chunk_bf16.cu): one slot per (v-head,
+  // block); block c of sequence n uses slot bos_n / C + n + c, which is unique and
+  // below nslots = total_tokens / C + num_seqs.  A slot holds, for the C rows of the
+  // block (rows past the sequence end are zero), in the shared-memory layout the
+  // pass-2 kernel uses:
+  //   W  bf16 [C][128] (swizzled)   W = (I+N)^-1 diag(beta e^G) K
+  //   Q  bf16 [C][128] (swizzled)   K  bf16 [C][128] (swizzled)
+  //   Ah, Al bf16 [C][C] (swizzled) decay-masked causal Q K^T, hi and lo parts
+  //   U  fp32 [128][C+4]            U^T, U = (I+N)^-1 diag(beta) V
+  //   G  fp32 [C]                   in-block inclusive cumsum of g
+  int nslots;
+  char *slot_ws;      // Hv * nslots slots of slot_bytes(C) bytes, 128-byte aligned
+  int *err;           // device status word: nonzero if a kernel wait timed out
 };
 
-constexpr int kWsRegions = 6;
-// Workspace layout of the bf16 chunk path (offsets of w_hi, w_lo, u, a_hi, a_lo, g);
-// returns total bytes.
-size_t chunk_workspace_layout(int total_tokens, int hv, int chunk, size_t offsets[kWsRegions]);
+// Bytes of one workspace slot for block length C.
+__host__ __device__ constexpr size_t slot_head_bytes(int C) {
+  return (size_t)3 * 256 * C + (size_t)4 * C * C;
+}
+__host__ __device__ constexpr size_t slot_u_bytes(int C) { return (size_t)128 * (C + 4) * 4; }
+__host__ __device__ constexpr size_t slot_bytes(int C) {
+  return (slot_head_bytes(C) + slot_u_bytes(C) + (size_t)4 * C + 127) / 128 * 128;
+}
+
+// Workspace bytes of the bf16 chunk path: a 256-byte header (status word) + slots.
+size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk);
 
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_chunk_bf16(const ChunkParams &p, cudaStream_t stream);
