@@ -77,11 +77,14 @@ struct PrepSmem {
   float T[C][C + 4];
   float M[32 * 33];
   float G[C], EG[C], B[C];
+  float gRaw[C], bRaw[C];
 };
 
+constexpr int kPrepThreads = 256;
+
 template <int C>
-__global__ void __launch_bounds__(2 * C) prep_kernel(ChunkParams p, int per_head) {
-  constexpr int NW = C / 16, NT = 32 * NW, MT = C / 16, RB = 2 * C, LD = C + 4;
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChunkParams p, int per_head) {
+  constexpr int NW = kPrepThreads / 32, NT = kPrepThreads, MT = C / 16, RB = 2 * C, LD = C + 4;
   static_assert(8 * C * C <= C * kRowB + C * (C + 4) * 4, "overlay too small");
   extern __shared__ __align__(128) unsigned char smem_raw[];
   PrepSmem<C> &sm = *reinterpret_cast<PrepSmem<C> *>(smem_raw);
@@ -124,7 +127,16 @@ __global__ void __launch_bounds__(2 * C) prep_kernel(ChunkParams p, int per_head
       cp_async16(sQ + swz<kRowB>(r, gr * 16), q + (tok * p.hk + kh) * kD + gr * 8, nb);
       cp_async16(sm.V + swz<kRowB>(r, gr * 16), v + (tok * p.hv + h) * kD + gr * 8, nb);
     }
+    for (int t = tid; t < C; t += NT) {
+      const bool ok = t < L;
+      const size_t gi = ((size_t)tok0 + (ok ? t : 0)) * p.hv + h;
+      cp_async4(&sm.gRaw[t], p.g + gi, ok ? 4 : 0);
+      cp_async4(&sm.bRaw[t], p.beta + gi, ok ? 4 : 0);
+    }
     cp_async_commit();
+    for (int e = tid; e < C * LD; e += NT) (&sm.T[0][0])[e] = 0.f;
+    cp_async_wait<0>();
+    __syncthreads();
 
     // in-block inclusive cumsum of g (padding contributes 0), exp(G), beta
     if (warp == 0) {
@@ -133,9 +145,8 @@ __global__ void __launch_bounds__(2 * C) prep_kernel(ChunkParams p, int per_head
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int t = lane * E + e;
-        const bool ok = t < L;
-        gv[e] = ok ? p.g[((size_t)tok0 + t) * p.hv + h] : 0.f;
-        bv[e] = ok ? p.beta[((size_t)tok0 + t) * p.hv + h] : 0.f;
+        gv[e] = t < C ? sm.gRaw[t] : 0.f;
+        bv[e] = t < C ? sm.bRaw[t] : 0.f;
         run += gv[e];
         gv[e] = run;
       }
@@ -157,21 +168,18 @@ __global__ void __launch_bounds__(2 * C) prep_kernel(ChunkParams p, int per_head
         }
       }
     }
-    for (int e = tid; e < C * LD; e += NT) (&sm.T[0][0])[e] = 0.f;
-    cp_async_wait<0>();
-    __syncthreads();
 
     // the block's q and k rows (swizzled, zero past the sequence end) go to the slot as is
     for (int e = tid; e < C * 16; e += NT) {
       reinterpret_cast<uint4 *>(q_out)[e] = reinterpret_cast<const uint4 *>(sQ)[e];
       reinterpret_cast<uint4 *>(k_out)[e] = reinterpret_cast<const uint4 *>(sm.K)[e];
     }
+    __syncthreads();  // G, EG, B written by warp 0
 
     // ---- decay-masked Grams on tensor cores: warp w takes items 2w, 2w+1 of
     //      [KK(0), KK(MT-1), KK(1), ..., QK(0), QK(MT-1), ...] (balanced triangles)
 #pragma unroll 1
-    for (int it = 0; it < 2; ++it) {
-      const int item = warp * 2 + it;
+    for (int item = warp; item < 2 * MT; item += NW) {
       const int prod = item / MT;  // 0: K K^T, 1: Q K^T
       const int r = item % MT;
       const int mt = (r & 1) ? (MT - 1 - r / 2) : (r / 2);
@@ -270,30 +278,35 @@ __global__ void __launch_bounds__(2 * C) prep_kernel(ChunkParams p, int per_head
     }
     // Level 2 (32 -> 64): lower-left 32x32 block = -T_BB (N_BA T_AA); two tiles per warp.
     if (C == 64) {
-      const int r0 = 16 * (warp >> 1), nb = 16 * (warp & 1);
-      float acc[2][4] = {};
+      const int r0 = 16 * ((warp >> 1) & 1), nb = 16 * (warp & 1);
+      const bool lv2 = warp < 4;
+      if (lv2) {
+        float acc[2][4] = {};
 #pragma unroll
-      for (int a = 0; a < 2; ++a)
+        for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-          mma_f32x3(acc[a], &sN[32][0], LD, &sm.T[0][0], LD, r0, 16 * ks, nb + 8 * a, lane);
+          for (int ks = 0; ks < 2; ++ks)
+            mma_f32x3(acc[a], &sN[32][0], LD, &sm.T[0][0], LD, r0, 16 * ks, nb + 8 * a, lane);
 #pragma unroll
-      for (int a = 0; a < 2; ++a)
+        for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sm.M[(r0 + gid + 8 * (e >> 1)) * 33 + nb + 8 * a + 2 * tig + (e & 1)] = acc[a][e];
+          for (int e = 0; e < 4; ++e)
+            sm.M[(r0 + gid + 8 * (e >> 1)) * 33 + nb + 8 * a + 2 * tig + (e & 1)] = acc[a][e];
+      }
       __syncthreads();
-      float acc2[2][4] = {};
+      if (lv2) {
+        float acc2[2][4] = {};
 #pragma unroll
-      for (int a = 0; a < 2; ++a)
+        for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-          mma_f32x3(acc2[a], &sm.T[32][32], LD, sm.M, 33, r0, 16 * ks, nb + 8 * a, lane);
+          for (int ks = 0; ks < 2; ++ks)
+            mma_f32x3(acc2[a], &sm.T[32][32], LD, sm.M, 33, r0, 16 * ks, nb + 8 * a, lane);
 #pragma unroll
-      for (int a = 0; a < 2; ++a)
+        for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sm.T[32 + r0 + gid + 8 * (e >> 1)][nb + 8 * a + 2 * tig + (e & 1)] = -acc2[a][e];
+          for (int e = 0; e < 4; ++e)
+            sm.T[32 + r0 + gid + 8 * (e >> 1)][nb + 8 * a + 2 * tig + (e & 1)] = -acc2[a][e];
+      }
       __syncthreads();
     }
 
@@ -697,7 +710,7 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
     const size_t s1 = sizeof(PrepSmem<C>);
     err = cudaFuncSetAttribute(prep_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     if (err != cudaSuccess) return err;
-    prep_kernel<C><<<(unsigned)(heads * per_head), 2 * C, s1, stream>>>(p, (int)per_head);
+    prep_kernel<C><<<(unsigned)(heads * per_head), kPrepThreads, s1, stream>>>(p, (int)per_head);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }

@@ -246,3 +246,14 @@ def test_varlen_packed_matches_separate_runs_bf16():
         o1, s1, _ = gpu_prefill(xs, wl1)
         np.testing.assert_array_equal(o1, o[a:b])
         np.testing.assert_array_equal(s1[0], s[n])
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_repeated_runs_are_bit_identical(chunk):
+    """Races between warps or CTAs show up as run-to-run differences."""
+    wl = gi.Workload("det", [40, 15, 130], 1, 2, chunk=chunk, dtype="bf16", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=12)
+    o0, s0, _ = gpu_prefill(x, wl, o_fp32=True)
+    for _ in range(8):
+        o1, s1, _ = gpu_prefill(x, wl, o_fp32=True)
+        assert np.array_equal(o0, o1) and np.array_equal(s0, s1)
