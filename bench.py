@@ -328,51 +328,61 @@ def bench_decode(torch, gdn, gi, device, pk, args):
             "us_per_step_l2_resident": round(times["resident"] * 1e3, 3), "gpu_launches": steps}
 
 
-def bench_verify(torch, gdn, gi, device, pk, args, flush):
-    wl = gi.verify_b128_h32()
-    x = gi.make_inputs(wl)
-    d = dev_inputs(x, torch, device)
+SCHEDULES = (("two_pass", 1), ("single_pass", 2))
+
+
+def bench_chunked_schedules(torch, gdn, d, wl, chunk, fn, op, n, flush):
+    """Mean ms per call of each bf16 schedule, and the one AUTO picks for this shape."""
     s_out = torch.empty_like(d["state0"])
     o = torch.empty_like(d["v"])
-    shape = gdn.make_shape(wl.num_seqs, wl.total_tokens, wl.num_k_heads, wl.num_v_heads, chunk=16)
-    ws = torch.empty(gdn.gdn_workspace_size(shape, gdn.GDN_OP_VERIFY) + 256, dtype=torch.uint8,
-                     device=device)
+    res = {}
+    for name, algo in SCHEDULES:
+        shape = gdn.make_shape(wl.num_seqs, wl.total_tokens, wl.num_k_heads, wl.num_v_heads,
+                               chunk=chunk, algo=algo)
+        ws = torch.empty(gdn.gdn_workspace_size(shape, op) + 256, dtype=torch.uint8,
+                         device=d["q"].device)
 
-    def step():
-        gdn.gdn_verify_block(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
-                             d["cu"], o, chunk=16, workspace=ws)
+        def step():
+            fn(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out, d["cu"], o,
+               chunk=chunk, workspace=ws, algo=algo)
 
+        res[name] = statistics.mean(timed_steps(torch, step, n, 3, flush))
+    auto = "single_pass" if wl.num_seqs * wl.num_v_heads >= gdn.GDN_SINGLE_PASS_MIN_HEADS \
+        else "two_pass"
+    return res, auto
+
+
+def bench_verify(torch, gdn, gi, device, pk, args, flush):
+    wl = gi.verify_b128_h32()
+    d = dev_inputs(gi.make_inputs(wl), torch, device)
     n = max(5, min(args.steps, 50))
-    ms = statistics.mean(timed_steps(torch, step, n, 3, flush))
+    res, auto = bench_chunked_schedules(torch, gdn, d, wl, 16, gdn.gdn_verify_block,
+                                        gdn.GDN_OP_VERIFY, n, flush)
+    ms = res[auto]
     flops, byts = prefill_work(wl.lengths, wl.num_k_heads, wl.num_v_heads, 16)
-    return {"workload": wl.name, "us_per_step": round(ms * 1e3, 2),
+    return {"workload": wl.name, "schedule": auto, "us_per_step": round(ms * 1e3, 2),
+            "us_per_step_by_schedule": {k: round(v * 1e3, 2) for k, v in res.items()},
             "tokens_per_s": round(wl.total_tokens / (ms * 1e-3), 1),
             "roofline": roofline("hbm", byts / (ms * 1e-3) / 1e9, pk["hbm"], "GB/s"),
-            "algorithmic_bytes": byts, "gpu_launches": 2 * n}
+            "algorithmic_bytes": byts,
+            "gpu_launches": n * (1 if auto == "single_pass" else 2)}
 
 
 def bench_varlen(torch, gdn, gi, device, pk, args, flush):
     wl = gi.varlen_8seq_hk16_hv32()
-    x = gi.make_inputs(wl)
-    d = dev_inputs(x, torch, device)
-    s_out = torch.empty_like(d["state0"])
-    o = torch.empty_like(d["v"])
-    shape = gdn.make_shape(wl.num_seqs, wl.total_tokens, wl.num_k_heads, wl.num_v_heads, chunk=64)
-    ws = torch.empty(gdn.gdn_workspace_size(shape, gdn.GDN_OP_PREFILL) + 256, dtype=torch.uint8,
-                     device=device)
-
-    def step():
-        gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
-                                d["cu"], o, chunk=64, workspace=ws)
-
+    d = dev_inputs(gi.make_inputs(wl), torch, device)
     n = max(5, min(args.steps, 30))
-    ms = statistics.mean(timed_steps(torch, step, n, 3, flush))
+    res, auto = bench_chunked_schedules(torch, gdn, d, wl, 64, gdn.gdn_prefill_chunked,
+                                        gdn.GDN_OP_PREFILL, n, flush)
+    ms = res[auto]
     flops, byts = prefill_work(wl.lengths, wl.num_k_heads, wl.num_v_heads, 64)
-    return {"workload": wl.name, "lengths": wl.lengths, "us_per_step": round(ms * 1e3, 2),
+    return {"workload": wl.name, "lengths": wl.lengths, "schedule": auto,
+            "us_per_step": round(ms * 1e3, 2),
+            "us_per_step_by_schedule": {k: round(v * 1e3, 2) for k, v in res.items()},
             "tokens_per_s": round(wl.total_tokens / (ms * 1e-3), 1),
             "roofline": roofline("hbm", byts / (ms * 1e-3) / 1e9, pk["hbm"], "GB/s"),
             "tensor_frac": round(flops / (ms * 1e-3) / 1e12 / pk["bf16"], 4),
-            "gpu_launches": 2 * n}
+            "gpu_launches": n * (1 if auto == "single_pass" else 2)}
 
 
 # ------------------------------------------------------------------ CPU oracle

@@ -23,6 +23,8 @@ GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIAS, GDN_ERR_WORKSPA
     GDN_ERR_CUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_OP_PREFILL, GDN_OP_DECODE, GDN_OP_VERIFY = 0, 1, 2
+GDN_ALGO_AUTO, GDN_ALGO_TWO_PASS, GDN_ALGO_SINGLE_PASS = 0, 1, 2
+GDN_SINGLE_PASS_MIN_HEADS = 128
 
 EXPORTS = ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_block",
            "gdn_workspace_size", "gdn_status_string", "gdn_prefill_chunked_noalloc")
@@ -45,7 +47,7 @@ class GdnShape(ctypes.Structure):
                 ("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
                 ("chunk", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32),
-                ("o_fp32", ctypes.c_int32)]
+                ("o_fp32", ctypes.c_int32), ("algo", ctypes.c_int32)]
 
 
 _lib = None
@@ -84,8 +86,9 @@ def gdn_status_string(status: int) -> str:
 
 def make_shape(num_seqs: int, total_tokens: int, num_k_heads: int, num_v_heads: int,
                dk: int = 128, dv: int = 128, chunk: int = 64, dtype: int = GDN_BF16,
-               o_fp32: int = 0) -> GdnShape:
-    return GdnShape(num_seqs, total_tokens, num_k_heads, num_v_heads, dk, dv, chunk, dtype, o_fp32)
+               o_fp32: int = 0, algo: int = GDN_ALGO_AUTO) -> GdnShape:
+    return GdnShape(num_seqs, total_tokens, num_k_heads, num_v_heads, dk, dv, chunk, dtype, o_fp32,
+                    algo)
 
 
 def gdn_workspace_size(shape: GdnShape, op: int) -> int:
@@ -115,7 +118,7 @@ def _dtype_code(t) -> int:
     raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
 
 
-def _shape_of(q, v, o, state_out, cu_seqlens, chunk: int) -> GdnShape:
+def _shape_of(q, v, o, state_out, cu_seqlens, chunk: int, algo: int = 0) -> GdnShape:
     """Shape from the tensors; o may be float32 while q/k/v are bf16 (o_fp32 = 1)."""
     T, hk, dk = q.shape
     hv, dv = v.shape[1], v.shape[2]
@@ -124,7 +127,7 @@ def _shape_of(q, v, o, state_out, cu_seqlens, chunk: int) -> GdnShape:
     o_fp32 = int(code == GDN_BF16 and _dtype_code(o) == GDN_F32)
     if code == GDN_F32 and _dtype_code(o) != GDN_F32:
         raise TypeError("o must be float32 when q/k/v are float32")
-    return make_shape(n, T, hk, hv, dk, dv, chunk, code, o_fp32)
+    return make_shape(n, T, hk, hv, dk, dv, chunk, code, o_fp32, algo)
 
 
 def _check_tensors(*ts):
@@ -152,9 +155,9 @@ def _workspace(shape: GdnShape, op: int, device, workspace):
 
 
 def _call(name, op, q, k, v, g, beta, state_in, state_out, cu_seqlens, o, chunk,
-          workspace, stream):
+          workspace, stream, algo=GDN_ALGO_AUTO):
     _check_tensors(q, k, v, g, beta, state_in, state_out, cu_seqlens, o, workspace)
-    shape = _shape_of(q, v, o, state_out, cu_seqlens, chunk)
+    shape = _shape_of(q, v, o, state_out, cu_seqlens, chunk, algo)
     ws_ptr, ws_bytes = _workspace(shape, op, q.device, workspace)
     st = getattr(lib(), name)(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                               _ptr(beta), _ptr(state_in), _ptr(state_out), _ptr(cu_seqlens),
@@ -165,23 +168,24 @@ def _call(name, op, q, k, v, g, beta, state_in, state_out, cu_seqlens, o, chunk,
 
 
 def gdn_prefill_chunked(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,
-                        chunk: int = 64, workspace=None, stream=None):
+                        chunk: int = 64, workspace=None, stream=None, algo: int = GDN_ALGO_AUTO):
     """Chunkwise-parallel prompt pass.  Tensors as in include/gdn.h:
     q, k [T, Hk, 128]; v [T, Hv, 128]; g, beta [T, Hv] fp32; state_in (or None),
-    state_out [N, Hv, 128, 128] fp32; cu_seqlens [N+1] int32.  Returns (o, state_out)."""
+    state_out [N, Hv, 128, 128] fp32; cu_seqlens [N+1] int32.  algo: a GDN_ALGO_* schedule.
+    Returns (o, state_out)."""
     if o is None:
         o = _torch().empty_like(v)
     return _call("gdn_prefill_chunked", GDN_OP_PREFILL, q, k, v, g, beta, state_in, state_out,
-                 cu_seqlens, o, chunk, workspace, stream)
+                 cu_seqlens, o, chunk, workspace, stream, algo)
 
 
 def gdn_verify_block(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,
-                     chunk: int = 16, workspace=None, stream=None):
+                     chunk: int = 16, workspace=None, stream=None, algo: int = GDN_ALGO_AUTO):
     """Draft-verify block from the snapshot state_in (left unchanged)."""
     if o is None:
         o = _torch().empty_like(v)
     return _call("gdn_verify_block", GDN_OP_VERIFY, q, k, v, g, beta, state_in, state_out,
-                 cu_seqlens, o, chunk, workspace, stream)
+                 cu_seqlens, o, chunk, workspace, stream, algo)
 
 
 def gdn_decode_step(q, k, v, g, beta, state_in, state_out, cu_seqlens=None, o=None,

@@ -1,0 +1,501 @@
+// Single-pass chunkwise gated delta rule for batches with many (sequence, head) pairs
+// ("Qwen3.5-9B-npu" model card, section "How it works", chunkwise form):
+//   N   = diag(beta) [exp(G_t - G_j) k_t.k_j]_{j<t},   T = (I + N)^-1
+//   D   = U - W S,  U = T diag(beta) V,  W = T diag(beta exp G) K
+//   O   = diag(exp G) Q S + [exp(G_t - G_j) q_t.k_j]_{j<=t} D
+//   S_T = exp(G_T) S + K^T diag(exp(G_T - G)) D
+//
+// One CTA of 8 warps per (sequence, v-head) walks the sequence's blocks in order.  Per
+// block, the warps first build the state-independent operands together in shared
+// memory (cumsum G, the decay-masked Grams, T by block doubling, W), then each warp
+// carries 16 of the 128 value columns through the dependent part on its own: its slice
+// of the state, S^T[16 columns][128 keys], stays in mma accumulators for the whole
+// sequence and feeds the next products directly as A fragments, so the state never
+// goes through shared memory and the warps never exchange data inside the chain:
+//   D^T  = V^T T_u^T - S^T W^T        (starts from U^T, subtracts the state part)
+//   O^T  = exp(G) S^T Q^T + D^T A^T
+//   S^T <- exp(G_T) S^T + (D^T diag(exp(G_T - G))) K
+// This needs no workspace.  With one CTA per head it suits batches of at least about
+// one CTA per SM; few-head batches use the two-pass path (chunk_bf16.cu), which spreads
+// each head over several CTAs.
+// Precision as in the two-pass path: q, k, v enter exactly; T, the state, D and A are
+// carried as bf16 (hi, lo) pairs; W is rounded to bf16 once; fp32 accumulation.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kFRowB = kD * 2;
+constexpr int kFThreads = 256;
+
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  split_bf16(x0, x1, hi, lo);
+}
+
+// acc (16x8) += A[r0.., k0..k0+16) * B[k0.., n0..n0+8), fp32 row-major shared matrices,
+// as hi*hi + lo*hi + hi*lo of their bf16 splits.
+__device__ __forceinline__ void mma_f32x3f(float (&acc)[4], const float *A, int lda,
+                                           const float *B, int ldb, int r0, int k0, int n0,
+                                           int lane) {
+  const int gid = lane >> 2, tig = lane & 3;
+  uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+  const float *a0 = A + (r0 + gid) * lda + k0 + 2 * tig;
+  const float *a1 = a0 + 8 * lda;
+  split_pair(a0[0], a0[1], ah[0], al[0]);
+  split_pair(a1[0], a1[1], ah[1], al[1]);
+  split_pair(a0[8], a0[9], ah[2], al[2]);
+  split_pair(a1[8], a1[9], ah[3], al[3]);
+  const float *b0 = B + (k0 + 2 * tig) * ldb + n0 + gid;
+  split_pair(b0[0], b0[ldb], bh0, bl0);
+  split_pair(b0[8 * ldb], b0[9 * ldb], bh1, bl1);
+  mma_bf16(acc, ah, bh0, bh1);
+  mma_bf16(acc, al, bh0, bh1);
+  mma_bf16(acc, ah, bl0, bl1);
+}
+
+template <int C, typename TO>
+struct FusedSmem {
+  alignas(128) char K[C * kFRowB];
+  alignas(128) char Q[C * kFRowB];
+  alignas(128) char V[C * kFRowB];
+  alignas(128) char W[C * kFRowB];
+  alignas(128) char Ah[C * 2 * C];
+  alignas(128) char Al[C * 2 * C];
+  alignas(128) char TWh[C * 2 * C];
+  alignas(128) char TWl[C * 2 * C];
+  alignas(128) char TUh[C * 2 * C];
+  alignas(128) char TUl[C * 2 * C];
+  float N[C][C + 4];
+  float T[C][C + 4];
+  float M[32 * 33];
+  float G[C], EG[C], B[C], gRaw[C], bRaw[C];
+  alignas(16) TO O[8][C][16];
+};
+
+// A fragment (16 rows x 16 k) from two 16x8 accumulator tiles (k = their column index),
+// scaled per column by f0 (first tile) / f1 (second tile) pairs, as bf16 (hi, lo).
+__device__ __forceinline__ void acc_to_frag(const float (&x)[4], const float (&y)[4], float s0,
+                                            float s1, float t0, float t1, uint32_t (&hi)[4],
+                                            uint32_t (&lo)[4]) {
+  split_pair(x[0] * s0, x[1] * s1, hi[0], lo[0]);
+  split_pair(x[2] * s0, x[3] * s1, hi[1], lo[1]);
+  split_pair(y[0] * t0, y[1] * t1, hi[2], lo[2]);
+  split_pair(y[2] * t0, y[3] * t1, hi[3], lo[3]);
+}
+
+template <int C, typename TO>
+__global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
+  constexpr int NW = kFThreads / 32, NT = kFThreads, MT = C / 16, RB = 2 * C, LD = C + 4;
+  constexpr int NTC = C / 8;  // 8-wide token tiles
+  using Smem = FusedSmem<C, TO>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int n = blockIdx.x / p.hv;
+  const int h = blockIdx.x - n * p.hv;
+  const int kh = h / (p.hv / p.hk);
+  const int j0 = 16 * warp;  // this warp's value columns
+  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+  const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
+  const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
+  TO *o = static_cast<TO *>(p.o);
+
+  int bos, eos;
+  seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
+  const int nchunks = (eos - bos + C - 1) / C;
+  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD;
+
+  // S^T[j][i] for j = j0 + gid (+8), i = 8nt + 2tig (+1): 16 accumulator tiles
+  float S[16][4];
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = 8 * nt + 2 * tig + (e & 1), j = j0 + gid + 8 * (e >> 1);
+      S[nt][e] = p.state_in ? p.state_in[sbase + (size_t)i * kD + j] : 0.f;
+    }
+
+#pragma unroll 1
+  for (int c = 0; c < nchunks; ++c) {
+    const int tok0 = bos + c * C;
+    const int L = min(C, eos - tok0);
+    __syncthreads();  // the previous block is done with shared memory
+    for (int e = tid; e < C * 16; e += NT) {
+      const int r = e >> 4, gr = e & 15;
+      const bool ok = r < L;
+      const size_t tok = (size_t)tok0 + (ok ? r : 0);
+      const int nb = ok ? 16 : 0;
+      cp_async16(sm.K + swz<kFRowB>(r, gr * 16), k + (tok * p.hk + kh) * kD + gr * 8, nb);
+      cp_async16(sm.Q + swz<kFRowB>(r, gr * 16), q + (tok * p.hk + kh) * kD + gr * 8, nb);
+      cp_async16(sm.V + swz<kFRowB>(r, gr * 16), v + (tok * p.hv + h) * kD + gr * 8, nb);
+    }
+    for (int t = tid; t < C; t += NT) {
+      const bool ok = t < L;
+      const size_t gi = ((size_t)tok0 + (ok ? t : 0)) * p.hv + h;
+      cp_async4(&sm.gRaw[t], p.g + gi, ok ? 4 : 0);
+      cp_async4(&sm.bRaw[t], p.beta + gi, ok ? 4 : 0);
+    }
+    cp_async_commit();
+    for (int e = tid; e < C * LD; e += NT) (&sm.T[0][0])[e] = 0.f;
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // in-block inclusive cumsum of g (padding contributes 0), exp(G), beta
+    if (warp == 0) {
+      constexpr int E = (C + 31) / 32;
+      float gv[E], bv[E], run = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int t = lane * E + e;
+        gv[e] = t < C ? sm.gRaw[t] : 0.f;
+        bv[e] = t < C ? sm.bRaw[t] : 0.f;
+        run += gv[e];
+        gv[e] = run;
+      }
+      float incl = run;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const float excl = incl - run;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int t = lane * E + e;
+        if (t < C) {
+          sm.G[t] = gv[e] + excl;
+          sm.EG[t] = __expf(gv[e] + excl);
+          sm.B[t] = bv[e];
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- decay-masked Grams: N (fp32) and the causal A (bf16 hi, lo)
+#pragma unroll 1
+    for (int item = warp; item < 2 * MT; item += NW) {
+      const int prod = item / MT;  // 0: K K^T, 1: Q K^T
+      const int mt = item % MT;
+      const char *Asrc = prod ? sm.Q : sm.K;
+      float acc[NTC][4];
+#pragma unroll
+      for (int a = 0; a < NTC; ++a)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < kD / 16; ++ks) {
+        uint32_t a[4];
+        lda_tile<kFRowB>(a, Asrc, 16 * mt, 16 * ks, lane);
+#pragma unroll
+        for (int np = 0; np < MT; ++np) {
+          if (np <= mt) {
+            uint32_t b[4];
+            ldb_nk<kFRowB>(b, sm.K, 16 * np, 16 * ks, lane);
+            mma_bf16(acc[2 * np], a, b[0], b[1]);
+            mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NTC; ++nt)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int t = 16 * mt + gid + 8 * hr, j = 8 * nt + 2 * tig;
+          float x0 = 0.f, x1 = 0.f;
+          if (nt <= 2 * mt + 1) {
+            const float d0 = __expf(sm.G[t] - sm.G[j]), d1 = __expf(sm.G[t] - sm.G[j + 1]);
+            if (prod == 0) {
+              x0 = (j < t) ? sm.B[t] * d0 * acc[nt][2 * hr] : 0.f;
+              x1 = (j + 1 < t) ? sm.B[t] * d1 * acc[nt][2 * hr + 1] : 0.f;
+            } else {
+              x0 = (j <= t) ? d0 * acc[nt][2 * hr] : 0.f;
+              x1 = (j + 1 <= t) ? d1 * acc[nt][2 * hr + 1] : 0.f;
+            }
+          }
+          if (prod == 0) {
+            if (nt <= 2 * mt + 1) {
+              sm.N[t][j] = x0;
+              sm.N[t][j + 1] = x1;
+            }
+          } else {
+            uint32_t hi, lo;
+            split_pair(x0, x1, hi, lo);
+            *reinterpret_cast<uint32_t *>(sm.Ah + swz<RB>(t, 2 * j)) = hi;
+            *reinterpret_cast<uint32_t *>(sm.Al + swz<RB>(t, 2 * j)) = lo;
+          }
+        }
+    }
+    __syncthreads();
+
+    // ---- T = (I + N)^-1 by block doubling (16x16 forward substitution, then MMA levels)
+    if (tid < C) {
+      const int base = (tid >> 4) * 16, cc = tid & 15;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float val = (r == cc) ? 1.f : 0.f;
+        if (r > cc) {
+          float acc = 0.f;
+#pragma unroll
+          for (int m = 0; m < r; ++m)
+            if (m >= cc) acc += sm.N[base + r][base + m] * x[m];
+          val = -acc;
+        }
+        x[r] = val;
+        sm.T[base + r][base + cc] = val;
+      }
+    }
+    __syncthreads();
+    if (C >= 32) {
+      const int pr = warp >> 1, top = 32 * pr, bot = top + 16, n0 = 8 * (warp & 1);
+      const bool act = warp < 2 * (C / 32);
+      if (act) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f32x3f(acc, &sm.N[bot][top], LD, &sm.T[top][top], LD, 0, 0, n0, lane);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sm.M[pr * 256 + (gid + 8 * (e >> 1)) * 16 + n0 + 2 * tig + (e & 1)] = acc[e];
+      }
+      __syncthreads();
+      if (act) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f32x3f(acc, &sm.T[bot][bot], LD, &sm.M[pr * 256], 16, 0, 0, n0, lane);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sm.T[bot + gid + 8 * (e >> 1)][top + n0 + 2 * tig + (e & 1)] = -acc[e];
+      }
+      __syncthreads();
+    }
+    if (C == 64) {
+      const int r0 = 16 * ((warp >> 1) & 1), nb = 16 * (warp & 1);
+      const bool act = warp < 4;
+      if (act) {
+        float acc[2][4] = {};
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+            mma_f32x3f(acc[a], &sm.N[32][0], LD, &sm.T[0][0], LD, r0, 16 * ks, nb + 8 * a, lane);
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            sm.M[(r0 + gid + 8 * (e >> 1)) * 33 + nb + 8 * a + 2 * tig + (e & 1)] = acc[a][e];
+      }
+      __syncthreads();
+      if (act) {
+        float acc[2][4] = {};
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+            mma_f32x3f(acc[a], &sm.T[32][32], LD, sm.M, 33, r0, 16 * ks, nb + 8 * a, lane);
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            sm.T[32 + r0 + gid + 8 * (e >> 1)][nb + 8 * a + 2 * tig + (e & 1)] = -acc[a][e];
+      }
+      __syncthreads();
+    }
+
+    // ---- bf16 operands T diag(beta exp G) and T diag(beta), each as high + low part
+    for (int e = tid; e < C * C / 2; e += NT) {
+      const int t = e / (C / 2), j = 2 * (e % (C / 2));
+      const float x0 = sm.T[t][j], x1 = sm.T[t][j + 1];
+      uint32_t hi, lo;
+      split_pair(x0 * sm.B[j] * sm.EG[j], x1 * sm.B[j + 1] * sm.EG[j + 1], hi, lo);
+      *reinterpret_cast<uint32_t *>(sm.TWh + swz<RB>(t, 2 * j)) = hi;
+      *reinterpret_cast<uint32_t *>(sm.TWl + swz<RB>(t, 2 * j)) = lo;
+      split_pair(x0 * sm.B[j], x1 * sm.B[j + 1], hi, lo);
+      *reinterpret_cast<uint32_t *>(sm.TUh + swz<RB>(t, 2 * j)) = hi;
+      *reinterpret_cast<uint32_t *>(sm.TUl + swz<RB>(t, 2 * j)) = lo;
+    }
+    __syncthreads();
+
+    // ---- W = T diag(beta e^G) K  [t][i], this warp's 16 key columns
+    {
+      const int i0 = 16 * warp;
+#pragma unroll 1
+      for (int mt = 0; mt < MT; ++mt) {
+        float acc[2][4] = {};
+        for (int ks = 0; ks <= mt; ++ks) {
+          uint32_t ah[4], al[4], b[4];
+          lda_tile<RB>(ah, sm.TWh, 16 * mt, 16 * ks, lane);
+          lda_tile<RB>(al, sm.TWl, 16 * mt, 16 * ks, lane);
+          ldb_kn<kFRowB>(b, sm.K, 16 * ks, i0, lane);
+          mma_bf16(acc[0], ah, b[0], b[1]);
+          mma_bf16(acc[0], al, b[0], b[1]);
+          mma_bf16(acc[1], ah, b[2], b[3]);
+          mma_bf16(acc[1], al, b[2], b[3]);
+        }
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int t = 16 * mt + gid + 8 * hr, col = i0 + 8 * a + 2 * tig;
+            *reinterpret_cast<uint32_t *>(sm.W + swz<kFRowB>(t, 2 * col)) =
+                pack_bf16(acc[a][2 * hr], acc[a][2 * hr + 1]);
+          }
+      }
+    }
+    __syncthreads();
+
+    // ================= per-warp state chain for value columns j0 .. j0+15
+    // D^T = V^T T_u^T  (U^T), then minus S^T W^T
+    float Dc[NTC][4];
+#pragma unroll
+    for (int a = 0; a < NTC; ++a)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) Dc[a][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < MT; ++ks) {
+      uint32_t a[4];
+      lda_tile_t<kFRowB>(a, sm.V, j0, 16 * ks, lane);
+#pragma unroll
+      for (int np = 0; np < MT; ++np) {
+        if (np >= ks) {
+          uint32_t bh[4], bl[4];
+          ldb_nk<RB>(bh, sm.TUh, 16 * np, 16 * ks, lane);
+          ldb_nk<RB>(bl, sm.TUl, 16 * np, 16 * ks, lane);
+          mma_bf16(Dc[2 * np], a, bh[0], bh[1]);
+          mma_bf16(Dc[2 * np], a, bl[0], bl[1]);
+          mma_bf16(Dc[2 * np + 1], a, bh[2], bh[3]);
+          mma_bf16(Dc[2 * np + 1], a, bl[2], bl[3]);
+        }
+      }
+    }
+    float Rc[NTC][4];
+#pragma unroll
+    for (int a = 0; a < NTC; ++a)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) Rc[a][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kD / 16; ++ks) {
+      uint32_t sh[4], sl[4], nh[4], nl[4];
+      acc_to_frag(S[2 * ks], S[2 * ks + 1], 1.f, 1.f, 1.f, 1.f, sh, sl);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        nh[e] = sh[e] ^ 0x80008000u;  // -S
+        nl[e] = sl[e] ^ 0x80008000u;
+      }
+#pragma unroll
+      for (int np = 0; np < MT; ++np) {
+        uint32_t bw[4], bq[4];
+        ldb_nk<kFRowB>(bw, sm.W, 16 * np, 16 * ks, lane);
+        ldb_nk<kFRowB>(bq, sm.Q, 16 * np, 16 * ks, lane);
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          mma_bf16(Dc[2 * np + a], nh, bw[2 * a], bw[2 * a + 1]);
+          mma_bf16(Dc[2 * np + a], nl, bw[2 * a], bw[2 * a + 1]);
+          mma_bf16(Rc[2 * np + a], sh, bq[2 * a], bq[2 * a + 1]);
+          mma_bf16(Rc[2 * np + a], sl, bq[2 * a], bq[2 * a + 1]);
+        }
+      }
+    }
+    const float gC = sm.G[C - 1];
+    // O^T = exp(G) R^T + D^T A^T over the causal part
+#pragma unroll
+    for (int nt = 0; nt < NTC; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) Rc[nt][e] *= sm.EG[8 * nt + 2 * tig + (e & 1)];
+#pragma unroll
+    for (int ks = 0; ks < MT; ++ks) {
+      uint32_t dh[4], dl[4];
+      acc_to_frag(Dc[2 * ks], Dc[2 * ks + 1], 1.f, 1.f, 1.f, 1.f, dh, dl);
+#pragma unroll
+      for (int np = 0; np < MT; ++np) {
+        if (np >= ks) {
+          uint32_t bh[4], bl[4];
+          ldb_nk<RB>(bh, sm.Ah, 16 * np, 16 * ks, lane);
+          ldb_nk<RB>(bl, sm.Al, 16 * np, 16 * ks, lane);
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
+            mma_bf16(Rc[2 * np + a], dh, bh[2 * a], bh[2 * a + 1]);
+            mma_bf16(Rc[2 * np + a], dl, bh[2 * a], bh[2 * a + 1]);
+            mma_bf16(Rc[2 * np + a], dh, bl[2 * a], bl[2 * a + 1]);
+          }
+        }
+      }
+    }
+    // stage O^T [j][t] as rows t and store this warp's 16 columns of the valid rows
+#pragma unroll
+    for (int nt = 0; nt < NTC; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        Elem<TO>::store(&sm.O[warp][8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)], Rc[nt][e]);
+    __syncwarp();
+    {
+      constexpr int EPG = 16 / sizeof(TO);
+      constexpr int GPR = 16 / EPG;
+      for (int e = lane; e < C * GPR; e += 32) {
+        const int t = e / GPR, gi = e % GPR;
+        if (t < L)
+          *reinterpret_cast<uint4 *>(o + ((size_t)(tok0 + t) * p.hv + h) * kD + j0 + gi * EPG) =
+              *reinterpret_cast<const uint4 *>(&sm.O[warp][t][gi * EPG]);
+      }
+    }
+    // S^T <- exp(G_T) S^T + (D^T diag(exp(G_T - G))) K
+    const float egc = __expf(gC);
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) S[nt][e] *= egc;
+#pragma unroll
+    for (int ks = 0; ks < MT; ++ks) {
+      const int t0 = 16 * ks + 2 * tig;
+      uint32_t th[4], tl[4];
+      acc_to_frag(Dc[2 * ks], Dc[2 * ks + 1], __expf(gC - sm.G[t0]), __expf(gC - sm.G[t0 + 1]),
+                  __expf(gC - sm.G[t0 + 8]), __expf(gC - sm.G[t0 + 9]), th, tl);
+#pragma unroll
+      for (int np = 0; np < 8; ++np) {
+        uint32_t b[4];
+        ldb_kn<kFRowB>(b, sm.K, 16 * ks, 16 * np, lane);
+        mma_bf16(S[2 * np], th, b[0], b[1]);
+        mma_bf16(S[2 * np], tl, b[0], b[1]);
+        mma_bf16(S[2 * np + 1], th, b[2], b[3]);
+        mma_bf16(S[2 * np + 1], tl, b[2], b[3]);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = 8 * nt + 2 * tig + (e & 1), j = j0 + gid + 8 * (e >> 1);
+      p.state_out[sbase + (size_t)i * kD + j] = S[nt][e];
+    }
+}
+
+template <int C, typename TO>
+cudaError_t launch_fused_t(const ChunkParams &p, cudaStream_t stream) {
+  const size_t smem = sizeof(FusedSmem<C, TO>);
+  cudaError_t err = cudaFuncSetAttribute(fused_kernel<C, TO>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  fused_kernel<C, TO><<<(unsigned)((long long)p.num_seqs * p.hv), kFThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int C>
+cudaError_t launch_fused_c(const ChunkParams &p, cudaStream_t stream) {
+  return p.o_fp32 ? launch_fused_t<C, float>(p, stream) : launch_fused_t<C, __nv_bfloat16>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_fused(const ChunkParams &p, cudaStream_t stream) {
+  if ((long long)p.num_seqs * p.hv == 0) return cudaSuccess;
+  switch (p.chunk) {
+    case 16: return launch_fused_c<16>(p, stream);
+    case 32: return launch_fused_c<32>(p, stream);
+    case 64: return launch_fused_c<64>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gdn

@@ -20,6 +20,8 @@ gdn_status check_shape(const gdn_shape *s, bool needs_chunk) {
   if (s->dk != gdn::kD || s->dv != gdn::kD) return GDN_ERR_UNSUPPORTED;
   if (s->qkv_dtype != GDN_F32 && s->qkv_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if (s->o_fp32 != 0 && s->o_fp32 != 1) return GDN_ERR_INVALID_ARG;
+  if (s->algo != GDN_ALGO_AUTO && s->algo != GDN_ALGO_TWO_PASS && s->algo != GDN_ALGO_SINGLE_PASS)
+    return GDN_ERR_INVALID_ARG;
   if (needs_chunk && s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return GDN_ERR_UNSUPPORTED;
   // grids are sized (sequences x v-heads x 8) in one dimension
   if ((long long)s->num_seqs * s->num_v_heads * 8 > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
@@ -65,6 +67,18 @@ size_t state_bytes(const gdn_shape *s) {
 
 gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
 
+// bf16 chunked pass: one CTA per (sequence, v-head) without workspace, or two passes
+bool single_pass(const gdn_shape *s) {
+  if (s->algo == GDN_ALGO_SINGLE_PASS) return true;
+  if (s->algo == GDN_ALGO_TWO_PASS) return false;
+  return (long long)s->num_seqs * s->num_v_heads >= GDN_SINGLE_PASS_MIN_HEADS;
+}
+
+size_t chunked_workspace(const gdn_shape *s) {
+  if (s->qkv_dtype == GDN_F32 || single_pass(s)) return 0;
+  return gdn::chunk_workspace_bytes(s->total_tokens, s->num_seqs, s->num_v_heads, s->chunk);
+}
+
 gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes, void *stream) {
   const gdn_shape *s = c.s;
   ChunkParams p{};
@@ -86,8 +100,8 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   p.o = c.o;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s->qkv_dtype == GDN_F32) return cuda_status(gdn::launch_chunk_f32(p, st));
-  const size_t need =
-      gdn::chunk_workspace_bytes(s->total_tokens, s->num_seqs, s->num_v_heads, s->chunk);
+  if (single_pass(s)) return cuda_status(gdn::launch_chunk_fused(p, st));
+  const size_t need = chunked_workspace(s);
   if (need > 0 && (!workspace || workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return GDN_ERR_WORKSPACE;
@@ -106,8 +120,7 @@ size_t gdn_workspace_size(const gdn_shape *s, int op) {
   if (op != GDN_OP_PREFILL && op != GDN_OP_DECODE && op != GDN_OP_VERIFY) return (size_t)-1;
   const bool chunked = (op == GDN_OP_PREFILL || op == GDN_OP_VERIFY);
   if (check_shape(s, chunked) != GDN_OK) return (size_t)-1;
-  if (!chunked || s->qkv_dtype == GDN_F32) return 0;
-  return gdn::chunk_workspace_bytes(s->total_tokens, s->num_seqs, s->num_v_heads, s->chunk);
+  return chunked ? chunked_workspace(s) : 0;
 }
 
 const char *gdn_status_string(gdn_status status) {

@@ -77,6 +77,19 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
 typedef enum { GDN_OP_PREFILL = 0, GDN_OP_DECODE = 1, GDN_OP_VERIFY = 2 } gdn_op;
 
+/* Kernel schedule of the bf16 chunked pass (prefill and verify); f32 q/k/v have one.
+ *   TWO_PASS     a parallel pass over all blocks of all heads builds the state-free
+ *                operands into the workspace, then a second pass walks each head's
+ *                blocks in order, spread over 8 CTAs per head.  Suits few heads.
+ *   SINGLE_PASS  one CTA per (sequence, v-head) builds the operands and walks the
+ *                blocks itself; no workspace.  Suits batches of >= ~1 head per SM.
+ *   AUTO         SINGLE_PASS when num_seqs * num_v_heads >= GDN_SINGLE_PASS_MIN_HEADS,
+ *                else TWO_PASS (a rule of the shape alone, so that
+ *                gdn_workspace_size does not depend on the device).
+ * Both give results within the same bounds; they are not bit-identical to each other. */
+typedef enum { GDN_ALGO_AUTO = 0, GDN_ALGO_TWO_PASS = 1, GDN_ALGO_SINGLE_PASS = 2 } gdn_algo;
+#define GDN_SINGLE_PASS_MIN_HEADS 128
+
 typedef struct {
   int32_t num_seqs;      /* N >= 0                                                  */
   int32_t total_tokens;  /* = cu_seqlens[N]; decode without cu_seqlens: = N         */
@@ -88,6 +101,7 @@ typedef struct {
   int32_t o_fp32;        /* 0: o has qkv_dtype; 1: o is float32 (the unrounded       */
                          /* fp32 result; the bf16 o of the same call is exactly its  */
                          /* round-to-nearest-even rounding)                          */
+  int32_t algo;          /* a gdn_algo; 0 = GDN_ALGO_AUTO                            */
 } gdn_shape;
 
 /*
@@ -98,8 +112,8 @@ typedef struct {
  * GDN_ERR_ALIAS.  bf16 q/k/v: products on tensor cores with fp32 accumulation, the
  * state kept in fp32.  f32 q/k/v: all arithmetic in fp32 on CUDA cores.
  * workspace: at least gdn_workspace_size(shape, GDN_OP_PREFILL) bytes, 256-byte
- * aligned (may be NULL when that size is 0); its contents on entry do not matter and
- * are unspecified on return.
+ * aligned (may be NULL when that size is 0, as for f32 q/k/v and the bf16 single-pass
+ * schedule); its contents on entry do not matter and are unspecified on return.
  */
 gdn_status gdn_prefill_chunked(const gdn_shape *shape, const void *q, const void *k,
                                const void *v, const float *g, const float *beta,

@@ -37,10 +37,12 @@ def to_np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def gpu_prefill(x, wl, chunk=None, state_in=True, inplace=False, verify=False, o_fp32=False):
+def gpu_prefill(x, wl, chunk=None, state_in=True, inplace=False, verify=False, o_fp32=False,
+                algo=0):
     """Run the chunked path (or verify) on the seeded inputs; returns (o, state_out, dev).
 
-    o_fp32: ask for the unrounded fp32 output even when q/k/v are bf16."""
+    o_fp32: ask for the unrounded fp32 output even when q/k/v are bf16.
+    algo: the bf16 schedule (0 auto, 1 two-pass, 2 single-pass)."""
     import torch
     import gated_deltanet_linear_05_gb300 as gdn
     d = device_inputs(x, wl.dtype)
@@ -55,7 +57,7 @@ def gpu_prefill(x, wl, chunk=None, state_in=True, inplace=False, verify=False, o
                    dtype=torch.float32 if o_fp32 else d["v"].dtype)
     fn = gdn.gdn_verify_block if verify else gdn.gdn_prefill_chunked
     o, s = fn(d["q"], d["k"], d["v"], d["g"], d["beta"], s_in, s_out, d["cu_seqlens"], o,
-              chunk=chunk or wl.chunk)
+              chunk=chunk or wl.chunk, algo=algo)
     torch.cuda.synchronize()
     d["o_raw"] = o
     return to_np(o), to_np(s), d

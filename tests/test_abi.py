@@ -41,7 +41,7 @@ def test_status_strings(L):
 
 
 def test_workspace_size(L):
-    sh = gdn.make_shape(8, 4096, 16, 32, chunk=64)
+    sh = gdn.make_shape(8, 4096, 16, 32, chunk=64, algo=gdn.GDN_ALGO_TWO_PASS)
     n = gdn.gdn_workspace_size(sh, gdn.GDN_OP_PREFILL)
     rows = 4096 * 32
     assert n >= rows * (128 * 2 + 128 * 4 + 64 * 2 + 4)
@@ -53,6 +53,22 @@ def test_workspace_size(L):
         gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, dk=64), gdn.GDN_OP_PREFILL)
     with pytest.raises(gdn.GdnError):
         gdn.gdn_workspace_size(sh, 7)
+
+
+def test_workspace_size_follows_the_schedule(L):
+    """The single-pass schedule needs no workspace; AUTO picks it from the head count."""
+    for n, hv in [(8, 32), (1, 16), (127, 1), (128, 1), (2, 64)]:
+        two = gdn.gdn_workspace_size(gdn.make_shape(n, 64 * n, 1, hv, chunk=64,
+                                                    algo=gdn.GDN_ALGO_TWO_PASS), gdn.GDN_OP_PREFILL)
+        one = gdn.gdn_workspace_size(gdn.make_shape(n, 64 * n, 1, hv, chunk=64,
+                                                    algo=gdn.GDN_ALGO_SINGLE_PASS),
+                                     gdn.GDN_OP_PREFILL)
+        auto = gdn.gdn_workspace_size(gdn.make_shape(n, 64 * n, 1, hv, chunk=64),
+                                      gdn.GDN_OP_VERIFY)
+        assert two > 0 and one == 0
+        assert auto == (0 if n * hv >= gdn.GDN_SINGLE_PASS_MIN_HEADS else two)
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, algo=3), gdn.GDN_OP_PREFILL)
 
 
 # fake, well-aligned device addresses: every call below must fail validation first
@@ -74,6 +90,7 @@ def test_validation(L, name):
     assert _call(L, name, gdn.make_shape(2, 10, 2, 3)) == gdn.GDN_ERR_INVALID_ARG   # Hv % Hk
     assert _call(L, name, gdn.make_shape(-1, 10, 1, 1)) == gdn.GDN_ERR_INVALID_ARG
     assert _call(L, name, gdn.make_shape(2, 10, 1, 2, dtype=5)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _call(L, name, gdn.make_shape(2, 10, 1, 2, algo=-1)) == gdn.GDN_ERR_INVALID_ARG
     assert _call(L, name, ok_shape, q=None) == gdn.GDN_ERR_INVALID_ARG
     assert _call(L, name, ok_shape, o=None) == gdn.GDN_ERR_INVALID_ARG
     assert _call(L, name, ok_shape, s_out=None) == gdn.GDN_ERR_INVALID_ARG

@@ -19,6 +19,8 @@ from gdn_testlib import device_inputs, gpu_prefill, half_ulp_bf16, rel_err, to_n
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": 1e-4, "bf16": 2e-2}
+# the two kernel schedules of the bf16 chunked pass (f32 q/k/v have one)
+ALGOS = {"two_pass": 1, "single_pass": 2}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -67,49 +69,80 @@ def test_chunk_vs_sequential_fp32_T64_C16():
     _check(o, s, o_ref, s_ref, "f32")
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+SMALL_CASES = [([1], 1, 1), ([2], 1, 1), ([15], 1, 2), ([16], 2, 2), ([17], 1, 1),
+               ([63, 64, 65], 1, 2), ([200, 3, 129], 2, 4), ([0, 70, 0, 1], 1, 1)]
+
+
 @pytest.mark.parametrize("chunk", [16, 32, 64])
-@pytest.mark.parametrize("lengths,hk,hv", [
-    ([1], 1, 1), ([2], 1, 1), ([15], 1, 2), ([16], 2, 2), ([17], 1, 1),
-    ([63, 64, 65], 1, 2), ([200, 3, 129], 2, 4), ([0, 70, 0, 1], 1, 1)])
-def test_prefill_small_shapes(dtype, chunk, lengths, hk, hv):
-    wl = gi.Workload("small", lengths, hk, hv, chunk=chunk, dtype=dtype, s0_scale=0.1)
+@pytest.mark.parametrize("lengths,hk,hv", SMALL_CASES)
+def test_prefill_small_shapes_f32(chunk, lengths, hk, hv):
+    wl = gi.Workload("small", lengths, hk, hv, chunk=chunk, dtype="f32", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=len(lengths) + chunk)
     o_ref, s_ref = _oracle(x)
     _run_and_check(x, wl, o_ref, s_ref, "T=%s C=%d" % (lengths, chunk))
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_prefill_zero_initial_state_and_in_place(dtype):
+@pytest.mark.parametrize("algo", list(ALGOS))
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+@pytest.mark.parametrize("lengths,hk,hv", SMALL_CASES)
+def test_prefill_small_shapes_bf16(algo, chunk, lengths, hk, hv):
+    wl = gi.Workload("small", lengths, hk, hv, chunk=chunk, dtype="bf16", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=len(lengths) + chunk)
+    o_ref, s_ref = _oracle(x)
+    _run_and_check(x, wl, o_ref, s_ref, "T=%s C=%d %s" % (lengths, chunk, algo),
+                   algo=ALGOS[algo])
+
+
+@pytest.mark.parametrize("dtype,algo", [("f32", None), ("bf16", "two_pass"),
+                                        ("bf16", "single_pass")])
+def test_prefill_zero_initial_state_and_in_place(dtype, algo):
+    kw = {"algo": ALGOS[algo]} if algo else {}
     wl = gi.Workload("small", [37, 90], 2, 2, chunk=32, dtype=dtype, s0_scale=0.1)
     x = gi.make_inputs(wl, seed=7)
     o_ref, s_ref = _oracle(x)
-    _run_and_check(x, wl, o_ref, s_ref, "in place", inplace=True)
+    _run_and_check(x, wl, o_ref, s_ref, "in place", inplace=True, **kw)
     x0 = dict(x, state0=None)
     o_ref0, s_ref0 = _oracle(x0)
-    _run_and_check(x0, wl, o_ref0, s_ref0, "zero state", state_in=False)
+    _run_and_check(x0, wl, o_ref0, s_ref0, "zero state", state_in=False, **kw)
 
 
-def test_prefill_slow_decay_bf16():
+@pytest.mark.parametrize("algo", list(ALGOS))
+def test_prefill_slow_decay_bf16(algo):
     """g = -0.01 softplus(.): the state carries across many blocks."""
     wl = gi.Workload("slow", [1000], 1, 2, chunk=64, dtype="bf16", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=11, gate_scale=0.01)
     o_ref, s_ref = _oracle(x)
-    _run_and_check(x, wl, o_ref, s_ref, "slow decay")
+    _run_and_check(x, wl, o_ref, s_ref, "slow decay", algo=ALGOS[algo])
 
 
-def test_prefill_T4096_H16_full():
+@pytest.mark.parametrize("algo", list(ALGOS))
+def test_prefill_T4096_H16_full(algo):
     wl = gi.prefill_t4096_h16()
     x = gi.make_inputs(wl)
     o_ref, s_ref = _oracle(x)
-    _run_and_check(x, wl, o_ref, s_ref, "T=4096")
+    _run_and_check(x, wl, o_ref, s_ref, "T=4096", algo=ALGOS[algo])
+
+
+def test_many_heads_take_the_single_pass_schedule_by_default():
+    """AUTO: at least GDN_SINGLE_PASS_MIN_HEADS (sequence, head) pairs -> single pass,
+    which is bit-identical to asking for it."""
+    import gated_deltanet_linear_05_gb300 as gdn
+    wl = gi.Workload("many", [5, 40, 17, 64] * 8, 2, 4, chunk=32, dtype="bf16", s0_scale=0.1)
+    assert wl.num_seqs * wl.num_v_heads >= gdn.GDN_SINGLE_PASS_MIN_HEADS
+    x = gi.make_inputs(wl, seed=21)
+    o_ref, s_ref = _oracle(x)
+    _run_and_check(x, wl, o_ref, s_ref, "many heads")
+    o_a, s_a, _ = gpu_prefill(x, wl, o_fp32=True)
+    o_1, s_1, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS["single_pass"])
+    assert np.array_equal(o_a, o_1) and np.array_equal(s_a, s_1)
 
 
 @pytest.mark.slow
-def test_varlen_N8_Hk16_Hv32_sampled():
+@pytest.mark.parametrize("algo", list(ALGOS))
+def test_varlen_N8_Hk16_Hv32_sampled(algo):
     wl = gi.varlen_8seq_hk16_hv32()
     x = gi.make_inputs(wl)
-    o, s, _ = gpu_prefill(x, wl, o_fp32=True)
+    o, s, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS[algo])
     rng = np.random.default_rng(0)
     pairs = [(n, int(h)) for n in range(8) for h in rng.choice(32, 2, replace=False)]
     o_ref, s_ref = _oracle(x, pairs=pairs)
@@ -121,7 +154,8 @@ def test_varlen_N8_Hk16_Hv32_sampled():
 
 # ------------------------------------------------------------------ verify
 
-def test_verify_B128_H32_T16_full():
+@pytest.mark.parametrize("algo", list(ALGOS))
+def test_verify_B128_H32_T16_full(algo):
     import torch
     wl = gi.verify_b128_h32()
     x = gi.make_inputs(wl)
@@ -131,12 +165,12 @@ def test_verify_B128_H32_T16_full():
     o = torch.empty(d["v"].shape, dtype=torch.float32, device="cuda")
     import gated_deltanet_linear_05_gb300 as gdn
     o, s = gdn.gdn_verify_block(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
-                                d["cu_seqlens"], o, chunk=16)
+                                d["cu_seqlens"], o, chunk=16, algo=ALGOS[algo])
     torch.cuda.synchronize()
     assert torch.equal(d["state0"], snap)  # the snapshot is untouched, bit for bit
     o_ref, s_ref = _oracle(x)
     _check(to_np(o), to_np(s), o_ref, s_ref, "bf16", "verify")
-    _run_and_check(x, wl, o_ref, s_ref, "verify", verify=True)
+    _run_and_check(x, wl, o_ref, s_ref, "verify", verify=True, algo=ALGOS[algo])
 
 
 # ------------------------------------------------------------------ decode
@@ -223,19 +257,29 @@ def test_chunked_matches_gpu_decode_loop(dtype):
     _check(o_c, s_c, to_np(o_d), to_np(s_d), dtype, "chunked vs decode loop")
 
 
-def test_chunk16_matches_chunk64_bf16():
+@pytest.mark.parametrize("algo", list(ALGOS))
+def test_chunk16_matches_chunk64_bf16(algo):
     wl = gi.Workload("c", [300, 77], 2, 2, dtype="bf16", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=4)
-    o16, s16, _ = gpu_prefill(x, wl, chunk=16, o_fp32=True)
-    o64, s64, _ = gpu_prefill(x, wl, chunk=64, o_fp32=True)
+    o16, s16, _ = gpu_prefill(x, wl, chunk=16, o_fp32=True, algo=ALGOS[algo])
+    o64, s64, _ = gpu_prefill(x, wl, chunk=64, o_fp32=True, algo=ALGOS[algo])
     _check(o16, s16, o64, s64, "bf16", "C16 vs C64")
 
 
-def test_varlen_packed_matches_separate_runs_bf16():
+def test_two_schedules_agree_bf16():
+    wl = gi.Workload("c", [300, 77, 1], 2, 4, dtype="bf16", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=5)
+    o1, s1, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS["two_pass"])
+    o2, s2, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS["single_pass"])
+    _check(o2, s2, o1, s1, "bf16", "single vs two pass")
+
+
+@pytest.mark.parametrize("algo", list(ALGOS))
+def test_varlen_packed_matches_separate_runs_bf16(algo):
     lengths = [100, 5, 64]
     wl = gi.Workload("v", lengths, 1, 2, chunk=64, dtype="bf16", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=3)
-    o, s, _ = gpu_prefill(x, wl)
+    o, s, _ = gpu_prefill(x, wl, algo=ALGOS[algo])
     cu = x["cu_seqlens"]
     for n, L in enumerate(lengths):
         a, b = cu[n], cu[n + 1]
@@ -243,17 +287,18 @@ def test_varlen_packed_matches_separate_runs_bf16():
         xs["state0"] = x["state0"][n:n + 1]
         xs["cu_seqlens"] = np.array([0, L], np.int32)
         wl1 = gi.Workload("v1", [L], 1, 2, chunk=64, dtype="bf16")
-        o1, s1, _ = gpu_prefill(xs, wl1)
+        o1, s1, _ = gpu_prefill(xs, wl1, algo=ALGOS[algo])
         np.testing.assert_array_equal(o1, o[a:b])
         np.testing.assert_array_equal(s1[0], s[n])
 
 
+@pytest.mark.parametrize("algo", list(ALGOS))
 @pytest.mark.parametrize("chunk", [16, 32, 64])
-def test_repeated_runs_are_bit_identical(chunk):
+def test_repeated_runs_are_bit_identical(chunk, algo):
     """Races between warps or CTAs show up as run-to-run differences."""
     wl = gi.Workload("det", [40, 15, 130], 1, 2, chunk=chunk, dtype="bf16", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=12)
-    o0, s0, _ = gpu_prefill(x, wl, o_fp32=True)
+    o0, s0, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS[algo])
     for _ in range(8):
-        o1, s1, _ = gpu_prefill(x, wl, o_fp32=True)
+        o1, s1, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS[algo])
         assert np.array_equal(o0, o1) and np.array_equal(s0, s1)
