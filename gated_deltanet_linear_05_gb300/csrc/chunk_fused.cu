@@ -57,9 +57,13 @@ __device__ __forceinline__ void mma_f32x3f(float (&acc)[4], const float *A, int 
 
 template <int C, typename TO>
 struct FusedSmem {
-  alignas(128) char K[C * kFRowB];
-  alignas(128) char Q[C * kFRowB];
-  alignas(128) char V[C * kFRowB];
+  static constexpr int LD = C + 4;
+  static constexpr size_t kNTBytes = (size_t)2 * C * LD * 4;
+  static constexpr size_t kOBytes = (size_t)8 * C * 16 * sizeof(TO);
+  // q, k, v tiles of the current block and of the next one (prefetched)
+  alignas(128) char K[2][C * kFRowB];
+  alignas(128) char Q[2][C * kFRowB];
+  alignas(128) char V[2][C * kFRowB];
   alignas(128) char W[C * kFRowB];
   alignas(128) char Ah[C * 2 * C];
   alignas(128) char Al[C * 2 * C];
@@ -67,11 +71,12 @@ struct FusedSmem {
   alignas(128) char TWl[C * 2 * C];
   alignas(128) char TUh[C * 2 * C];
   alignas(128) char TUl[C * 2 * C];
-  float N[C][C + 4];
-  float T[C][C + 4];
+  // N and T (fp32 [C][C+4] each) while the operands are built, then the per-warp
+  // output staging [8][C][16]
+  alignas(128) char NTO[kNTBytes > kOBytes ? kNTBytes : kOBytes];
   float M[32 * 33];
-  float G[C], EG[C], B[C], gRaw[C], bRaw[C];
-  alignas(16) TO O[8][C][16];
+  float G[C], EG[C], B[C];
+  float gRaw[2][C], bRaw[2][C];
 };
 
 // A fragment (16 rows x 16 k) from two 16x8 accumulator tiles (k = their column index),
@@ -85,13 +90,18 @@ __device__ __forceinline__ void acc_to_frag(const float (&x)[4], const float (&y
   split_pair(y[2] * t0, y[3] * t1, hi[3], lo[3]);
 }
 
+// C = 16 fits two CTAs per SM (<= 128 registers), so one CTA's state load and store
+// overlap another's arithmetic
 template <int C, typename TO>
-__global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
-  constexpr int NW = kFThreads / 32, NT = kFThreads, MT = C / 16, RB = 2 * C, LD = C + 4;
+__global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(ChunkParams p) {
+  constexpr int NT = kFThreads, MT = C / 16, RB = 2 * C, LD = C + 4;
   constexpr int NTC = C / 8;  // 8-wide token tiles
   using Smem = FusedSmem<C, TO>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  float(*Nm)[LD] = reinterpret_cast<float(*)[LD]>(sm.NTO);
+  float(*Tm)[LD] = Nm + C;
+  TO(*Ost)[C][16] = reinterpret_cast<TO(*)[C][16]>(sm.NTO);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int n = blockIdx.x / p.hv;
@@ -108,6 +118,28 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
   const int nchunks = (eos - bos + C - 1) / C;
   const size_t sbase = ((size_t)n * p.hv + h) * kD * kD;
 
+  // q, k, v rows and gates of block cc into buffer buf (rows past the end: zeros)
+  auto issue_loads = [&](int cc, int buf) {
+    const int t0 = bos + cc * C, Lc = min(C, eos - t0);
+    for (int e = tid; e < C * 16; e += NT) {
+      const int r = e >> 4, gr = e & 15;
+      const bool ok = r < Lc;
+      const size_t tok = (size_t)t0 + (ok ? r : 0);
+      const int nb = ok ? 16 : 0;
+      cp_async16(sm.K[buf] + swz<kFRowB>(r, gr * 16), k + (tok * p.hk + kh) * kD + gr * 8, nb);
+      cp_async16(sm.Q[buf] + swz<kFRowB>(r, gr * 16), q + (tok * p.hk + kh) * kD + gr * 8, nb);
+      cp_async16(sm.V[buf] + swz<kFRowB>(r, gr * 16), v + (tok * p.hv + h) * kD + gr * 8, nb);
+    }
+    for (int t = tid; t < C; t += NT) {
+      const bool ok = t < Lc;
+      const size_t gi = ((size_t)t0 + (ok ? t : 0)) * p.hv + h;
+      cp_async4(&sm.gRaw[buf][t], p.g + gi, ok ? 4 : 0);
+      cp_async4(&sm.bRaw[buf][t], p.beta + gi, ok ? 4 : 0);
+    }
+  };
+  if (nchunks > 0) issue_loads(0, 0);
+  cp_async_commit();
+
   // S^T[j][i] for j = j0 + gid (+8), i = 8nt + 2tig (+1): 16 accumulator tiles
   float S[16][4];
 #pragma unroll
@@ -118,40 +150,47 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
       S[nt][e] = p.state_in ? p.state_in[sbase + (size_t)i * kD + j] : 0.f;
     }
 
+  // Gram tiles of this warp: warps 0-3 take K K^T, warps 4-7 Q K^T, each a balanced share
+  // of the causal 16x16 tiles (mt, np <= mt): np0 .. np0+n0-1 of row mt0, and for one
+  // warp at C = 64 also tile (mt1 = 0, 0)
+  const int prod = warp >> 2, qw = warp & 3;
+  int mt0 = 0, np0 = 0, n0 = 0, mt1 = -1;
+  if (C == 64) {  // rows 3: {0,1}, {2,3}; row 2: {0,1,2}; rows 1: {0,1} and 0: {0}
+    mt0 = qw < 2 ? 3 : (qw == 2 ? 2 : 1);
+    np0 = qw == 1 ? 2 : 0;
+    n0 = qw == 2 ? 3 : 2;
+    if (qw == 3) mt1 = 0;
+  } else if (C == 32) {  // row 1: {0}, {1}; row 0: {0}
+    mt0 = qw < 2 ? 1 : 0;
+    np0 = qw == 1 ? 1 : 0;
+    n0 = qw < 3 ? 1 : 0;
+  } else {
+    n0 = qw == 0 ? 1 : 0;
+  }
+
 #pragma unroll 1
   for (int c = 0; c < nchunks; ++c) {
+    const int buf = c & 1;
     const int tok0 = bos + c * C;
     const int L = min(C, eos - tok0);
     __syncthreads();  // the previous block is done with shared memory
-    for (int e = tid; e < C * 16; e += NT) {
-      const int r = e >> 4, gr = e & 15;
-      const bool ok = r < L;
-      const size_t tok = (size_t)tok0 + (ok ? r : 0);
-      const int nb = ok ? 16 : 0;
-      cp_async16(sm.K + swz<kFRowB>(r, gr * 16), k + (tok * p.hk + kh) * kD + gr * 8, nb);
-      cp_async16(sm.Q + swz<kFRowB>(r, gr * 16), q + (tok * p.hk + kh) * kD + gr * 8, nb);
-      cp_async16(sm.V + swz<kFRowB>(r, gr * 16), v + (tok * p.hv + h) * kD + gr * 8, nb);
-    }
-    for (int t = tid; t < C; t += NT) {
-      const bool ok = t < L;
-      const size_t gi = ((size_t)tok0 + (ok ? t : 0)) * p.hv + h;
-      cp_async4(&sm.gRaw[t], p.g + gi, ok ? 4 : 0);
-      cp_async4(&sm.bRaw[t], p.beta + gi, ok ? 4 : 0);
-    }
+    if (c + 1 < nchunks) issue_loads(c + 1, buf ^ 1);
     cp_async_commit();
-    for (int e = tid; e < C * LD; e += NT) (&sm.T[0][0])[e] = 0.f;
-    cp_async_wait<0>();
+    for (int e = tid; e < C * LD; e += NT) (&Tm[0][0])[e] = 0.f;
+    cp_async_wait<1>();  // this block's group has landed
     __syncthreads();
+    const char *Kb = sm.K[buf], *Qb = sm.Q[buf], *Vb = sm.V[buf];
 
-    // in-block inclusive cumsum of g (padding contributes 0), exp(G), beta
+    // in-block inclusive cumsum of g (padding contributes 0), exp(G), beta -- warp 0,
+    // while the Gram products (which do not need the gates) run
     if (warp == 0) {
       constexpr int E = (C + 31) / 32;
       float gv[E], bv[E], run = 0.f;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int t = lane * E + e;
-        gv[e] = t < C ? sm.gRaw[t] : 0.f;
-        bv[e] = t < C ? sm.bRaw[t] : 0.f;
+        gv[e] = t < C ? sm.gRaw[buf][t] : 0.f;
+        bv[e] = t < C ? sm.bRaw[buf][t] : 0.f;
         run += gv[e];
         gv[e] = run;
       }
@@ -172,57 +211,67 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
         }
       }
     }
-    __syncthreads();
 
     // ---- decay-masked Grams: N (fp32) and the causal A (bf16 hi, lo)
-#pragma unroll 1
-    for (int item = warp; item < 2 * MT; item += NW) {
-      const int prod = item / MT;  // 0: K K^T, 1: Q K^T
-      const int mt = item % MT;
-      const char *Asrc = prod ? sm.Q : sm.K;
-      float acc[NTC][4];
+    float ga[6][4];
 #pragma unroll
-      for (int a = 0; a < NTC; ++a)
+    for (int u = 0; u < 6; ++u)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
+      for (int e = 0; e < 4; ++e) ga[u][e] = 0.f;
+    {
+      const char *Asrc = prod ? Qb : Kb;
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
-        uint32_t a[4];
-        lda_tile<kFRowB>(a, Asrc, 16 * mt, 16 * ks, lane);
+        if (n0 > 0) {
+          uint32_t a[4];
+          lda_tile<kFRowB>(a, Asrc, 16 * mt0, 16 * ks, lane);
 #pragma unroll
-        for (int np = 0; np < MT; ++np) {
-          if (np <= mt) {
-            uint32_t b[4];
-            ldb_nk<kFRowB>(b, sm.K, 16 * np, 16 * ks, lane);
-            mma_bf16(acc[2 * np], a, b[0], b[1]);
-            mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+          for (int u = 0; u < 3; ++u) {
+            if (u < n0) {
+              uint32_t b[4];
+              ldb_nk<kFRowB>(b, Kb, 16 * (np0 + u), 16 * ks, lane);
+              mma_bf16(ga[2 * u], a, b[0], b[1]);
+              mma_bf16(ga[2 * u + 1], a, b[2], b[3]);
+            }
           }
         }
+        if (mt1 >= 0) {
+          uint32_t a[4], b[4];
+          lda_tile<kFRowB>(a, Asrc, 16 * mt1, 16 * ks, lane);
+          ldb_nk<kFRowB>(b, Kb, 0, 16 * ks, lane);
+          mma_bf16(ga[4], a, b[0], b[1]);
+          mma_bf16(ga[5], a, b[2], b[3]);
+        }
+      }
+    }
+    __syncthreads();  // G, EG, B written
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      int mt, np;
+      if (u < n0) {
+        mt = mt0;
+        np = np0 + u;
+      } else if (u == 2 && mt1 >= 0) {
+        mt = mt1;
+        np = 0;
+      } else {
+        continue;
       }
 #pragma unroll
-      for (int nt = 0; nt < NTC; ++nt)
+      for (int half = 0; half < 2; ++half)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
-          const int t = 16 * mt + gid + 8 * hr, j = 8 * nt + 2 * tig;
-          float x0 = 0.f, x1 = 0.f;
-          if (nt <= 2 * mt + 1) {
-            const float d0 = __expf(sm.G[t] - sm.G[j]), d1 = __expf(sm.G[t] - sm.G[j + 1]);
-            if (prod == 0) {
-              x0 = (j < t) ? sm.B[t] * d0 * acc[nt][2 * hr] : 0.f;
-              x1 = (j + 1 < t) ? sm.B[t] * d1 * acc[nt][2 * hr + 1] : 0.f;
-            } else {
-              x0 = (j <= t) ? d0 * acc[nt][2 * hr] : 0.f;
-              x1 = (j + 1 <= t) ? d1 * acc[nt][2 * hr + 1] : 0.f;
-            }
-          }
+          const int t = 16 * mt + gid + 8 * hr, j = 16 * np + 8 * half + 2 * tig;
+          const float gt = sm.G[t];
+          const float d0 = __expf(gt - sm.G[j]), d1 = __expf(gt - sm.G[j + 1]);
+          const float v0 = ga[2 * u + half][2 * hr], v1 = ga[2 * u + half][2 * hr + 1];
           if (prod == 0) {
-            if (nt <= 2 * mt + 1) {
-              sm.N[t][j] = x0;
-              sm.N[t][j + 1] = x1;
-            }
+            const float bt = sm.B[t];
+            Nm[t][j] = (j < t) ? bt * d0 * v0 : 0.f;
+            Nm[t][j + 1] = (j + 1 < t) ? bt * d1 * v1 : 0.f;
           } else {
             uint32_t hi, lo;
-            split_pair(x0, x1, hi, lo);
+            split_pair((j <= t) ? d0 * v0 : 0.f, (j + 1 <= t) ? d1 * v1 : 0.f, hi, lo);
             *reinterpret_cast<uint32_t *>(sm.Ah + swz<RB>(t, 2 * j)) = hi;
             *reinterpret_cast<uint32_t *>(sm.Al + swz<RB>(t, 2 * j)) = lo;
           }
@@ -230,22 +279,25 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
     }
     __syncthreads();
 
-    // ---- T = (I + N)^-1 by block doubling (16x16 forward substitution, then MMA levels)
+    // ---- T = (I + N)^-1 by block doubling: 16x16 diagonal blocks by forward
+    // substitution (a thread per column; x[m] = 0 above the column's diagonal), then
+    // (D + C)^-1 = D^-1 - D^-1 C D^-1 on 16 -> 32 -> 64 with tensor-core products
     if (tid < C) {
       const int base = (tid >> 4) * 16, cc = tid & 15;
       float x[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
-        float val = (r == cc) ? 1.f : 0.f;
-        if (r > cc) {
-          float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-          for (int m = 0; m < r; ++m)
-            if (m >= cc) acc += sm.N[base + r][base + m] * x[m];
-          val = -acc;
+        for (int m = 0; m < r; ++m) {
+          if (m & 1)
+            a1 = fmaf(Nm[base + r][base + m], x[m], a1);
+          else
+            a0 = fmaf(Nm[base + r][base + m], x[m], a0);
         }
+        const float val = (r == cc) ? 1.f : (r < cc ? 0.f : -(a0 + a1));
         x[r] = val;
-        sm.T[base + r][base + cc] = val;
+        Tm[base + r][base + cc] = val;
       }
     }
     __syncthreads();
@@ -254,7 +306,7 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
       const bool act = warp < 2 * (C / 32);
       if (act) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f32x3f(acc, &sm.N[bot][top], LD, &sm.T[top][top], LD, 0, 0, n0, lane);
+        mma_f32x3f(acc, &Nm[bot][top], LD, &Tm[top][top], LD, 0, 0, n0, lane);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           sm.M[pr * 256 + (gid + 8 * (e >> 1)) * 16 + n0 + 2 * tig + (e & 1)] = acc[e];
@@ -262,10 +314,10 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
       __syncthreads();
       if (act) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f32x3f(acc, &sm.T[bot][bot], LD, &sm.M[pr * 256], 16, 0, 0, n0, lane);
+        mma_f32x3f(acc, &Tm[bot][bot], LD, &sm.M[pr * 256], 16, 0, 0, n0, lane);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          sm.T[bot + gid + 8 * (e >> 1)][top + n0 + 2 * tig + (e & 1)] = -acc[e];
+          Tm[bot + gid + 8 * (e >> 1)][top + n0 + 2 * tig + (e & 1)] = -acc[e];
       }
       __syncthreads();
     }
@@ -278,7 +330,7 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks)
-            mma_f32x3f(acc[a], &sm.N[32][0], LD, &sm.T[0][0], LD, r0, 16 * ks, nb + 8 * a, lane);
+            mma_f32x3f(acc[a], &Nm[32][0], LD, &Tm[0][0], LD, r0, 16 * ks, nb + 8 * a, lane);
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -292,12 +344,12 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks)
-            mma_f32x3f(acc[a], &sm.T[32][32], LD, sm.M, 33, r0, 16 * ks, nb + 8 * a, lane);
+            mma_f32x3f(acc[a], &Tm[32][32], LD, sm.M, 33, r0, 16 * ks, nb + 8 * a, lane);
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            sm.T[32 + r0 + gid + 8 * (e >> 1)][nb + 8 * a + 2 * tig + (e & 1)] = -acc[a][e];
+            Tm[32 + r0 + gid + 8 * (e >> 1)][nb + 8 * a + 2 * tig + (e & 1)] = -acc[a][e];
       }
       __syncthreads();
     }
@@ -305,7 +357,7 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
     // ---- bf16 operands T diag(beta exp G) and T diag(beta), each as high + low part
     for (int e = tid; e < C * C / 2; e += NT) {
       const int t = e / (C / 2), j = 2 * (e % (C / 2));
-      const float x0 = sm.T[t][j], x1 = sm.T[t][j + 1];
+      const float x0 = Tm[t][j], x1 = Tm[t][j + 1];
       uint32_t hi, lo;
       split_pair(x0 * sm.B[j] * sm.EG[j], x1 * sm.B[j + 1] * sm.EG[j + 1], hi, lo);
       *reinterpret_cast<uint32_t *>(sm.TWh + swz<RB>(t, 2 * j)) = hi;
@@ -326,7 +378,7 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
           uint32_t ah[4], al[4], b[4];
           lda_tile<RB>(ah, sm.TWh, 16 * mt, 16 * ks, lane);
           lda_tile<RB>(al, sm.TWl, 16 * mt, 16 * ks, lane);
-          ldb_kn<kFRowB>(b, sm.K, 16 * ks, i0, lane);
+          ldb_kn<kFRowB>(b, Kb, 16 * ks, i0, lane);
           mma_bf16(acc[0], ah, b[0], b[1]);
           mma_bf16(acc[0], al, b[0], b[1]);
           mma_bf16(acc[1], ah, b[2], b[3]);
@@ -354,7 +406,7 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
 #pragma unroll
     for (int ks = 0; ks < MT; ++ks) {
       uint32_t a[4];
-      lda_tile_t<kFRowB>(a, sm.V, j0, 16 * ks, lane);
+      lda_tile_t<kFRowB>(a, Vb, j0, 16 * ks, lane);
 #pragma unroll
       for (int np = 0; np < MT; ++np) {
         if (np >= ks) {
@@ -386,7 +438,7 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
       for (int np = 0; np < MT; ++np) {
         uint32_t bw[4], bq[4];
         ldb_nk<kFRowB>(bw, sm.W, 16 * np, 16 * ks, lane);
-        ldb_nk<kFRowB>(bq, sm.Q, 16 * np, 16 * ks, lane);
+        ldb_nk<kFRowB>(bq, Qb, 16 * np, 16 * ks, lane);
 #pragma unroll
         for (int a = 0; a < 2; ++a) {
           mma_bf16(Dc[2 * np + a], nh, bw[2 * a], bw[2 * a + 1]);
@@ -426,7 +478,7 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
     for (int nt = 0; nt < NTC; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        Elem<TO>::store(&sm.O[warp][8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)], Rc[nt][e]);
+        Elem<TO>::store(&Ost[warp][8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)], Rc[nt][e]);
     __syncwarp();
     {
       constexpr int EPG = 16 / sizeof(TO);
@@ -435,7 +487,7 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
         const int t = e / GPR, gi = e % GPR;
         if (t < L)
           *reinterpret_cast<uint4 *>(o + ((size_t)(tok0 + t) * p.hv + h) * kD + j0 + gi * EPG) =
-              *reinterpret_cast<const uint4 *>(&sm.O[warp][t][gi * EPG]);
+              *reinterpret_cast<const uint4 *>(&Ost[warp][t][gi * EPG]);
       }
     }
     // S^T <- exp(G_T) S^T + (D^T diag(exp(G_T - G))) K
@@ -453,7 +505,7 @@ __global__ void __launch_bounds__(kFThreads) fused_kernel(ChunkParams p) {
 #pragma unroll
       for (int np = 0; np < 8; ++np) {
         uint32_t b[4];
-        ldb_kn<kFRowB>(b, sm.K, 16 * ks, 16 * np, lane);
+        ldb_kn<kFRowB>(b, Kb, 16 * ks, 16 * np, lane);
         mma_bf16(S[2 * np], th, b[0], b[1]);
         mma_bf16(S[2 * np], tl, b[0], b[1]);
         mma_bf16(S[2 * np + 1], th, b[2], b[3]);
