@@ -1,5 +1,5 @@
-// Chunkwise-parallel gated delta rule, bf16 q/k/v on tensor cores ("Qwen3.5-9B-npu"
-// model card, section "How it works", chunkwise form):
+// Chunkwise-parallel gated delta rule, bf16 q/k/v, two passes ("Qwen3.5-9B-npu" model
+// card, section "How it works", chunkwise form):
 //   N   = diag(beta) [exp(G_t - G_j) k_t.k_j]_{j<t}
 //   D   = (I + N)^-1 diag(beta) (V - diag(exp G) K S0)
 //   O   = diag(exp G) Q S0 + [exp(G_t - G_j) q_t.k_j]_{j<=t} D
@@ -8,30 +8,27 @@
 // The state-independent part of D is split off:  with T = (I + N)^-1,
 //   D = U - W S0,   U = T diag(beta) V,   W = T diag(beta exp G) K,
 // so the work falls in two passes:
-//   pass 1 (prep_kernel, every block of every head in parallel): G, the decay-masked
-//     Grams, T by exact block doubling in fp32 (16x16 diagonal blocks by forward
+//   pass 1 (prep_kernel, one CTA per (block, v-head), all in parallel): G, the
+//     decay-masked Grams, T by exact block doubling (16x16 diagonal blocks by forward
 //     substitution, then (D + C)^-1 = D^-1 - D^-1 C D^-1 on 16 -> 32 -> 64), and the
-//     products W, U on tensor cores.
-//     The doubling levels run on tensor cores with 3-term bf16 splits of the fp32
-//     operands.  Each block's results go to its own workspace slot, already in the
-//     swizzled shared-memory layout pass 2 uses.
+//     products W and U.  Each block's W, fp16 q and k rows, A, decays and U^T go to its
+//     own workspace slot in the padded shared-memory layout pass 2 reads.
 //   pass 2 (recur_kernel, one CTA per (sequence, v-head, 16 value columns)): walks the
 //     blocks of the sequence in order with the state block S[:, cols] in fp32 registers
 //     (read from state_in once, written to state_out once).  A producer warp streams
-//     each block's slot into a 2-stage shared-memory ring with bulk (TMA) copies
-//     signalled on mbarriers.  Four "state" warps run the dependent chain
-//       P = W S and D = U - P (each for 16 tokens),
-//       S <- exp(G_T) S + K^T diag(exp(G_T - G)) D (each for 32 keys),
-//     and four "output" warps form O = exp(G) Q S + A D for the same block from a
-//     snapshot of S.  All products run on mma.sync tensor cores, fp32 accumulation.
-// Precision: q, k, v are bf16 inputs and enter the products exactly.  T, the state, D
-// and A are fp32 values carried as two bf16 numbers, hi = bf16(x), lo = bf16(x - hi),
-// with products hi*y + lo*y (~16 significant bits); W is rounded to bf16 once.  The
-// layer's outputs have heavy tails (max/rms above 10), so single-bf16 copies of those
-// operands would put errors of a few 1e-2 of the rms on the largest entries.
-// Decay factors between two tokens are always the exp of a difference of cumsums.  A
-// partly filled block is padded with g = 0, beta = 0, zero q/k/v rows (token_valid),
-// which leaves the state exactly as after the sequence's last token.
+//     each block's slot part into a 2-stage shared-memory ring with two bulk (TMA)
+//     copies signalled on mbarriers.  Four compute warps each own 16 tokens
+//     of the block for
+//       D^T = U^T - S^T W^T   and   R^T = S^T Q^T   (sharing the S^T fragments),
+//     exchange D once through shared memory, then each carries 32 keys of the state,
+//       S^T <- exp(G_T) S^T + (D^T diag(exp(G_T - G))) K,
+//     and finishes its tokens' outputs O^T = diag(e^G) R^T + D^T A^T.
+// Tensor-core products (mma.sync) take fp16 operands with fp32 accumulation: bf16 q, k
+// and v enter exactly (converted to fp16), the state, D, T, W and A are rounded to fp16
+// (11 significant bits) for the products only; the state itself, the sums and every
+// decay are fp32.  Decay factors between two tokens are always the exp of a difference
+// of cumsums.  A partly filled block is padded with g = 0, beta = 0 and zero q/k/v rows
+// (token_valid), which leaves the state exactly as after the sequence's last token.
 #include "common.cuh"
 #include "internal.h"
 
@@ -39,14 +36,13 @@ namespace gdn {
 
 namespace {
 
-constexpr int kRowB = kD * 2;  // bytes in a 128-element bf16 row
-
 __device__ __forceinline__ size_t slot_index(int bos, int chunk, int n, int c) {
   return (size_t)(bos / chunk + n + c);
 }
 
 // acc (16x8 tile) += A[r0.., k0..k0+16) * B[k0.., n0..n0+8) for fp32 row-major matrices in
 // shared memory, as hi*hi + lo*hi + hi*lo of their bf16 splits (~16 significant bits).
+// Used by the small block-doubling products, where T's own accuracy is set.
 __device__ __forceinline__ void mma_f32x3(float (&acc)[4], const float *A, int lda,
                                           const float *B, int ldb, int r0, int k0, int n0,
                                           int lane) {
@@ -70,27 +66,27 @@ __device__ __forceinline__ void mma_f32x3(float (&acc)[4], const float *A, int l
 
 template <int C>
 struct PrepSmem {
-  alignas(128) char K[C * kRowB];
-  alignas(128) char V[C * kRowB];
-  // Q tile followed by N (fp32); overlaid after the solve by the four bf16 copies of T
-  alignas(128) char X[C * kRowB + C * (C + 4) * 4];
+  static constexpr int RC = row_c(C);
+  alignas(16) char K[C * kP128];  // bf16 rows; converted in place to fp16 after the Grams
+  alignas(16) char V[C * kP128];  // bf16 rows; converted in place to fp16
+  alignas(16) char Q[C * kP128];  // bf16 rows; converted in place to fp16
+  float N[C][C + 4];
   float T[C][C + 4];
+  alignas(16) char TW[C * RC];    // A staging (fp16), then fp16 T diag(beta e^G)
+  alignas(16) char TU[C * RC];    // fp16 T diag(beta)
   float M[32 * 33];
-  float G[C], EG[C], B[C];
+  float G[C], EG[C], ED[C], B[C];
   float gRaw[C], bRaw[C];
 };
 
 constexpr int kPrepThreads = 256;
 
 template <int C>
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChunkParams p, int per_head) {
-  constexpr int NW = kPrepThreads / 32, NT = kPrepThreads, MT = C / 16, RB = 2 * C, LD = C + 4;
-  static_assert(8 * C * C <= C * kRowB + C * (C + 4) * 4, "overlay too small");
+__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, int per_head) {
+  constexpr int NT = kPrepThreads, MT = C / 16, RC = row_c(C), LD = C + 4;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   PrepSmem<C> &sm = *reinterpret_cast<PrepSmem<C> *>(smem_raw);
-  char *sQ = sm.X;
-  float(*sN)[LD] = reinterpret_cast<float(*)[LD]>(sm.X + C * kRowB);
-  char *TWH = sm.X, *TWL = sm.X + C * RB, *TUH = sm.X + 2 * C * RB, *TUL = sm.X + 3 * C * RB;
+  float(*sN)[LD] = sm.N;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -108,14 +104,15 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChunkParams p, int p
   seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
   const int nchunks = (eos - bos + C - 1) / C;
 
+#pragma unroll 1
   for (int c = part; c < nchunks; c += per_head) {
     const int tok0 = bos + c * C;
     const int L = min(C, eos - tok0);
     char *slot = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, c)) * slot_bytes(C);
-    char *w_out = slot, *q_out = slot + 256 * C, *k_out = slot + 512 * C;
-    char *ah_out = slot + 768 * C, *al_out = slot + 768 * C + 2 * C * C;
-    float *u_out = reinterpret_cast<float *>(slot + slot_head_bytes(C));
-    float *g_out = reinterpret_cast<float *>(slot + slot_head_bytes(C) + slot_u_bytes(C));
+    char *w_out = slot, *a_out = slot + slot_a_off(C);
+    char *q_out = slot + slot_q_off(C), *k_out = slot + slot_k_off(C);
+    float *dec_out = reinterpret_cast<float *>(slot + slot_dec_off(C));
+    char *u_out = slot + slot_u_off(C);
     __syncthreads();  // the previous block is done with shared memory
 
     for (int e = tid; e < C * 16; e += NT) {
@@ -123,9 +120,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChunkParams p, int p
       const bool ok = r < L;
       const size_t tok = (size_t)tok0 + (ok ? r : 0);
       const int nb = ok ? 16 : 0;
-      cp_async16(sm.K + swz<kRowB>(r, gr * 16), k + (tok * p.hk + kh) * kD + gr * 8, nb);
-      cp_async16(sQ + swz<kRowB>(r, gr * 16), q + (tok * p.hk + kh) * kD + gr * 8, nb);
-      cp_async16(sm.V + swz<kRowB>(r, gr * 16), v + (tok * p.hv + h) * kD + gr * 8, nb);
+      cp_async16(sm.K + r * kP128 + gr * 16, k + (tok * p.hk + kh) * kD + gr * 8, nb);
+      cp_async16(sm.Q + r * kP128 + gr * 16, q + (tok * p.hk + kh) * kD + gr * 8, nb);
+      cp_async16(sm.V + r * kP128 + gr * 16, v + (tok * p.hv + h) * kD + gr * 8, nb);
     }
     for (int t = tid; t < C; t += NT) {
       const bool ok = t < L;
@@ -134,11 +131,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChunkParams p, int p
       cp_async4(&sm.bRaw[t], p.beta + gi, ok ? 4 : 0);
     }
     cp_async_commit();
+    // T starts at zero: the doubling products read whole 32x32 blocks of T, whose upper
+    // parts are never written
     for (int e = tid; e < C * LD; e += NT) (&sm.T[0][0])[e] = 0.f;
     cp_async_wait<0>();
     __syncthreads();
 
-    // in-block inclusive cumsum of g (padding contributes 0), exp(G), beta
+    // in-block inclusive cumsum of g (padding contributes 0), e^G, e^(G_C - G), beta
     if (warp == 0) {
       constexpr int E = (C + 31) / 32;
       float gv[E], bv[E], run = 0.f;
@@ -157,122 +156,169 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChunkParams p, int p
         if (lane >= off) incl += y;
       }
       const float excl = incl - run;
+      const float gC = __shfl_sync(0xffffffffu, incl, 31);
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int t = lane * E + e;
         if (t < C) {
-          sm.G[t] = gv[e] + excl;
-          sm.EG[t] = __expf(gv[e] + excl);
+          const float G = gv[e] + excl;
+          sm.G[t] = G;
+          sm.EG[t] = __expf(G);
+          sm.ED[t] = __expf(gC - G);
           sm.B[t] = bv[e];
-          g_out[t] = gv[e] + excl;
         }
       }
     }
 
-    // the block's q and k rows (swizzled, zero past the sequence end) go to the slot as is
-    for (int e = tid; e < C * 16; e += NT) {
-      reinterpret_cast<uint4 *>(q_out)[e] = reinterpret_cast<const uint4 *>(sQ)[e];
-      reinterpret_cast<uint4 *>(k_out)[e] = reinterpret_cast<const uint4 *>(sm.K)[e];
+    // ---- raw Grams on tensor cores (bf16 inputs, exact products): warps 0-3 K K^T,
+    //      warps 4-7 Q K^T, each a balanced share of the causal 16x16 tiles (mt, np<=mt):
+    //      tiles np0 .. np0+n0-1 of row mt0, plus tile (mt1, 0) for one warp at C = 64
+    const int prod = warp >> 2, qw = warp & 3;
+    int mt0 = 0, np0 = 0, n0 = 0, mt1 = -1;
+    if (C == 64) {  // row 3: {0,1}, {2,3}; row 2: {0,1,2}; row 1: {0,1} and row 0: {0}
+      mt0 = qw < 2 ? 3 : (qw == 2 ? 2 : 1);
+      np0 = qw == 1 ? 2 : 0;
+      n0 = qw == 2 ? 3 : 2;
+      if (qw == 3) mt1 = 0;
+    } else if (C == 32) {  // row 1: {0}, {1}; row 0: {0}
+      mt0 = qw < 2 ? 1 : 0;
+      np0 = qw == 1 ? 1 : 0;
+      n0 = qw < 3 ? 1 : 0;
+    } else {
+      n0 = qw == 0 ? 1 : 0;
     }
-    __syncthreads();  // G, EG, B written by warp 0
-
-    // ---- decay-masked Grams on tensor cores: warp w takes items 2w, 2w+1 of
-    //      [KK(0), KK(MT-1), KK(1), ..., QK(0), QK(MT-1), ...] (balanced triangles)
-#pragma unroll 1
-    for (int item = warp; item < 2 * MT; item += NW) {
-      const int prod = item / MT;  // 0: K K^T, 1: Q K^T
-      const int r = item % MT;
-      const int mt = (r & 1) ? (MT - 1 - r / 2) : (r / 2);
-      const char *Asrc = prod ? sQ : sm.K;
-      float acc[C / 8][4];
+    float ga[6][4];
 #pragma unroll
-      for (int a = 0; a < C / 8; ++a)
+    for (int u = 0; u < 6; ++u)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
+      for (int e = 0; e < 4; ++e) ga[u][e] = 0.f;
+    {
+      const char *Asrc = prod ? sm.Q : sm.K;
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
-        uint32_t a[4];
-        lda_tile<kRowB>(a, Asrc, 16 * mt, 16 * ks, lane);
+        if (n0 > 0) {
+          uint32_t a[4];
+          lda_p<kP128>(a, Asrc, 16 * mt0, 16 * ks, lane);
 #pragma unroll
-        for (int np = 0; np < C / 16; ++np) {
-          if (np <= mt) {
-            uint32_t b[4];
-            ldb_nk<kRowB>(b, sm.K, 16 * np, 16 * ks, lane);
-            mma_bf16(acc[2 * np], a, b[0], b[1]);
-            mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+          for (int u = 0; u < 3; ++u) {
+            if (u < n0) {
+              uint32_t b[4];
+              ldb_nk_p<kP128>(b, sm.K, 16 * (np0 + u), 16 * ks, lane);
+              mma_bf16(ga[2 * u], a, b[0], b[1]);
+              mma_bf16(ga[2 * u + 1], a, b[2], b[3]);
+            }
           }
         }
+        if (mt1 >= 0) {
+          uint32_t a[4], b[4];
+          lda_p<kP128>(a, Asrc, 16 * mt1, 16 * ks, lane);
+          ldb_nk_p<kP128>(b, sm.K, 0, 16 * ks, lane);
+          mma_bf16(ga[4], a, b[0], b[1]);
+          mma_bf16(ga[5], a, b[2], b[3]);
+        }
+      }
+    }
+    __syncthreads();  // gates ready
+
+    // ---- decay masks: N (fp32, strictly lower, beta_t e^(G_t - G_j)) and A (fp16,
+    //      causal with its diagonal, e^(G_t - G_j)) into the A staging tile
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      int mt, np;
+      if (u < n0) {
+        mt = mt0;
+        np = np0 + u;
+      } else if (u == 2 && mt1 >= 0) {
+        mt = mt1;
+        np = 0;
+      } else {
+        continue;
       }
 #pragma unroll
-      for (int nt = 0; nt < C / 8; ++nt) {
+      for (int half = 0; half < 2; ++half)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
-          const int t = 16 * mt + gid + 8 * hr;
-          const int j = 8 * nt + 2 * tig;
-          float x0 = 0.f, x1 = 0.f;
-          if (nt <= 2 * mt + 1) {
-            const float d0 = __expf(sm.G[t] - sm.G[j]), d1 = __expf(sm.G[t] - sm.G[j + 1]);
-            if (prod == 0) {
-              x0 = (j < t) ? sm.B[t] * d0 * acc[nt][2 * hr] : 0.f;
-              x1 = (j + 1 < t) ? sm.B[t] * d1 * acc[nt][2 * hr + 1] : 0.f;
-            } else {
-              x0 = (j <= t) ? d0 * acc[nt][2 * hr] : 0.f;
-              x1 = (j + 1 <= t) ? d1 * acc[nt][2 * hr + 1] : 0.f;
-            }
-          }
+          const int t = 16 * mt + gid + 8 * hr, j = 16 * np + 8 * half + 2 * tig;
+          const float gt = sm.G[t];
+          const float d0 = __expf(gt - sm.G[j]), d1 = __expf(gt - sm.G[j + 1]);
+          const float v0 = ga[2 * u + half][2 * hr], v1 = ga[2 * u + half][2 * hr + 1];
           if (prod == 0) {
-            if (nt <= 2 * mt + 1) {
-              sN[t][j] = x0;
-              sN[t][j + 1] = x1;
-            }
+            const float bt = sm.B[t];
+            sN[t][j] = (j < t) ? bt * d0 * v0 : 0.f;
+            sN[t][j + 1] = (j + 1 < t) ? bt * d1 * v1 : 0.f;
           } else {
-            uint32_t hi, lo;
-            split_bf16(x0, x1, hi, lo);
-            *reinterpret_cast<uint32_t *>(ah_out + swz<RB>(t, 2 * j)) = hi;
-            *reinterpret_cast<uint32_t *>(al_out + swz<RB>(t, 2 * j)) = lo;
+            *reinterpret_cast<uint32_t *>(sm.TW + t * RC + 2 * j) =
+                pack_f16((j <= t) ? d0 * v0 : 0.f, (j + 1 <= t) ? d1 * v1 : 0.f);
           }
         }
-      }
+    }
+    // the A tile's upper 16x16 blocks (never computed) are zero
+    for (int e = tid; e < C * C / 2; e += NT) {
+      const int t = e / (C / 2), j = 2 * (e % (C / 2));
+      if ((j >> 4) > (t >> 4)) *reinterpret_cast<uint32_t *>(sm.TW + t * RC + 2 * j) = 0u;
     }
     __syncthreads();
 
-    // ---- T = (I + N)^-1 by block doubling.  Level 0: 16x16 diagonal blocks in fp32,
-    //      one column per thread, forward substitution.
+    // ---- T = (I + N)^-1.  Level 0: 16x16 diagonal blocks in fp32, one column per
+    //      thread, forward substitution; meanwhile the other warps convert q, k and v to
+    //      fp16 and ship q, k, A and the decays to the slot.
     if (tid < C) {
       const int base = (tid >> 4) * 16, cc = tid & 15;
       float x[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
-        float val = (r == cc) ? 1.f : 0.f;
-        if (r > cc) {
-          float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-          for (int m = 0; m < r; ++m)
-            if (m >= cc) acc += sN[base + r][base + m] * x[m];
-          val = -acc;
+        for (int m = 0; m < r; ++m) {  // x[m] = 0 above the column's diagonal
+          if (m & 1)
+            a1 = fmaf(sN[base + r][base + m], x[m], a1);
+          else
+            a0 = fmaf(sN[base + r][base + m], x[m], a0);
         }
+        const float val = (r == cc) ? 1.f : (r < cc ? 0.f : -(a0 + a1));
         x[r] = val;
         sm.T[base + r][base + cc] = val;
+      }
+    } else {
+      const int t2 = tid - C, n2 = NT - C;
+      for (int e = t2; e < C * 64; e += n2) {  // 64 packed pairs per 128-element row
+        const int r = e >> 6, cp = e & 63;
+        uint32_t *pk = reinterpret_cast<uint32_t *>(sm.K + r * kP128) + cp;
+        uint32_t *pq = reinterpret_cast<uint32_t *>(sm.Q + r * kP128) + cp;
+        uint32_t *pv = reinterpret_cast<uint32_t *>(sm.V + r * kP128) + cp;
+        const uint32_t k16 = bf16x2_to_f16x2(*pk), q16 = bf16x2_to_f16x2(*pq);
+        *pk = k16;
+        *pv = bf16x2_to_f16x2(*pv);
+        reinterpret_cast<uint32_t *>(k_out + r * kP128)[cp] = k16;
+        reinterpret_cast<uint32_t *>(q_out + r * kP128)[cp] = q16;
+      }
+      constexpr int G16 = RC / 16;  // 16-byte granules per A row (incl. padding)
+      for (int e = t2; e < C * G16; e += n2)
+        reinterpret_cast<uint4 *>(a_out)[e] = reinterpret_cast<const uint4 *>(sm.TW)[e];
+      for (int t = t2; t < C; t += n2) {
+        dec_out[t] = sm.G[t];
+        dec_out[C + t] = sm.EG[t];
+        dec_out[2 * C + t] = sm.ED[t];
       }
     }
     __syncthreads();
     // Level 1 (16 -> 32): lower-left block = -T_bot (N_bl T_top); one 16x8 tile per warp.
     if (C >= 32) {
-      const int pr = warp >> 1, top = 32 * pr, bot = top + 16, n0 = 8 * (warp & 1);
+      const int pr = warp >> 1, top = 32 * pr, bot = top + 16, nb = 8 * (warp & 1);
       if (warp < 2 * (C / 32)) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f32x3(acc, &sN[bot][top], LD, &sm.T[top][top], LD, 0, 0, n0, lane);
+        mma_f32x3(acc, &sN[bot][top], LD, &sm.T[top][top], LD, 0, 0, nb, lane);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          sm.M[pr * 256 + (gid + 8 * (e >> 1)) * 16 + n0 + 2 * tig + (e & 1)] = acc[e];
+          sm.M[pr * 256 + (gid + 8 * (e >> 1)) * 16 + nb + 2 * tig + (e & 1)] = acc[e];
       }
       __syncthreads();
       if (warp < 2 * (C / 32)) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f32x3(acc, &sm.T[bot][bot], LD, &sm.M[pr * 256], 16, 0, 0, n0, lane);
+        mma_f32x3(acc, &sm.T[bot][bot], LD, &sm.M[pr * 256], 16, 0, 0, nb, lane);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          sm.T[bot + gid + 8 * (e >> 1)][top + n0 + 2 * tig + (e & 1)] = -acc[e];
+          sm.T[bot + gid + 8 * (e >> 1)][top + nb + 2 * tig + (e & 1)] = -acc[e];
       }
       __syncthreads();
     }
@@ -310,62 +356,53 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChunkParams p, int p
       __syncthreads();
     }
 
-    // ---- bf16 operands T diag(beta exp G) and T diag(beta), each as high + low part
+    // ---- fp16 operands T diag(beta e^G) and T diag(beta) (T is lower triangular; the
+    //      never-written upper part is masked here)
     for (int e = tid; e < C * C / 2; e += NT) {
       const int t = e / (C / 2), j = 2 * (e % (C / 2));
-      const float x0 = sm.T[t][j], x1 = sm.T[t][j + 1];
-      uint32_t hi, lo;
-      split_bf16(x0 * sm.B[j] * sm.EG[j], x1 * sm.B[j + 1] * sm.EG[j + 1], hi, lo);
-      *reinterpret_cast<uint32_t *>(TWH + swz<RB>(t, 2 * j)) = hi;
-      *reinterpret_cast<uint32_t *>(TWL + swz<RB>(t, 2 * j)) = lo;
-      split_bf16(x0 * sm.B[j], x1 * sm.B[j + 1], hi, lo);
-      *reinterpret_cast<uint32_t *>(TUH + swz<RB>(t, 2 * j)) = hi;
-      *reinterpret_cast<uint32_t *>(TUL + swz<RB>(t, 2 * j)) = lo;
+      const float x0 = (j <= t) ? sm.T[t][j] : 0.f, x1 = (j + 1 <= t) ? sm.T[t][j + 1] : 0.f;
+      *reinterpret_cast<uint32_t *>(sm.TW + t * RC + 2 * j) =
+          pack_f16(x0 * sm.B[j] * sm.EG[j], x1 * sm.B[j + 1] * sm.EG[j + 1]);
+      *reinterpret_cast<uint32_t *>(sm.TU + t * RC + 2 * j) =
+          pack_f16(x0 * sm.B[j], x1 * sm.B[j + 1]);
     }
     __syncthreads();
 
-    // ---- W = T diag(beta e^G) K  [t][i]: this warp's 128/NW key columns, all rows.
-    //      Causal: T[t][j] = 0 for j > t.
-    {
-      constexpr int NTI = 16 / NW;  // 8-wide n-tiles of keys per warp
-      const int i0 = warp * (kD / NW);
+    if (warp < 4) {
+      // ---- W = T diag(beta e^G) K  [t][key]: keys 32 warp .. +32, causal k-steps
+      const int i0 = 32 * warp;
 #pragma unroll 1
       for (int mt = 0; mt < MT; ++mt) {
-        float acc[NTI][4];
+        float acc[4][4];
 #pragma unroll
-        for (int a = 0; a < NTI; ++a)
+        for (int a = 0; a < 4; ++a)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
         for (int ks = 0; ks <= mt; ++ks) {
-          uint32_t ah[4], al[4];
-          lda_tile<RB>(ah, TWH, 16 * mt, 16 * ks, lane);
-          lda_tile<RB>(al, TWL, 16 * mt, 16 * ks, lane);
+          uint32_t a[4];
+          lda_p<RC>(a, sm.TW, 16 * mt, 16 * ks, lane);
 #pragma unroll
-          for (int np = 0; np < NTI / 2; ++np) {
+          for (int np = 0; np < 2; ++np) {
             uint32_t b[4];
-            ldb_kn<kRowB>(b, sm.K, 16 * ks, i0 + 16 * np, lane);
-            mma_bf16(acc[2 * np], ah, b[0], b[1]);
-            mma_bf16(acc[2 * np], al, b[0], b[1]);
-            mma_bf16(acc[2 * np + 1], ah, b[2], b[3]);
-            mma_bf16(acc[2 * np + 1], al, b[2], b[3]);
+            ldb_kn_p<kP128>(b, sm.K, 16 * ks, i0 + 16 * np, lane);
+            mma_f16(acc[2 * np], a, b[0], b[1]);
+            mma_f16(acc[2 * np + 1], a, b[2], b[3]);
           }
         }
 #pragma unroll
-        for (int nt = 0; nt < NTI; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
             const int t = 16 * mt + gid + 8 * hr, col = i0 + 8 * nt + 2 * tig;
-            *reinterpret_cast<uint32_t *>(w_out + swz<kRowB>(t, 2 * col)) =
-                pack_bf16(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+            *reinterpret_cast<uint32_t *>(w_out + t * kP128 + 2 * col) =
+                pack_f16(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
           }
       }
-    }
-    // ---- U^T = V^T (T diag(beta))^T  [j][t]: this warp's 128/NW value rows.
-    {
-      constexpr int MJ = 8 / NW;  // 16-row m-tiles of value columns per warp
+    } else {
+      // ---- U^T = V^T (T diag(beta))^T  [value col][t]: value cols 32 (warp-4) .. +32
+      const int j0 = 32 * (warp - 4);
 #pragma unroll 1
-      for (int mj = 0; mj < MJ; ++mj) {
-        const int j0 = warp * (kD / NW) + 16 * mj;
+      for (int mj = 0; mj < 2; ++mj) {
         float acc[C / 8][4];
 #pragma unroll
         for (int a = 0; a < C / 8; ++a)
@@ -374,17 +411,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChunkParams p, int p
 #pragma unroll
         for (int ks = 0; ks < MT; ++ks) {
           uint32_t a[4];
-          lda_tile_t<kRowB>(a, sm.V, j0, 16 * ks, lane);
+          lda_t_p<kP128>(a, sm.V, j0 + 16 * mj, 16 * ks, lane);
 #pragma unroll
           for (int np = 0; np < MT; ++np) {
             if (np >= ks) {
-              uint32_t bh[4], bl[4];
-              ldb_nk<RB>(bh, TUH, 16 * np, 16 * ks, lane);
-              ldb_nk<RB>(bl, TUL, 16 * np, 16 * ks, lane);
-              mma_bf16(acc[2 * np], a, bh[0], bh[1]);
-              mma_bf16(acc[2 * np], a, bl[0], bl[1]);
-              mma_bf16(acc[2 * np + 1], a, bh[2], bh[3]);
-              mma_bf16(acc[2 * np + 1], a, bl[2], bl[3]);
+              uint32_t b[4];
+              ldb_nk_p<RC>(b, sm.TU, 16 * np, 16 * ks, lane);
+              mma_f16(acc[2 * np], a, b[0], b[1]);
+              mma_f16(acc[2 * np + 1], a, b[2], b[3]);
             }
           }
         }
@@ -392,9 +426,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChunkParams p, int p
         for (int nt = 0; nt < C / 8; ++nt)
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
-            const int j = j0 + gid + 8 * hr, t = 8 * nt + 2 * tig;
-            *reinterpret_cast<float2 *>(u_out + j * (C + 4) + t) =
-                make_float2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+            const int j = j0 + 16 * mj + gid + 8 * hr, t = 8 * nt + 2 * tig;
+            *reinterpret_cast<uint32_t *>(u_out + j * RC + 2 * t) =
+                pack_f16(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
           }
       }
     }
@@ -403,39 +437,32 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(ChunkParams p, int p
 
 // ================================================================== pass 2
 
-constexpr int kStateWarps = 4, kOutWarps = 4;
-constexpr int kRecThreads = 32 * (kStateWarps + kOutWarps + 1);  // + 1 producer warp
-constexpr int kConsumers = 32 * (kStateWarps + kOutWarps);
+constexpr int kCompWarps = 4;
+constexpr int kRecThreads = 32 * (kCompWarps + 1);  // + 1 producer warp
+constexpr int kComp = 32 * kCompWarps;
 constexpr int kDVB = 16;  // value columns per CTA
 
 template <int C, typename TO>
 struct RecSmem {
-  struct Stage {  // mirrors a workspace slot: W | Q | K | Ah | Al contiguous, then U, G
-    alignas(128) char W[C * kRowB];
-    char Q[C * kRowB];
-    char K[C * kRowB];
-    char Ah[C * 2 * C];
-    char Al[C * 2 * C];
-    alignas(16) float U[kDVB][C + 4];  // U^T rows of this CTA's value columns
-    alignas(16) float G[C];
+  static constexpr int RC = row_c(C);
+  struct Stage {
+    alignas(128) char H[slot_head_bytes(C)];  // W | Q | K | A | DEC, as in the slot
+    alignas(16) char U[kDVB * RC];            // U^T rows of this CTA's value columns
   } st[2];
   alignas(8) uint64_t full[2], empty[2];
-  alignas(128) char Sh[kDVB * kRowB];  // S^T snapshot (hi, lo)
-  alignas(128) char Sl[kDVB * kRowB];
-  alignas(128) char Dh[kDVB * 2 * C];  // D^T (hi, lo)
-  alignas(128) char Dl[kDVB * 2 * C];
-  alignas(128) char Th[kDVB * 2 * C];  // (diag(exp(G_T - G)) D)^T (hi, lo)
-  alignas(128) char Tl[kDVB * 2 * C];
-  alignas(16) TO O[kOutWarps][16][kDVB];
+  alignas(16) char Sn[kDVB * kP128];  // S^T (fp16) [16 value cols][128 keys]
+  alignas(16) char Db[kDVB * RC];     // D^T (fp16) [16 value cols][C tokens]
+  alignas(16) char Dd[kDVB * RC];     // (D diag(e^(G_C - G)))^T (fp16)
+  alignas(16) TO O[kCompWarps][16][kDVB];
   alignas(16) float S32[kD][kDVB + 4];  // fp32 staging of the state block
 };
 
 template <int C, typename TO>
 __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
-  constexpr int NB = kD / kDVB, TT = C / 16, RB = 2 * C;
+  constexpr int NB = kD / kDVB, MT = C / 16, RC = row_c(C);
   constexpr uint32_t kHeadB = (uint32_t)slot_head_bytes(C);
-  constexpr uint32_t kUB = (uint32_t)(kDVB * (C + 4) * 4);
-  constexpr uint32_t kStageTx = kHeadB + kUB + 4 * C;
+  constexpr uint32_t kUB = (uint32_t)(kDVB * RC);
+  constexpr uint32_t kStageTx = kHeadB + kUB;
   using Smem = RecSmem<C, TO>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
@@ -460,133 +487,164 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
     }
     mbar_fence_init();
   }
-  // state block S[:, blk*16 .. +16) -> fp32 staging (coalesced 64-byte rows)
-  for (int e = tid; e < kD * kDVB / 4; e += kRecThreads) {
-    const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
-    const float4 val =
-        p.state_in ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + 4 * c4)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4 *>(&sm.S32[i][4 * c4]) = val;
-  }
   __syncthreads();
 
-  if (warp == kStateWarps + kOutWarps) {
-    // ---- producer: stream block slots into the 2-stage ring
+  if (warp == kCompWarps) {
+    // ---- producer: stream each block's slot part into the 2-stage ring
     if (lane == 0) {
       bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
         if (c >= 2) ok = mbar_wait(&sm.empty[s], ((c - 2) >> 1) & 1) && ok;
+        typename Smem::Stage &st = sm.st[s];
         const char *src = slot0 + (size_t)c * slot_bytes(C);
         mbar_arrive_expect_tx(&sm.full[s], kStageTx);
-        bulk_g2s(sm.st[s].W, src, kHeadB, &sm.full[s]);
-        bulk_g2s(&sm.st[s].U[0][0], src + kHeadB + (size_t)blk * kUB, kUB, &sm.full[s]);
-        bulk_g2s(sm.st[s].G, src + kHeadB + slot_u_bytes(C), 4 * C, &sm.full[s]);
+        bulk_g2s(st.H, src, kHeadB, &sm.full[s]);
+        bulk_g2s(st.U, src + slot_u_off(C) + (size_t)blk * kDVB * RC, kUB, &sm.full[s]);
       }
       // the last copies are consumed before the CTA's final barrier
       if (!ok) atomicExch(p.err, 1);
     }
-  } else if (warp < kStateWarps) {
-    // ---- state warps: wq owns tokens 16wq.. (P, D) and keys 32wq.. (state carry)
-    const int wq = warp;
-    float Sa[4][4];  // S^T[j][i], j = gid (+8), i = 32wq + 8nt + 2tig (+1)
+  } else {
+    const int w = warp;
+    // state block S[:, blk*16 .. +16) -> fp32 staging (coalesced 64-byte rows)
+    for (int e = tid; e < kD * kDVB / 4; e += kComp) {
+      const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
+      const float4 val =
+          p.state_in ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + 4 * c4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4 *>(&sm.S32[i][4 * c4]) = val;
+    }
+    bar_sync(1, kComp);
+    // S^T[j][i] for j = gid (+8), i = 32w + 8nt + 2tig (+1)
+    float Sa[4][4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        Sa[nt][e] = sm.S32[32 * wq + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)];
+        Sa[nt][e] = sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)];
     auto write_snapshot = [&]() {
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
-          const int j = gid + 8 * hr, i = 32 * wq + 8 * nt + 2 * tig;
-          uint32_t hi, lo;
-          split_bf16(Sa[nt][2 * hr], Sa[nt][2 * hr + 1], hi, lo);
-          *reinterpret_cast<uint32_t *>(sm.Sh + swz<kRowB>(j, 2 * i)) = hi;
-          *reinterpret_cast<uint32_t *>(sm.Sl + swz<kRowB>(j, 2 * i)) = lo;
+          const int j = gid + 8 * hr, i = 32 * w + 8 * nt + 2 * tig;
+          *reinterpret_cast<uint32_t *>(sm.Sn + j * kP128 + 2 * i) =
+              pack_f16(Sa[nt][2 * hr], Sa[nt][2 * hr + 1]);
         }
     };
     write_snapshot();
-    bar_sync(2, kConsumers);
+    bar_sync(1, kComp);
+
     bool ok = true;
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
       const int s = c & 1;
       typename Smem::Stage &st = sm.st[s];
+      const char *W = st.H, *Qs = st.H + slot_q_off(C), *Ks = st.H + slot_k_off(C);
+      const char *A = st.H + slot_a_off(C);
+      const float *DG = reinterpret_cast<const float *>(st.H + slot_dec_off(C));
+      const float *EG = DG + C, *ED = DG + 2 * C;
+      const int tok0 = bos + c * C;
+      const int L = min(C, eos - tok0);
       ok = mbar_wait(&sm.full[s], (c >> 1) & 1) && ok;
-      const float gC = st.G[C - 1];
-      if (wq < TT) {
-        // P^T = S^T W^T for this warp's 16 tokens (k split in halves for shorter chains)
-        float Ph[2][2][4], Pl[2][2][4];
-#pragma unroll
-        for (int x = 0; x < 2; ++x)
-#pragma unroll
-          for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) Ph[x][a][e] = Pl[x][a][e] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          uint32_t sh[4], sl[4], bw[4];
-          lda_tile<kRowB>(sh, sm.Sh, 0, 16 * ks, lane);
-          lda_tile<kRowB>(sl, sm.Sl, 0, 16 * ks, lane);
-          ldb_nk<kRowB>(bw, st.W, 16 * wq, 16 * ks, lane);
-          const int x = ks & 1;
-#pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            mma_bf16(Ph[x][a], sh, bw[2 * a], bw[2 * a + 1]);
-            mma_bf16(Pl[x][a], sl, bw[2 * a], bw[2 * a + 1]);
-          }
-        }
-        // D = U - P, and its carry-scaled copy, as bf16 (hi, lo) for the other warps
+
+      // ---- D^T = U^T - S^T W^T and R^T = S^T Q^T for tokens 16w .. 16w+15
+      float Dc[2][4], Rc[2][4];
+      if (w < MT) {
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
-            const int j = gid + 8 * hr, t = 16 * wq + 8 * a + 2 * tig;
-            const float2 u = *reinterpret_cast<const float2 *>(&st.U[j][t]);
-            const int e0 = 2 * hr, e1 = 2 * hr + 1;
-            const float d0 = u.x - ((Ph[0][a][e0] + Pl[0][a][e0]) + (Ph[1][a][e0] + Pl[1][a][e0]));
-            const float d1 = u.y - ((Ph[0][a][e1] + Pl[0][a][e1]) + (Ph[1][a][e1] + Pl[1][a][e1]));
-            const int so = swz<RB>(j, 2 * t);
-            uint32_t hi, lo;
-            split_bf16(d0, d1, hi, lo);
-            *reinterpret_cast<uint32_t *>(sm.Dh + so) = hi;
-            *reinterpret_cast<uint32_t *>(sm.Dl + so) = lo;
-            split_bf16(d0 * __expf(gC - st.G[t]), d1 * __expf(gC - st.G[t + 1]), hi, lo);
-            *reinterpret_cast<uint32_t *>(sm.Th + so) = hi;
-            *reinterpret_cast<uint32_t *>(sm.Tl + so) = lo;
+            const float2 u = f16x2_to_float2(*reinterpret_cast<const uint32_t *>(
+                st.U + (gid + 8 * hr) * RC + 2 * (16 * w + 8 * a + 2 * tig)));
+            Dc[a][2 * hr] = u.x;
+            Dc[a][2 * hr + 1] = u.y;
+            Rc[a][2 * hr] = Rc[a][2 * hr + 1] = 0.f;
+          }
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          uint32_t sf[4], nf[4], bw[4], bq[4];
+          lda_p<kP128>(sf, sm.Sn, 0, 16 * ks, lane);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) nf[e] = sf[e] ^ 0x80008000u;  // -S
+          ldb_nk_p<kP128>(bw, W, 16 * w, 16 * ks, lane);
+          ldb_nk_p<kP128>(bq, Qs, 16 * w, 16 * ks, lane);
+          mma_f16(Dc[0], nf, bw[0], bw[1]);
+          mma_f16(Dc[1], nf, bw[2], bw[3]);
+          mma_f16(Rc[0], sf, bq[0], bq[1]);
+          mma_f16(Rc[1], sf, bq[2], bq[3]);
+        }
+        // D and its carry-scaled copy (fp16) for the other warps; R scaled by e^(G_t)
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int j = gid + 8 * hr, t = 16 * w + 8 * a + 2 * tig;
+            const float d0 = Dc[a][2 * hr], d1 = Dc[a][2 * hr + 1];
+            *reinterpret_cast<uint32_t *>(sm.Db + j * RC + 2 * t) = pack_f16(d0, d1);
+            *reinterpret_cast<uint32_t *>(sm.Dd + j * RC + 2 * t) =
+                pack_f16(d0 * ED[t], d1 * ED[t + 1]);
+            Rc[a][2 * hr] *= EG[t];
+            Rc[a][2 * hr + 1] *= EG[t + 1];
           }
       }
-      bar_sync(1, kConsumers);
-      // S^T <- exp(G_T) S^T + Dt^T K over this warp's 32 keys
-      float Xh[4][4], Xl[4][4];
+      bar_sync(1, kComp);
+
+      // ---- S^T <- e^(G_C) S^T + Dd^T K over keys 32w .. 32w+31
+      {
+        float X[4][4];
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) Xh[a][e] = Xl[a][e] = 0.f;
+          for (int e = 0; e < 4; ++e) X[a][e] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < TT; ++ks) {
-        uint32_t th[4], tl[4];
-        lda_tile<RB>(th, sm.Th, 0, 16 * ks, lane);
-        lda_tile<RB>(tl, sm.Tl, 0, 16 * ks, lane);
+        for (int ks = 0; ks < MT; ++ks) {
+          uint32_t df[4];
+          lda_p<RC>(df, sm.Dd, 0, 16 * ks, lane);
 #pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          uint32_t b[4];
-          ldb_kn<kRowB>(b, st.K, 16 * ks, 32 * wq + 16 * np, lane);
-          mma_bf16(Xh[2 * np], th, b[0], b[1]);
-          mma_bf16(Xl[2 * np], tl, b[0], b[1]);
-          mma_bf16(Xh[2 * np + 1], th, b[2], b[3]);
-          mma_bf16(Xl[2 * np + 1], tl, b[2], b[3]);
+          for (int np = 0; np < 2; ++np) {
+            uint32_t b[4];
+            ldb_kn_p<kP128>(b, Ks, 16 * ks, 32 * w + 16 * np, lane);
+            mma_f16(X[2 * np], df, b[0], b[1]);
+            mma_f16(X[2 * np + 1], df, b[2], b[3]);
+          }
+        }
+        const float egc = EG[C - 1];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) Sa[nt][e] = fmaf(egc, Sa[nt][e], X[nt][e]);
+      }
+
+      if (w < MT) {
+        // ---- O^T += D^T A^T over the causal part (A is zero above the diagonal)
+        for (int ks = 0; ks <= w; ++ks) {
+          uint32_t df[4], ba[4];
+          lda_p<RC>(df, sm.Db, 0, 16 * ks, lane);
+          ldb_nk_p<RC>(ba, A, 16 * w, 16 * ks, lane);
+          mma_f16(Rc[0], df, ba[0], ba[1]);
+          mma_f16(Rc[1], df, ba[2], ba[3]);
+        }
+        // stage O^T [t][j] and store this warp's rows that lie in the sequence
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            Elem<TO>::store(&sm.O[w][8 * a + 2 * tig + (e & 1)][gid + 8 * (e >> 1)], Rc[a][e]);
+        __syncwarp();
+        constexpr int EPG = 16 / sizeof(TO);  // elements per 16-byte granule
+        constexpr int GPR = kDVB / EPG;       // granules per output row
+        for (int e = lane; e < 16 * GPR; e += 32) {
+          const int r = e / GPR, gi = e % GPR, t = 16 * w + r;
+          if (t < L)
+            *reinterpret_cast<uint4 *>(o + ((size_t)(tok0 + t) * p.hv + h) * kD + blk * kDVB +
+                                       gi * EPG) =
+                *reinterpret_cast<const uint4 *>(&sm.O[w][r][gi * EPG]);
         }
       }
-      const float egc = __expf(gC);
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) Sa[nt][e] = egc * Sa[nt][e] + (Xh[nt][e] + Xl[nt][e]);
       write_snapshot();
-      bar_sync(2, kConsumers);
+      bar_sync(1, kComp);
       if (tid == 0) mbar_arrive(&sm.empty[s]);
     }
     if (!ok && lane == 0) atomicExch(p.err, 1);
@@ -595,85 +653,7 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        sm.S32[32 * wq + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)] = Sa[nt][e];
-  } else {
-    // ---- output warps: wq owns tokens 16wq..16wq+15
-    const int wq = warp - kStateWarps;
-    bar_sync(2, kConsumers);
-    bool ok = true;
-#pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1;
-      typename Smem::Stage &st = sm.st[s];
-      ok = mbar_wait(&sm.full[s], (c >> 1) & 1) && ok;
-      const int tok0 = bos + c * C;
-      const int L = min(C, eos - tok0);
-      float Rh[2][2][4], Rl[2][2][4];  // [k half][n-tile][.]
-#pragma unroll
-      for (int x = 0; x < 2; ++x)
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) Rh[x][a][e] = Rl[x][a][e] = 0.f;
-      if (wq < TT) {
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          uint32_t sh[4], sl[4], bq[4];
-          lda_tile<kRowB>(sh, sm.Sh, 0, 16 * ks, lane);
-          lda_tile<kRowB>(sl, sm.Sl, 0, 16 * ks, lane);
-          ldb_nk<kRowB>(bq, st.Q, 16 * wq, 16 * ks, lane);
-          const int x = ks & 1;
-#pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            mma_bf16(Rh[x][a], sh, bq[2 * a], bq[2 * a + 1]);
-            mma_bf16(Rl[x][a], sl, bq[2 * a], bq[2 * a + 1]);
-          }
-        }
-      }
-      bar_sync(1, kConsumers);
-      if (wq < TT) {
-        // O^T = exp(G) R^T + D^T A^T over the causal part of the block
-        float O1[2][4], O2[2][4], O3[2][4];
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) O1[a][e] = O2[a][e] = O3[a][e] = 0.f;
-        for (int ks = 0; ks <= wq; ++ks) {
-          uint32_t dh[4], dl[4], bh[4], bl[4];
-          lda_tile<RB>(dh, sm.Dh, 0, 16 * ks, lane);
-          lda_tile<RB>(dl, sm.Dl, 0, 16 * ks, lane);
-          ldb_nk<RB>(bh, st.Ah, 16 * wq, 16 * ks, lane);
-          ldb_nk<RB>(bl, st.Al, 16 * wq, 16 * ks, lane);
-#pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            mma_bf16(O1[a], dh, bh[2 * a], bh[2 * a + 1]);
-            mma_bf16(O2[a], dl, bh[2 * a], bh[2 * a + 1]);
-            mma_bf16(O3[a], dh, bl[2 * a], bl[2 * a + 1]);
-          }
-        }
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int t = 16 * wq + 8 * a + 2 * tig + (e & 1);
-            const float r = (Rh[0][a][e] + Rl[0][a][e]) + (Rh[1][a][e] + Rl[1][a][e]);
-            Elem<TO>::store(&sm.O[wq][t - 16 * wq][gid + 8 * (e >> 1)],
-                            __expf(st.G[t]) * r + (O1[a][e] + O2[a][e] + O3[a][e]));
-          }
-        __syncwarp();
-        constexpr int EPG = 16 / sizeof(TO);  // elements per 16-byte granule
-        constexpr int GPR = kDVB / EPG;       // granules per output row
-        for (int e = lane; e < 16 * GPR; e += 32) {
-          const int r = e / GPR, gi = e % GPR, t = 16 * wq + r;
-          if (t < L)
-            *reinterpret_cast<uint4 *>(o + ((size_t)(tok0 + t) * p.hv + h) * kD + blk * kDVB +
-                                       gi * EPG) =
-                *reinterpret_cast<const uint4 *>(&sm.O[wq][r][gi * EPG]);
-        }
-      }
-      bar_sync(2, kConsumers);
-    }
-    if (!ok && lane == 0) atomicExch(p.err, 1);
+        sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)] = Sa[nt][e];
   }
   __syncthreads();
   for (int e = tid; e < kD * kDVB / 4; e += kRecThreads) {
@@ -702,8 +682,8 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   const long long heads = (long long)p.num_seqs * p.hv;
   const long long max_chunks = ((long long)p.total_tokens + C - 1) / C;
-  // prep CTAs per (sequence, head): enough to fill the GPU a few times over
-  long long per_head = (4LL * sms + heads - 1) / heads;
+  // pass-1 CTAs per (sequence, head): one per block up to about 8 CTAs per SM in total
+  long long per_head = (8LL * sms + heads - 1) / heads;
   per_head = max(1LL, min(per_head, max(1LL, max_chunks)));
 
   if (p.total_tokens > 0) {
@@ -722,7 +702,13 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
 
 size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk) {
   const size_t slots = (size_t)hv * ((size_t)total_tokens / chunk + num_seqs);
-  return 256 + slots * slot_bytes(chunk);
+  size_t sb = 0;
+  switch (chunk) {
+    case 16: sb = slot_bytes(16); break;
+    case 32: sb = slot_bytes(32); break;
+    default: sb = slot_bytes(64); break;
+  }
+  return 256 + slots * sb;
 }
 
 cudaError_t launch_chunk_bf16(const ChunkParams &p, cudaStream_t stream) {

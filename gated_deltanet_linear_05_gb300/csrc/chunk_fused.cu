@@ -18,8 +18,9 @@
 // This needs no workspace.  With one CTA per head it suits batches of at least about
 // one CTA per SM; few-head batches use the two-pass path (chunk_bf16.cu), which spreads
 // each head over several CTAs.
-// Precision as in the two-pass path: q, k, v enter exactly; T, the state, D and A are
-// carried as bf16 (hi, lo) pairs; W is rounded to bf16 once; fp32 accumulation.
+// Precision as in the two-pass path: the Grams take the bf16 inputs exactly; every
+// other product takes fp16 operands (q, k, v converted exactly; T, W, A, D and the
+// state rounded to 11 significant bits for the product only) with fp32 accumulation.
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,15 +28,43 @@ namespace gdn {
 
 namespace {
 
-constexpr int kFRowB = kD * 2;
 constexpr int kFThreads = 256;
 
-__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-  split_bf16(x0, x1, hi, lo);
+template <int C, typename TO>
+struct FusedSmem {
+  static constexpr int RC = row_c(C);
+  static constexpr int LD = C + 4;
+  static constexpr size_t kNTBytes = (size_t)2 * C * LD * 4;
+  static constexpr size_t kOBytes = (size_t)8 * C * 16 * sizeof(TO);
+  // q, k, v rows of the current block and of the next one (prefetched); bf16 as loaded,
+  // converted in place to fp16 once the Grams are done
+  alignas(128) char K[2][C * kP128];
+  alignas(16) char Q[2][C * kP128];
+  alignas(16) char V[2][C * kP128];
+  alignas(16) char W[C * kP128];  // fp16 W [t][key]
+  alignas(16) char A[C * RC];     // fp16 causal decay-masked Q K^T [t][j]
+  alignas(16) char TW[C * RC];    // fp16 T diag(beta e^G)
+  alignas(16) char TU[C * RC];    // fp16 T diag(beta)
+  // N and T (fp32 [C][C+4] each) while the operands are built, then the per-warp
+  // output staging [8][C][16]
+  alignas(16) char NTO[kNTBytes > kOBytes ? kNTBytes : kOBytes];
+  float M[32 * 33];
+  float G[C], EG[C], ED[C], B[C];
+  float gRaw[2][C], bRaw[2][C];
+};
+
+// A fragment (16 rows x 16 k) as fp16 from two 16x8 accumulator tiles (k = their column
+// index), columns scaled by s0, s1 (first tile) and t0, t1 (second tile)
+__device__ __forceinline__ void acc_to_f16(const float (&x)[4], const float (&y)[4], float s0,
+                                           float s1, float t0, float t1, uint32_t (&a)[4]) {
+  a[0] = pack_f16(x[0] * s0, x[1] * s1);
+  a[1] = pack_f16(x[2] * s0, x[3] * s1);
+  a[2] = pack_f16(y[0] * t0, y[1] * t1);
+  a[3] = pack_f16(y[2] * t0, y[3] * t1);
 }
 
-// acc (16x8) += A[r0.., k0..k0+16) * B[k0.., n0..n0+8), fp32 row-major shared matrices,
-// as hi*hi + lo*hi + hi*lo of their bf16 splits.
+// acc (16x8 tile) += A[r0.., k0..k0+16) * B[k0.., n0..n0+8) for fp32 row-major shared
+// matrices, as hi*hi + lo*hi + hi*lo of their bf16 splits (block-doubling products).
 __device__ __forceinline__ void mma_f32x3f(float (&acc)[4], const float *A, int lda,
                                            const float *B, int ldb, int r0, int k0, int n0,
                                            int lane) {
@@ -43,58 +72,23 @@ __device__ __forceinline__ void mma_f32x3f(float (&acc)[4], const float *A, int 
   uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
   const float *a0 = A + (r0 + gid) * lda + k0 + 2 * tig;
   const float *a1 = a0 + 8 * lda;
-  split_pair(a0[0], a0[1], ah[0], al[0]);
-  split_pair(a1[0], a1[1], ah[1], al[1]);
-  split_pair(a0[8], a0[9], ah[2], al[2]);
-  split_pair(a1[8], a1[9], ah[3], al[3]);
+  split_bf16(a0[0], a0[1], ah[0], al[0]);
+  split_bf16(a1[0], a1[1], ah[1], al[1]);
+  split_bf16(a0[8], a0[9], ah[2], al[2]);
+  split_bf16(a1[8], a1[9], ah[3], al[3]);
   const float *b0 = B + (k0 + 2 * tig) * ldb + n0 + gid;
-  split_pair(b0[0], b0[ldb], bh0, bl0);
-  split_pair(b0[8 * ldb], b0[9 * ldb], bh1, bl1);
+  split_bf16(b0[0], b0[ldb], bh0, bl0);
+  split_bf16(b0[8 * ldb], b0[9 * ldb], bh1, bl1);
   mma_bf16(acc, ah, bh0, bh1);
   mma_bf16(acc, al, bh0, bh1);
   mma_bf16(acc, ah, bl0, bl1);
-}
-
-template <int C, typename TO>
-struct FusedSmem {
-  static constexpr int LD = C + 4;
-  static constexpr size_t kNTBytes = (size_t)2 * C * LD * 4;
-  static constexpr size_t kOBytes = (size_t)8 * C * 16 * sizeof(TO);
-  // q, k, v tiles of the current block and of the next one (prefetched)
-  alignas(128) char K[2][C * kFRowB];
-  alignas(128) char Q[2][C * kFRowB];
-  alignas(128) char V[2][C * kFRowB];
-  alignas(128) char W[C * kFRowB];
-  alignas(128) char Ah[C * 2 * C];
-  alignas(128) char Al[C * 2 * C];
-  alignas(128) char TWh[C * 2 * C];
-  alignas(128) char TWl[C * 2 * C];
-  alignas(128) char TUh[C * 2 * C];
-  alignas(128) char TUl[C * 2 * C];
-  // N and T (fp32 [C][C+4] each) while the operands are built, then the per-warp
-  // output staging [8][C][16]
-  alignas(128) char NTO[kNTBytes > kOBytes ? kNTBytes : kOBytes];
-  float M[32 * 33];
-  float G[C], EG[C], B[C];
-  float gRaw[2][C], bRaw[2][C];
-};
-
-// A fragment (16 rows x 16 k) from two 16x8 accumulator tiles (k = their column index),
-// scaled per column by f0 (first tile) / f1 (second tile) pairs, as bf16 (hi, lo).
-__device__ __forceinline__ void acc_to_frag(const float (&x)[4], const float (&y)[4], float s0,
-                                            float s1, float t0, float t1, uint32_t (&hi)[4],
-                                            uint32_t (&lo)[4]) {
-  split_pair(x[0] * s0, x[1] * s1, hi[0], lo[0]);
-  split_pair(x[2] * s0, x[3] * s1, hi[1], lo[1]);
-  split_pair(y[0] * t0, y[1] * t1, hi[2], lo[2]);
-  split_pair(y[2] * t0, y[3] * t1, hi[3], lo[3]);
 }
 
 // C = 16 fits two CTAs per SM (<= 128 registers), so one CTA's state load and store
 // overlap another's arithmetic
 template <int C, typename TO>
 __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(ChunkParams p) {
-  constexpr int NT = kFThreads, MT = C / 16, RB = 2 * C, LD = C + 4;
+  constexpr int NT = kFThreads, MT = C / 16, RC = row_c(C), LD = C + 4;
   constexpr int NTC = C / 8;  // 8-wide token tiles
   using Smem = FusedSmem<C, TO>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -126,9 +120,9 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
       const bool ok = r < Lc;
       const size_t tok = (size_t)t0 + (ok ? r : 0);
       const int nb = ok ? 16 : 0;
-      cp_async16(sm.K[buf] + swz<kFRowB>(r, gr * 16), k + (tok * p.hk + kh) * kD + gr * 8, nb);
-      cp_async16(sm.Q[buf] + swz<kFRowB>(r, gr * 16), q + (tok * p.hk + kh) * kD + gr * 8, nb);
-      cp_async16(sm.V[buf] + swz<kFRowB>(r, gr * 16), v + (tok * p.hv + h) * kD + gr * 8, nb);
+      cp_async16(sm.K[buf] + r * kP128 + gr * 16, k + (tok * p.hk + kh) * kD + gr * 8, nb);
+      cp_async16(sm.Q[buf] + r * kP128 + gr * 16, q + (tok * p.hk + kh) * kD + gr * 8, nb);
+      cp_async16(sm.V[buf] + r * kP128 + gr * 16, v + (tok * p.hv + h) * kD + gr * 8, nb);
     }
     for (int t = tid; t < C; t += NT) {
       const bool ok = t < Lc;
@@ -176,13 +170,15 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
     __syncthreads();  // the previous block is done with shared memory
     if (c + 1 < nchunks) issue_loads(c + 1, buf ^ 1);
     cp_async_commit();
+    // T starts at zero: the doubling products read whole 32x32 blocks of T, whose upper
+    // parts are never written
     for (int e = tid; e < C * LD; e += NT) (&Tm[0][0])[e] = 0.f;
     cp_async_wait<1>();  // this block's group has landed
     __syncthreads();
-    const char *Kb = sm.K[buf], *Qb = sm.Q[buf], *Vb = sm.V[buf];
+    char *Kb = sm.K[buf], *Qb = sm.Q[buf], *Vb = sm.V[buf];
 
-    // in-block inclusive cumsum of g (padding contributes 0), exp(G), beta -- warp 0,
-    // while the Gram products (which do not need the gates) run
+    // in-block inclusive cumsum of g (padding contributes 0), e^G, e^(G_C - G), beta --
+    // warp 0, while the Gram products (which do not need the gates) run
     if (warp == 0) {
       constexpr int E = (C + 31) / 32;
       float gv[E], bv[E], run = 0.f;
@@ -201,18 +197,21 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
         if (lane >= off) incl += y;
       }
       const float excl = incl - run;
+      const float gC = __shfl_sync(0xffffffffu, incl, 31);
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int t = lane * E + e;
         if (t < C) {
-          sm.G[t] = gv[e] + excl;
-          sm.EG[t] = __expf(gv[e] + excl);
+          const float G = gv[e] + excl;
+          sm.G[t] = G;
+          sm.EG[t] = __expf(G);
+          sm.ED[t] = __expf(gC - G);
           sm.B[t] = bv[e];
         }
       }
     }
 
-    // ---- decay-masked Grams: N (fp32) and the causal A (bf16 hi, lo)
+    // ---- decay-masked Grams (bf16 inputs, exact products): N (fp32) and the causal A
     float ga[6][4];
 #pragma unroll
     for (int u = 0; u < 6; ++u)
@@ -224,12 +223,12 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
       for (int ks = 0; ks < kD / 16; ++ks) {
         if (n0 > 0) {
           uint32_t a[4];
-          lda_tile<kFRowB>(a, Asrc, 16 * mt0, 16 * ks, lane);
+          lda_p<kP128>(a, Asrc, 16 * mt0, 16 * ks, lane);
 #pragma unroll
           for (int u = 0; u < 3; ++u) {
             if (u < n0) {
               uint32_t b[4];
-              ldb_nk<kFRowB>(b, Kb, 16 * (np0 + u), 16 * ks, lane);
+              ldb_nk_p<kP128>(b, Kb, 16 * (np0 + u), 16 * ks, lane);
               mma_bf16(ga[2 * u], a, b[0], b[1]);
               mma_bf16(ga[2 * u + 1], a, b[2], b[3]);
             }
@@ -237,14 +236,14 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
         }
         if (mt1 >= 0) {
           uint32_t a[4], b[4];
-          lda_tile<kFRowB>(a, Asrc, 16 * mt1, 16 * ks, lane);
-          ldb_nk<kFRowB>(b, Kb, 0, 16 * ks, lane);
+          lda_p<kP128>(a, Asrc, 16 * mt1, 16 * ks, lane);
+          ldb_nk_p<kP128>(b, Kb, 0, 16 * ks, lane);
           mma_bf16(ga[4], a, b[0], b[1]);
           mma_bf16(ga[5], a, b[2], b[3]);
         }
       }
     }
-    __syncthreads();  // G, EG, B written
+    __syncthreads();  // G, EG, ED, B written; Grams done with the bf16 tiles
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
       int mt, np;
@@ -270,18 +269,22 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
             Nm[t][j] = (j < t) ? bt * d0 * v0 : 0.f;
             Nm[t][j + 1] = (j + 1 < t) ? bt * d1 * v1 : 0.f;
           } else {
-            uint32_t hi, lo;
-            split_pair((j <= t) ? d0 * v0 : 0.f, (j + 1 <= t) ? d1 * v1 : 0.f, hi, lo);
-            *reinterpret_cast<uint32_t *>(sm.Ah + swz<RB>(t, 2 * j)) = hi;
-            *reinterpret_cast<uint32_t *>(sm.Al + swz<RB>(t, 2 * j)) = lo;
+            *reinterpret_cast<uint32_t *>(sm.A + t * RC + 2 * j) =
+                pack_f16((j <= t) ? d0 * v0 : 0.f, (j + 1 <= t) ? d1 * v1 : 0.f);
           }
         }
+    }
+    // the A tile's upper 16x16 blocks (never computed) are zero
+    for (int e = tid; e < C * C / 2; e += NT) {
+      const int t = e / (C / 2), j = 2 * (e % (C / 2));
+      if ((j >> 4) > (t >> 4)) *reinterpret_cast<uint32_t *>(sm.A + t * RC + 2 * j) = 0u;
     }
     __syncthreads();
 
     // ---- T = (I + N)^-1 by block doubling: 16x16 diagonal blocks by forward
     // substitution (a thread per column; x[m] = 0 above the column's diagonal), then
-    // (D + C)^-1 = D^-1 - D^-1 C D^-1 on 16 -> 32 -> 64 with tensor-core products
+    // (D + C)^-1 = D^-1 - D^-1 C D^-1 on 16 -> 32 -> 64 with tensor-core products.
+    // Meanwhile the other threads convert the q, k, v tiles to fp16 in place.
     if (tid < C) {
       const int base = (tid >> 4) * 16, cc = tid & 15;
       float x[16];
@@ -299,25 +302,36 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
         x[r] = val;
         Tm[base + r][base + cc] = val;
       }
+    } else {
+      const int t2 = tid - C, n2 = NT - C;
+      for (int e = t2; e < C * 64; e += n2) {  // 64 packed pairs per 128-element row
+        const int r = e >> 6, cp = e & 63;
+        uint32_t *pk = reinterpret_cast<uint32_t *>(Kb + r * kP128) + cp;
+        uint32_t *pq = reinterpret_cast<uint32_t *>(Qb + r * kP128) + cp;
+        uint32_t *pv = reinterpret_cast<uint32_t *>(Vb + r * kP128) + cp;
+        *pk = bf16x2_to_f16x2(*pk);
+        *pq = bf16x2_to_f16x2(*pq);
+        *pv = bf16x2_to_f16x2(*pv);
+      }
     }
     __syncthreads();
     if (C >= 32) {
-      const int pr = warp >> 1, top = 32 * pr, bot = top + 16, n0 = 8 * (warp & 1);
+      const int pr = warp >> 1, top = 32 * pr, bot = top + 16, nb = 8 * (warp & 1);
       const bool act = warp < 2 * (C / 32);
       if (act) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f32x3f(acc, &Nm[bot][top], LD, &Tm[top][top], LD, 0, 0, n0, lane);
+        mma_f32x3f(acc, &Nm[bot][top], LD, &Tm[top][top], LD, 0, 0, nb, lane);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          sm.M[pr * 256 + (gid + 8 * (e >> 1)) * 16 + n0 + 2 * tig + (e & 1)] = acc[e];
+          sm.M[pr * 256 + (gid + 8 * (e >> 1)) * 16 + nb + 2 * tig + (e & 1)] = acc[e];
       }
       __syncthreads();
       if (act) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f32x3f(acc, &Tm[bot][bot], LD, &sm.M[pr * 256], 16, 0, 0, n0, lane);
+        mma_f32x3f(acc, &Tm[bot][bot], LD, &sm.M[pr * 256], 16, 0, 0, nb, lane);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          Tm[bot + gid + 8 * (e >> 1)][top + n0 + 2 * tig + (e & 1)] = -acc[e];
+          Tm[bot + gid + 8 * (e >> 1)][top + nb + 2 * tig + (e & 1)] = -acc[e];
       }
       __syncthreads();
     }
@@ -354,17 +368,14 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
       __syncthreads();
     }
 
-    // ---- bf16 operands T diag(beta exp G) and T diag(beta), each as high + low part
+    // ---- fp16 operands T diag(beta exp G) and T diag(beta) (upper part masked)
     for (int e = tid; e < C * C / 2; e += NT) {
       const int t = e / (C / 2), j = 2 * (e % (C / 2));
-      const float x0 = Tm[t][j], x1 = Tm[t][j + 1];
-      uint32_t hi, lo;
-      split_pair(x0 * sm.B[j] * sm.EG[j], x1 * sm.B[j + 1] * sm.EG[j + 1], hi, lo);
-      *reinterpret_cast<uint32_t *>(sm.TWh + swz<RB>(t, 2 * j)) = hi;
-      *reinterpret_cast<uint32_t *>(sm.TWl + swz<RB>(t, 2 * j)) = lo;
-      split_pair(x0 * sm.B[j], x1 * sm.B[j + 1], hi, lo);
-      *reinterpret_cast<uint32_t *>(sm.TUh + swz<RB>(t, 2 * j)) = hi;
-      *reinterpret_cast<uint32_t *>(sm.TUl + swz<RB>(t, 2 * j)) = lo;
+      const float x0 = (j <= t) ? Tm[t][j] : 0.f, x1 = (j + 1 <= t) ? Tm[t][j + 1] : 0.f;
+      *reinterpret_cast<uint32_t *>(sm.TW + t * RC + 2 * j) =
+          pack_f16(x0 * sm.B[j] * sm.EG[j], x1 * sm.B[j + 1] * sm.EG[j + 1]);
+      *reinterpret_cast<uint32_t *>(sm.TU + t * RC + 2 * j) =
+          pack_f16(x0 * sm.B[j], x1 * sm.B[j + 1]);
     }
     __syncthreads();
 
@@ -375,22 +386,19 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
       for (int mt = 0; mt < MT; ++mt) {
         float acc[2][4] = {};
         for (int ks = 0; ks <= mt; ++ks) {
-          uint32_t ah[4], al[4], b[4];
-          lda_tile<RB>(ah, sm.TWh, 16 * mt, 16 * ks, lane);
-          lda_tile<RB>(al, sm.TWl, 16 * mt, 16 * ks, lane);
-          ldb_kn<kFRowB>(b, Kb, 16 * ks, i0, lane);
-          mma_bf16(acc[0], ah, b[0], b[1]);
-          mma_bf16(acc[0], al, b[0], b[1]);
-          mma_bf16(acc[1], ah, b[2], b[3]);
-          mma_bf16(acc[1], al, b[2], b[3]);
+          uint32_t a[4], b[4];
+          lda_p<RC>(a, sm.TW, 16 * mt, 16 * ks, lane);
+          ldb_kn_p<kP128>(b, Kb, 16 * ks, i0, lane);
+          mma_f16(acc[0], a, b[0], b[1]);
+          mma_f16(acc[1], a, b[2], b[3]);
         }
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
             const int t = 16 * mt + gid + 8 * hr, col = i0 + 8 * a + 2 * tig;
-            *reinterpret_cast<uint32_t *>(sm.W + swz<kFRowB>(t, 2 * col)) =
-                pack_bf16(acc[a][2 * hr], acc[a][2 * hr + 1]);
+            *reinterpret_cast<uint32_t *>(sm.W + t * kP128 + 2 * col) =
+                pack_f16(acc[a][2 * hr], acc[a][2 * hr + 1]);
           }
       }
     }
@@ -406,17 +414,14 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
 #pragma unroll
     for (int ks = 0; ks < MT; ++ks) {
       uint32_t a[4];
-      lda_tile_t<kFRowB>(a, Vb, j0, 16 * ks, lane);
+      lda_t_p<kP128>(a, Vb, j0, 16 * ks, lane);
 #pragma unroll
       for (int np = 0; np < MT; ++np) {
         if (np >= ks) {
-          uint32_t bh[4], bl[4];
-          ldb_nk<RB>(bh, sm.TUh, 16 * np, 16 * ks, lane);
-          ldb_nk<RB>(bl, sm.TUl, 16 * np, 16 * ks, lane);
-          mma_bf16(Dc[2 * np], a, bh[0], bh[1]);
-          mma_bf16(Dc[2 * np], a, bl[0], bl[1]);
-          mma_bf16(Dc[2 * np + 1], a, bh[2], bh[3]);
-          mma_bf16(Dc[2 * np + 1], a, bl[2], bl[3]);
+          uint32_t b[4];
+          ldb_nk_p<RC>(b, sm.TU, 16 * np, 16 * ks, lane);
+          mma_f16(Dc[2 * np], a, b[0], b[1]);
+          mma_f16(Dc[2 * np + 1], a, b[2], b[3]);
         }
       }
     }
@@ -427,28 +432,22 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
       for (int e = 0; e < 4; ++e) Rc[a][e] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < kD / 16; ++ks) {
-      uint32_t sh[4], sl[4], nh[4], nl[4];
-      acc_to_frag(S[2 * ks], S[2 * ks + 1], 1.f, 1.f, 1.f, 1.f, sh, sl);
+      uint32_t sf[4], nf[4];
+      acc_to_f16(S[2 * ks], S[2 * ks + 1], 1.f, 1.f, 1.f, 1.f, sf);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        nh[e] = sh[e] ^ 0x80008000u;  // -S
-        nl[e] = sl[e] ^ 0x80008000u;
-      }
+      for (int e = 0; e < 4; ++e) nf[e] = sf[e] ^ 0x80008000u;  // -S
 #pragma unroll
       for (int np = 0; np < MT; ++np) {
         uint32_t bw[4], bq[4];
-        ldb_nk<kFRowB>(bw, sm.W, 16 * np, 16 * ks, lane);
-        ldb_nk<kFRowB>(bq, Qb, 16 * np, 16 * ks, lane);
+        ldb_nk_p<kP128>(bw, sm.W, 16 * np, 16 * ks, lane);
+        ldb_nk_p<kP128>(bq, Qb, 16 * np, 16 * ks, lane);
 #pragma unroll
         for (int a = 0; a < 2; ++a) {
-          mma_bf16(Dc[2 * np + a], nh, bw[2 * a], bw[2 * a + 1]);
-          mma_bf16(Dc[2 * np + a], nl, bw[2 * a], bw[2 * a + 1]);
-          mma_bf16(Rc[2 * np + a], sh, bq[2 * a], bq[2 * a + 1]);
-          mma_bf16(Rc[2 * np + a], sl, bq[2 * a], bq[2 * a + 1]);
+          mma_f16(Dc[2 * np + a], nf, bw[2 * a], bw[2 * a + 1]);
+          mma_f16(Rc[2 * np + a], sf, bq[2 * a], bq[2 * a + 1]);
         }
       }
     }
-    const float gC = sm.G[C - 1];
     // O^T = exp(G) R^T + D^T A^T over the causal part
 #pragma unroll
     for (int nt = 0; nt < NTC; ++nt)
@@ -456,20 +455,15 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
       for (int e = 0; e < 4; ++e) Rc[nt][e] *= sm.EG[8 * nt + 2 * tig + (e & 1)];
 #pragma unroll
     for (int ks = 0; ks < MT; ++ks) {
-      uint32_t dh[4], dl[4];
-      acc_to_frag(Dc[2 * ks], Dc[2 * ks + 1], 1.f, 1.f, 1.f, 1.f, dh, dl);
+      uint32_t df[4];
+      acc_to_f16(Dc[2 * ks], Dc[2 * ks + 1], 1.f, 1.f, 1.f, 1.f, df);
 #pragma unroll
       for (int np = 0; np < MT; ++np) {
         if (np >= ks) {
-          uint32_t bh[4], bl[4];
-          ldb_nk<RB>(bh, sm.Ah, 16 * np, 16 * ks, lane);
-          ldb_nk<RB>(bl, sm.Al, 16 * np, 16 * ks, lane);
+          uint32_t b[4];
+          ldb_nk_p<RC>(b, sm.A, 16 * np, 16 * ks, lane);
 #pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            mma_bf16(Rc[2 * np + a], dh, bh[2 * a], bh[2 * a + 1]);
-            mma_bf16(Rc[2 * np + a], dl, bh[2 * a], bh[2 * a + 1]);
-            mma_bf16(Rc[2 * np + a], dh, bl[2 * a], bl[2 * a + 1]);
-          }
+          for (int a = 0; a < 2; ++a) mma_f16(Rc[2 * np + a], df, b[2 * a], b[2 * a + 1]);
         }
       }
     }
@@ -491,7 +485,7 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
       }
     }
     // S^T <- exp(G_T) S^T + (D^T diag(exp(G_T - G))) K
-    const float egc = __expf(gC);
+    const float egc = sm.EG[C - 1];
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt)
 #pragma unroll
@@ -499,17 +493,15 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
 #pragma unroll
     for (int ks = 0; ks < MT; ++ks) {
       const int t0 = 16 * ks + 2 * tig;
-      uint32_t th[4], tl[4];
-      acc_to_frag(Dc[2 * ks], Dc[2 * ks + 1], __expf(gC - sm.G[t0]), __expf(gC - sm.G[t0 + 1]),
-                  __expf(gC - sm.G[t0 + 8]), __expf(gC - sm.G[t0 + 9]), th, tl);
+      uint32_t tf[4];
+      acc_to_f16(Dc[2 * ks], Dc[2 * ks + 1], sm.ED[t0], sm.ED[t0 + 1], sm.ED[t0 + 8],
+                 sm.ED[t0 + 9], tf);
 #pragma unroll
       for (int np = 0; np < 8; ++np) {
         uint32_t b[4];
-        ldb_kn<kFRowB>(b, Kb, 16 * ks, 16 * np, lane);
-        mma_bf16(S[2 * np], th, b[0], b[1]);
-        mma_bf16(S[2 * np], tl, b[0], b[1]);
-        mma_bf16(S[2 * np + 1], th, b[2], b[3]);
-        mma_bf16(S[2 * np + 1], tl, b[2], b[3]);
+        ldb_kn_p<kP128>(b, Kb, 16 * ks, 16 * np, lane);
+        mma_f16(S[2 * np], tf, b[0], b[1]);
+        mma_f16(S[2 * np + 1], tf, b[2], b[3]);
       }
     }
   }

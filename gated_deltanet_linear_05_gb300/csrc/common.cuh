@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -192,6 +193,68 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uin
   const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
   hi = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
   lo = pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+}
+
+// ------------------------------------------------------------------ fp16 operands
+// mma.sync m16n8k16 with fp16 inputs and fp32 accumulation (same fragment ownership as
+// mma_bf16).  fp16 keeps 11 significant bits against bf16's 8.
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (lo, hi) -> packed fp16 pair, round to nearest even
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// packed bf16 pair -> packed fp16 pair (exact for |x| >= 2^-14 and below 65504; tiny
+// values round to the fp16 subnormal grid, an absolute change below 2^-25)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+  return pack_f16(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t x) {
+  __half2 h = *reinterpret_cast<__half2 *>(&x);
+  return __half22float2(h);
+}
+
+// Padded row-major 16-bit tiles: row r starts at r * STRIDE bytes, STRIDE = 16 mod 128
+// (272 for 128-element rows, 2C + 16 for C-element rows), so the eight 16-byte rows
+// of an ldmatrix read fall on eight different bank groups.
+template <int STRIDE>
+__device__ __forceinline__ const char *pad_at(const char *base, int r, int col) {
+  return base + r * STRIDE + col * 2;
+}
+// A-operand 16x16 (rows m0.., k cols k0..) from a tile stored [m][k]
+template <int STRIDE>
+__device__ __forceinline__ void lda_p(uint32_t (&a)[4], const char *base, int m0, int k0,
+                                      int lane) {
+  ldsm_x4(a, pad_at<STRIDE>(base, m0 + (lane & 7) + ((lane >> 3) & 1) * 8, k0 + (lane >> 4) * 8));
+}
+// A-operand 16x16 (rows m0.., k cols k0..) from a tile stored [k][m]
+template <int STRIDE>
+__device__ __forceinline__ void lda_t_p(uint32_t (&a)[4], const char *base, int m0, int k0,
+                                        int lane) {
+  ldsm_x4_t(a, pad_at<STRIDE>(base, k0 + (lane & 7) + (lane >> 4) * 8, m0 + ((lane >> 3) & 1) * 8));
+}
+// Two B-operands (n-tiles n0, n0+8; k 16 wide at k0) from a tile stored [n][k]:
+// b[0], b[1] for n-tile n0, b[2], b[3] for n-tile n0 + 8
+template <int STRIDE>
+__device__ __forceinline__ void ldb_nk_p(uint32_t (&b)[4], const char *base, int n0, int k0,
+                                         int lane) {
+  ldsm_x4(b, pad_at<STRIDE>(base, n0 + (lane & 7) + (lane >> 4) * 8, k0 + ((lane >> 3) & 1) * 8));
+}
+// Two B-operands (n-tiles n0, n0+8; k 16 wide at k0) from a tile stored [k][n]
+template <int STRIDE>
+__device__ __forceinline__ void ldb_kn_p(uint32_t (&b)[4], const char *base, int k0, int n0,
+                                         int lane) {
+  ldsm_x4_t(b, pad_at<STRIDE>(base, k0 + (lane & 7) + ((lane >> 3) & 1) * 8, n0 + (lane >> 4) * 8));
 }
 
 // Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.

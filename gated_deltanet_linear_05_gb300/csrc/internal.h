@@ -29,28 +29,34 @@ struct ChunkParams {
   float *state_out;
   const int32_t *cu_seqlens;
   void *o;
-  // Workspace of the two-pass bf16 path (see chunk_bf16.cu): one slot per (v-head,
-  // block); block c of sequence n uses slot bos_n / C + n + c, which is unique and
-  // below nslots = total_tokens / C + num_seqs.  A slot holds, for the C rows of the
-  // block (rows past the sequence end are zero), in the shared-memory layout the
-  // pass-2 kernel uses:
-  //   W  bf16 [C][128] (swizzled)   W = (I+N)^-1 diag(beta e^G) K
-  //   Q  bf16 [C][128] (swizzled)   K  bf16 [C][128] (swizzled)
-  //   Ah, Al bf16 [C][C] (swizzled) decay-masked causal Q K^T, hi and lo parts
-  //   U  fp32 [128][C+4]            U^T, U = (I+N)^-1 diag(beta) V
-  //   G  fp32 [C]                   in-block inclusive cumsum of g
+  // Workspace of the two-pass bf16 path (chunk_bf16.cu): one slot per (v-head,
+  // block); block c of sequence n uses slot bos_n / C + n + c, which is unique and below
+  // nslots = total_tokens / C + num_seqs.  A slot holds the block's operands for pass 2
+  // in the padded shared-memory layout that pass reads (rows past the sequence end zero):
+  //   W   fp16 [C][128], rows of 272 B     W = (I+N)^-1 diag(beta e^G) K
+  //   Q   fp16 [C][128], rows of 272 B     the block's q rows (k-head of this v-head)
+  //   K   fp16 [C][128], rows of 272 B     the block's k rows
+  //   A   fp16 [C][C],   rows of 2C+16 B   decay-masked causal Q K^T
+  //   DEC fp32 [3][C]                      G (in-block cumsum), e^G, e^(G_C - G)
+  //   U^T fp16 [128][C], rows of 2C+16 B   U = (I+N)^-1 diag(beta) V, by value column
   int nslots;
   char *slot_ws;      // Hv * nslots slots of slot_bytes(C) bytes, 128-byte aligned
   int *err;           // device status word: nonzero if a kernel wait timed out
 };
 
-// Bytes of one workspace slot for block length C.
-__host__ __device__ constexpr size_t slot_head_bytes(int C) {
-  return (size_t)3 * 256 * C + (size_t)4 * C * C;
-}
-__host__ __device__ constexpr size_t slot_u_bytes(int C) { return (size_t)128 * (C + 4) * 4; }
+// Padded row bytes of 16-bit tiles: 128-element rows and C-element rows.
+constexpr int kP128 = 272;
+__host__ __device__ constexpr int row_c(int C) { return 2 * C + 16; }
+// Slot layout offsets (bytes) for block length C.
+__host__ __device__ constexpr size_t slot_q_off(int C) { return (size_t)C * kP128; }
+__host__ __device__ constexpr size_t slot_k_off(int C) { return (size_t)2 * C * kP128; }
+__host__ __device__ constexpr size_t slot_a_off(int C) { return (size_t)3 * C * kP128; }
+__host__ __device__ constexpr size_t slot_dec_off(int C) { return slot_a_off(C) + (size_t)C * row_c(C); }
+// W | Q | K | A | DEC, contiguous: what every pass-2 CTA of the head copies
+__host__ __device__ constexpr size_t slot_head_bytes(int C) { return slot_dec_off(C) + (size_t)12 * C; }
+__host__ __device__ constexpr size_t slot_u_off(int C) { return slot_head_bytes(C); }
 __host__ __device__ constexpr size_t slot_bytes(int C) {
-  return (slot_head_bytes(C) + slot_u_bytes(C) + (size_t)4 * C + 127) / 128 * 128;
+  return (slot_u_off(C) + (size_t)128 * row_c(C) + 127) / 128 * 128;
 }
 
 // Workspace bytes of the bf16 chunk path: a 256-byte header (status word) + slots.

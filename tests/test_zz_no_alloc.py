@@ -76,8 +76,9 @@ def test_noalloc_matches_workspace_entry_on_two_calls(gdn, o_fp32):
 
 def test_noalloc_rejects_requests_beyond_its_scratch(gdn):
     import torch
-    wl = gi.prefill_t4096_h16()      # needs ~84 MB of scratch, more than the 64 MiB built in
-    T, H = wl.total_tokens, wl.num_v_heads
+    # one sequence of 8192 tokens over 16 heads needs ~95 MB of scratch, more than the
+    # 64 MiB built in
+    T, H = 8192, 16
     shape = gdn.make_shape(1, T, H, H, chunk=64)
     assert gdn.gdn_workspace_size(shape, gdn.GDN_OP_PREFILL) > (64 << 20)
     d = {"q": torch.zeros((T, H, 128), dtype=torch.bfloat16, device="cuda")}
