@@ -9,18 +9,21 @@
 //   D = U - W S0,   U = T diag(beta) V,   W = T diag(beta exp G) K,
 // so the work falls in two passes:
 //   pass 1 (prep_kernel, one CTA per (block, v-head), all in parallel): G, the
-//     decay-masked Grams, T by exact block doubling (16x16 diagonal blocks by forward
-//     substitution, then (D + C)^-1 = D^-1 - D^-1 C D^-1 on 16 -> 32 -> 64), and the
-//     products W and U.  Each block's W, fp16 q and k rows, A, decays and U^T go to its
-//     own workspace slot in the padded shared-memory layout pass 2 reads.
+//     decay-masked Grams, the inverses T_ii = (I + N_ii)^-1 of the 16x16 diagonal blocks
+//     of I + N by forward substitution, and W and U by blocked forward substitution
+//     over the 16-token blocks, X_i = T_ii (R_i - sum_{j<i} N_ij X_j) -- the same
+//     triangular solve as the block inverse of the page, applied to the right-hand
+//     sides instead of forming (I + N)^-1.  Each block's W^T, fp16 q and k rows, A,
+//     decays and U^T go to its own workspace slot in the padded shared-memory layout
+//     pass 2 reads.
 //   pass 2 (recur_kernel, one CTA per (sequence, v-head, 16 value columns)): walks the
 //     blocks of the sequence in order with the state block S[:, cols] in fp32 registers
 //     (read from state_in once, written to state_out once).  A producer warp streams
 //     each block's slot part into a 2-stage shared-memory ring with two bulk (TMA)
-//     copies signalled on mbarriers.  Four compute warps each own 16 tokens
-//     of the block for
+//     copies signalled on mbarriers.  Eight compute warps each own 8 tokens of the
+//     block for
 //       D^T = U^T - S^T W^T   and   R^T = S^T Q^T   (sharing the S^T fragments),
-//     exchange D once through shared memory, then each carries 32 keys of the state,
+//     exchange D once through shared memory, then each carries 16 keys of the state,
 //       S^T <- exp(G_T) S^T + (D^T diag(exp(G_T - G))) K,
 //     and finishes its tokens' outputs O^T = diag(e^G) R^T + D^T A^T.
 // Tensor-core products (mma.sync) take fp16 operands with fp32 accumulation: bf16 q, k
@@ -40,41 +43,26 @@ __device__ __forceinline__ size_t slot_index(int bos, int chunk, int n, int c) {
   return (size_t)(bos / chunk + n + c);
 }
 
-// acc (16x8 tile) += A[r0.., k0..k0+16) * B[k0.., n0..n0+8) for fp32 row-major matrices in
-// shared memory, as hi*hi + lo*hi + hi*lo of their bf16 splits (~16 significant bits).
-// Used by the small block-doubling products, where T's own accuracy is set.
-__device__ __forceinline__ void mma_f32x3(float (&acc)[4], const float *A, int lda,
-                                          const float *B, int ldb, int r0, int k0, int n0,
-                                          int lane) {
-  const int gid = lane >> 2, tig = lane & 3;
-  uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
-  const float *a0 = A + (r0 + gid) * lda + k0 + 2 * tig;
-  const float *a1 = a0 + 8 * lda;
-  split_bf16(a0[0], a0[1], ah[0], al[0]);
-  split_bf16(a1[0], a1[1], ah[1], al[1]);
-  split_bf16(a0[8], a0[9], ah[2], al[2]);
-  split_bf16(a1[8], a1[9], ah[3], al[3]);
-  const float *b0 = B + (k0 + 2 * tig) * ldb + n0 + gid;
-  split_bf16(b0[0], b0[ldb], bh0, bl0);
-  split_bf16(b0[8 * ldb], b0[9 * ldb], bh1, bl1);
-  mma_bf16(acc, ah, bh0, bh1);
-  mma_bf16(acc, al, bh0, bh1);
-  mma_bf16(acc, ah, bl0, bl1);
+// A fragment (16 rows x 16 k) as fp16 from two 16x8 accumulator tiles (k = their column
+// index), columns scaled by s0, s1 (first tile) and t0, t1 (second tile)
+__device__ __forceinline__ void acc_to_f16(const float (&x)[4], const float (&y)[4], float s0,
+                                           float s1, float t0, float t1, uint32_t (&a)[4]) {
+  a[0] = pack_f16(x[0] * s0, x[1] * s1);
+  a[1] = pack_f16(x[2] * s0, x[3] * s1);
+  a[2] = pack_f16(y[0] * t0, y[1] * t1);
+  a[3] = pack_f16(y[2] * t0, y[3] * t1);
 }
 
 // ================================================================== pass 1
 
 template <int C>
 struct PrepSmem {
-  static constexpr int RC = row_c(C);
-  alignas(16) char K[C * kP128];  // bf16 rows; converted in place to fp16 after the Grams
-  alignas(16) char V[C * kP128];  // bf16 rows; converted in place to fp16
-  alignas(16) char Q[C * kP128];  // bf16 rows; converted in place to fp16
-  float N[C][C + 4];
-  float T[C][C + 4];
-  alignas(16) char TW[C * RC];    // A staging (fp16), then fp16 T diag(beta e^G)
-  alignas(16) char TU[C * RC];    // fp16 T diag(beta)
-  float M[32 * 33];
+  alignas(16) char K[C * kP128];  // bf16 rows as loaded (rows past the end: zero)
+  alignas(16) char Q[C * kP128];
+  alignas(16) char V[C * kP128];
+  float Nd[C / 16][16][17];       // diagonal 16x16 blocks of N (fp32)
+  alignas(16) char N16[C * row_c(C)];     // -N (fp16) [t][j], blocks below the diagonal
+  alignas(16) char T16[C / 16][16 * 48];  // fp16 T_ii = (I + N_ii)^-1, rows of 48 B
   float G[C], EG[C], ED[C], B[C];
   float gRaw[C], bRaw[C];
 };
@@ -82,11 +70,10 @@ struct PrepSmem {
 constexpr int kPrepThreads = 256;
 
 template <int C>
-__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, int per_head) {
-  constexpr int NT = kPrepThreads, MT = C / 16, RC = row_c(C), LD = C + 4;
+__global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, int per_head) {
+  constexpr int NT = kPrepThreads, MT = C / 16, RC = row_c(C);
   extern __shared__ __align__(128) unsigned char smem_raw[];
   PrepSmem<C> &sm = *reinterpret_cast<PrepSmem<C> *>(smem_raw);
-  float(*sN)[LD] = sm.N;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -109,12 +96,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, in
     const int tok0 = bos + c * C;
     const int L = min(C, eos - tok0);
     char *slot = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, c)) * slot_bytes(C);
-    char *w_out = slot, *a_out = slot + slot_a_off(C);
+    char *w_out = slot, *a_out = slot + slot_a_off(C), *u_out = slot + slot_u_off(C);
     char *q_out = slot + slot_q_off(C), *k_out = slot + slot_k_off(C);
     float *dec_out = reinterpret_cast<float *>(slot + slot_dec_off(C));
-    char *u_out = slot + slot_u_off(C);
     __syncthreads();  // the previous block is done with shared memory
 
+    // two copy groups: q, k and the gates (the Grams start on them), then v
     for (int e = tid; e < C * 16; e += NT) {
       const int r = e >> 4, gr = e & 15;
       const bool ok = r < L;
@@ -122,7 +109,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, in
       const int nb = ok ? 16 : 0;
       cp_async16(sm.K + r * kP128 + gr * 16, k + (tok * p.hk + kh) * kD + gr * 8, nb);
       cp_async16(sm.Q + r * kP128 + gr * 16, q + (tok * p.hk + kh) * kD + gr * 8, nb);
-      cp_async16(sm.V + r * kP128 + gr * 16, v + (tok * p.hv + h) * kD + gr * 8, nb);
     }
     for (int t = tid; t < C; t += NT) {
       const bool ok = t < L;
@@ -131,13 +117,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, in
       cp_async4(&sm.bRaw[t], p.beta + gi, ok ? 4 : 0);
     }
     cp_async_commit();
-    // T starts at zero: the doubling products read whole 32x32 blocks of T, whose upper
-    // parts are never written
-    for (int e = tid; e < C * LD; e += NT) (&sm.T[0][0])[e] = 0.f;
-    cp_async_wait<0>();
+    for (int e = tid; e < C * 16; e += NT) {
+      const int r = e >> 4, gr = e & 15;
+      const bool ok = r < L;
+      const size_t tok = (size_t)tok0 + (ok ? r : 0);
+      cp_async16(sm.V + r * kP128 + gr * 16, v + (tok * p.hv + h) * kD + gr * 8, ok ? 16 : 0);
+    }
+    cp_async_commit();
+    cp_async_wait<1>();
     __syncthreads();
 
-    // in-block inclusive cumsum of g (padding contributes 0), e^G, e^(G_C - G), beta
+    // in-block inclusive cumsum of g (padding contributes 0), e^G, e^(G_C - G), beta --
+    // warp 0, while the Gram products (which do not need the gates) run
     if (warp == 0) {
       constexpr int E = (C + 31) / 32;
       float gv[E], bv[E], run = 0.f;
@@ -220,8 +211,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, in
     }
     __syncthreads();  // gates ready
 
-    // ---- decay masks: N (fp32, strictly lower, beta_t e^(G_t - G_j)) and A (fp16,
-    //      causal with its diagonal, e^(G_t - G_j)) into the A staging tile
+    // ---- decay masks.  N = beta_t e^(G_t - G_j) k_t.k_j (j < t): fp32 for the diagonal
+    //      blocks, -N in fp16 below them.  A = e^(G_t - G_j) q_t.k_j (j <= t): fp16 to the slot.
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
       int mt, np;
@@ -244,10 +235,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, in
           const float v0 = ga[2 * u + half][2 * hr], v1 = ga[2 * u + half][2 * hr + 1];
           if (prod == 0) {
             const float bt = sm.B[t];
-            sN[t][j] = (j < t) ? bt * d0 * v0 : 0.f;
-            sN[t][j + 1] = (j + 1 < t) ? bt * d1 * v1 : 0.f;
+            const float x0 = (j < t) ? bt * d0 * v0 : 0.f, x1 = (j + 1 < t) ? bt * d1 * v1 : 0.f;
+            if (mt == np) {
+              sm.Nd[mt][t - 16 * mt][j - 16 * np] = x0;
+              sm.Nd[mt][t - 16 * mt][j + 1 - 16 * np] = x1;
+            } else {
+              *reinterpret_cast<uint32_t *>(sm.N16 + t * RC + 2 * j) = pack_f16(-x0, -x1);
+            }
           } else {
-            *reinterpret_cast<uint32_t *>(sm.TW + t * RC + 2 * j) =
+            *reinterpret_cast<uint32_t *>(a_out + t * RC + 2 * j) =
                 pack_f16((j <= t) ? d0 * v0 : 0.f, (j + 1 <= t) ? d1 * v1 : 0.f);
           }
         }
@@ -255,15 +251,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, in
     // the A tile's upper 16x16 blocks (never computed) are zero
     for (int e = tid; e < C * C / 2; e += NT) {
       const int t = e / (C / 2), j = 2 * (e % (C / 2));
-      if ((j >> 4) > (t >> 4)) *reinterpret_cast<uint32_t *>(sm.TW + t * RC + 2 * j) = 0u;
+      if ((j >> 4) > (t >> 4)) *reinterpret_cast<uint32_t *>(a_out + t * RC + 2 * j) = 0u;
     }
     __syncthreads();
 
-    // ---- T = (I + N)^-1.  Level 0: 16x16 diagonal blocks in fp32, one column per
-    //      thread, forward substitution; meanwhile the other warps convert q, k and v to
-    //      fp16 and ship q, k, A and the decays to the slot.
+    cp_async_wait<0>();  // v has landed (visible to all after the next barrier)
+    // ---- T_ii = (I + N_ii)^-1 for the 16x16 diagonal blocks in fp32: one column per
+    //      thread, forward substitution.  Meanwhile the other threads ship the fp16 q, k
+    //      rows and the decays to the slot.
     if (tid < C) {
-      const int base = (tid >> 4) * 16, cc = tid & 15;
+      const int blk = tid >> 4, cc = tid & 15;
       float x[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
@@ -271,30 +268,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, in
 #pragma unroll
         for (int m = 0; m < r; ++m) {  // x[m] = 0 above the column's diagonal
           if (m & 1)
-            a1 = fmaf(sN[base + r][base + m], x[m], a1);
+            a1 = fmaf(sm.Nd[blk][r][m], x[m], a1);
           else
-            a0 = fmaf(sN[base + r][base + m], x[m], a0);
+            a0 = fmaf(sm.Nd[blk][r][m], x[m], a0);
         }
         const float val = (r == cc) ? 1.f : (r < cc ? 0.f : -(a0 + a1));
         x[r] = val;
-        sm.T[base + r][base + cc] = val;
+        *reinterpret_cast<__half *>(sm.T16[blk] + r * 48 + 2 * cc) = __float2half_rn(val);
       }
     } else {
       const int t2 = tid - C, n2 = NT - C;
       for (int e = t2; e < C * 64; e += n2) {  // 64 packed pairs per 128-element row
         const int r = e >> 6, cp = e & 63;
-        uint32_t *pk = reinterpret_cast<uint32_t *>(sm.K + r * kP128) + cp;
-        uint32_t *pq = reinterpret_cast<uint32_t *>(sm.Q + r * kP128) + cp;
-        uint32_t *pv = reinterpret_cast<uint32_t *>(sm.V + r * kP128) + cp;
-        const uint32_t k16 = bf16x2_to_f16x2(*pk), q16 = bf16x2_to_f16x2(*pq);
-        *pk = k16;
-        *pv = bf16x2_to_f16x2(*pv);
-        reinterpret_cast<uint32_t *>(k_out + r * kP128)[cp] = k16;
-        reinterpret_cast<uint32_t *>(q_out + r * kP128)[cp] = q16;
+        reinterpret_cast<uint32_t *>(k_out + r * kP128)[cp] =
+            bf16x2_to_f16x2(reinterpret_cast<const uint32_t *>(sm.K + r * kP128)[cp]);
+        reinterpret_cast<uint32_t *>(q_out + r * kP128)[cp] =
+            bf16x2_to_f16x2(reinterpret_cast<const uint32_t *>(sm.Q + r * kP128)[cp]);
       }
-      constexpr int G16 = RC / 16;  // 16-byte granules per A row (incl. padding)
-      for (int e = t2; e < C * G16; e += n2)
-        reinterpret_cast<uint4 *>(a_out)[e] = reinterpret_cast<const uint4 *>(sm.TW)[e];
       for (int t = t2; t < C; t += n2) {
         dec_out[t] = sm.G[t];
         dec_out[C + t] = sm.EG[t];
@@ -302,134 +292,68 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, in
       }
     }
     __syncthreads();
-    // Level 1 (16 -> 32): lower-left block = -T_bot (N_bl T_top); one 16x8 tile per warp.
-    if (C >= 32) {
-      const int pr = warp >> 1, top = 32 * pr, bot = top + 16, nb = 8 * (warp & 1);
-      if (warp < 2 * (C / 32)) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f32x3(acc, &sN[bot][top], LD, &sm.T[top][top], LD, 0, 0, nb, lane);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sm.M[pr * 256 + (gid + 8 * (e >> 1)) * 16 + nb + 2 * tig + (e & 1)] = acc[e];
-      }
-      __syncthreads();
-      if (warp < 2 * (C / 32)) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f32x3(acc, &sm.T[bot][bot], LD, &sm.M[pr * 256], 16, 0, 0, nb, lane);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sm.T[bot + gid + 8 * (e >> 1)][top + nb + 2 * tig + (e & 1)] = -acc[e];
-      }
-      __syncthreads();
-    }
-    // Level 2 (32 -> 64): lower-left 32x32 block = -T_BB (N_BA T_AA); two tiles per warp.
-    if (C == 64) {
-      const int r0 = 16 * ((warp >> 1) & 1), nb = 16 * (warp & 1);
-      const bool lv2 = warp < 4;
-      if (lv2) {
-        float acc[2][4] = {};
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks)
-            mma_f32x3(acc[a], &sN[32][0], LD, &sm.T[0][0], LD, r0, 16 * ks, nb + 8 * a, lane);
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            sm.M[(r0 + gid + 8 * (e >> 1)) * 33 + nb + 8 * a + 2 * tig + (e & 1)] = acc[a][e];
-      }
-      __syncthreads();
-      if (lv2) {
-        float acc2[2][4] = {};
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks)
-            mma_f32x3(acc2[a], &sm.T[32][32], LD, sm.M, 33, r0, 16 * ks, nb + 8 * a, lane);
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            sm.T[32 + r0 + gid + 8 * (e >> 1)][nb + 8 * a + 2 * tig + (e & 1)] = -acc2[a][e];
-      }
-      __syncthreads();
-    }
 
-    // ---- fp16 operands T diag(beta e^G) and T diag(beta) (T is lower triangular; the
-    //      never-written upper part is masked here)
-    for (int e = tid; e < C * C / 2; e += NT) {
-      const int t = e / (C / 2), j = 2 * (e % (C / 2));
-      const float x0 = (j <= t) ? sm.T[t][j] : 0.f, x1 = (j + 1 <= t) ? sm.T[t][j + 1] : 0.f;
-      *reinterpret_cast<uint32_t *>(sm.TW + t * RC + 2 * j) =
-          pack_f16(x0 * sm.B[j] * sm.EG[j], x1 * sm.B[j + 1] * sm.EG[j + 1]);
-      *reinterpret_cast<uint32_t *>(sm.TU + t * RC + 2 * j) =
-          pack_f16(x0 * sm.B[j], x1 * sm.B[j + 1]);
-    }
-    __syncthreads();
-
-    if (warp < 4) {
-      // ---- W = T diag(beta e^G) K  [t][key]: keys 32 warp .. +32, causal k-steps
-      const int i0 = 32 * warp;
-#pragma unroll 1
-      for (int mt = 0; mt < MT; ++mt) {
-        float acc[4][4];
+    // ---- [W U] = (I + N)^-1 [diag(beta e^G) K  diag(beta) V] by blocked forward
+    //      substitution over the 16-token blocks, X_i = T_ii (R_i - sum_{j<i} N_ij X_j),
+    //      transposed so that each warp solves its own 32 columns without exchange:
+    //      X_i^T = (R_i^T - sum_j X_j^T N_ij^T) T_ii^T.  Warps 0-3: W (32 keys each),
+    //      warps 4-7: U (32 value columns each); both stored by column (W^T, U^T).
+    {
+      const int kind = warp >> 2, c0 = 32 * (warp & 3);
+      const char *X = kind ? sm.V : sm.K;
+      char *xo = kind ? u_out : w_out;
+      uint32_t Xf[MT][2][4];  // fp16 A fragments of the solved blocks X_j^T
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+      for (int i = 0; i < MT; ++i) {
+        float acc[2][2][4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
-        for (int ks = 0; ks <= mt; ++ks) {
-          uint32_t a[4];
-          lda_p<RC>(a, sm.TW, 16 * mt, 16 * ks, lane);
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-          for (int np = 0; np < 2; ++np) {
-            uint32_t b[4];
-            ldb_kn_p<kP128>(b, sm.K, 16 * ks, i0 + 16 * np, lane);
-            mma_f16(acc[2 * np], a, b[0], b[1]);
-            mma_f16(acc[2 * np + 1], a, b[2], b[3]);
-          }
-        }
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int t = 16 * mt + gid + 8 * hr, col = i0 + 8 * nt + 2 * tig;
-            *reinterpret_cast<uint32_t *>(w_out + t * kP128 + 2 * col) =
-                pack_f16(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
-          }
-      }
-    } else {
-      // ---- U^T = V^T (T diag(beta))^T  [value col][t]: value cols 32 (warp-4) .. +32
-      const int j0 = 32 * (warp - 4);
-#pragma unroll 1
-      for (int mj = 0; mj < 2; ++mj) {
-        float acc[C / 8][4];
-#pragma unroll
-        for (int a = 0; a < C / 8; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < MT; ++ks) {
-          uint32_t a[4];
-          lda_t_p<kP128>(a, sm.V, j0 + 16 * mj, 16 * ks, lane);
-#pragma unroll
-          for (int np = 0; np < MT; ++np) {
-            if (np >= ks) {
-              uint32_t b[4];
-              ldb_nk_p<RC>(b, sm.TU, 16 * np, 16 * ks, lane);
-              mma_f16(acc[2 * np], a, b[0], b[1]);
-              mma_f16(acc[2 * np + 1], a, b[2], b[3]);
+            for (int e = 0; e < 4; ++e) {
+              const int t = 16 * i + 8 * nt + 2 * tig + (e & 1);
+              const int col = c0 + 16 * mt + gid + 8 * (e >> 1);
+              const float sc = kind ? sm.B[t] : sm.B[t] * sm.EG[t];
+              acc[mt][nt][e] =
+                  sc * __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(X + t * kP128 + 2 * col));
             }
+#pragma unroll
+        for (int j = 0; j < i; ++j) {
+          uint32_t b[4];
+          ldb_nk_p<RC>(b, sm.N16, 16 * i, 16 * j, lane);  // B[k=j][n=t] = -N[t][j]
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            mma_f16(acc[mt][0], Xf[j][mt], b[0], b[1]);
+            mma_f16(acc[mt][1], Xf[j][mt], b[2], b[3]);
           }
         }
+        uint32_t y[2][4], bt[4];
 #pragma unroll
-        for (int nt = 0; nt < C / 8; ++nt)
+        for (int mt = 0; mt < 2; ++mt)
+          acc_to_f16(acc[mt][0], acc[mt][1], 1.f, 1.f, 1.f, 1.f, y[mt]);
+        ldb_nk_p<48>(bt, sm.T16[i], 0, 0, lane);  // B[k=j'][n=t'] = T_ii[t'][j']
+        float out[2][2][4];
 #pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int j = j0 + 16 * mj + gid + 8 * hr, t = 8 * nt + 2 * tig;
-            *reinterpret_cast<uint32_t *>(u_out + j * RC + 2 * t) =
-                pack_f16(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) out[mt][nt][e] = 0.f;
+            mma_f16(out[mt][nt], y[mt], bt[2 * nt], bt[2 * nt + 1]);
           }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+              const int col = c0 + 16 * mt + gid + 8 * hr, t = 16 * i + 8 * nt + 2 * tig;
+              *reinterpret_cast<uint32_t *>(xo + col * RC + 2 * t) =
+                  pack_f16(out[mt][nt][2 * hr], out[mt][nt][2 * hr + 1]);
+            }
+          if (i + 1 < MT) acc_to_f16(out[mt][0], out[mt][1], 1.f, 1.f, 1.f, 1.f, Xf[i][mt]);
+        }
       }
     }
   }
@@ -437,23 +361,31 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(ChunkParams p, in
 
 // ================================================================== pass 2
 
-constexpr int kCompWarps = 4;
-constexpr int kRecThreads = 32 * (kCompWarps + 1);  // + 1 producer warp
-constexpr int kComp = 32 * kCompWarps;
+constexpr int kChainWarps = 4, kOutWarps = 4;
+constexpr int kRecThreads = 32 * (kChainWarps + kOutWarps + 1);  // + 1 producer warp
+constexpr int kChain = 32 * kChainWarps;
+constexpr int kPair = 32 * (kChainWarps + kOutWarps);
+constexpr int kStages = 3;
 constexpr int kDVB = 16;  // value columns per CTA
+
+// Named barriers of pass 2 (0 is __syncthreads)
+constexpr int kBarChain = 1;   // the chain warps among themselves
+constexpr int kBarSReady = 2;  // +parity: snapshot S_c published (chain arrives, output waits)
+constexpr int kBarDone = 4;    // +parity: output warps done with block c (output arrives, chain waits)
+constexpr int kBarDReady = 6;  // +parity: D_c published (chain arrives, output waits)
 
 template <int C, typename TO>
 struct RecSmem {
   static constexpr int RC = row_c(C);
   struct Stage {
-    alignas(128) char H[slot_head_bytes(C)];  // W | Q | K | A | DEC, as in the slot
+    alignas(128) char H[slot_head_bytes(C)];  // W^T | Q | K | A | DEC, as in the slot
     alignas(16) char U[kDVB * RC];            // U^T rows of this CTA's value columns
-  } st[2];
-  alignas(8) uint64_t full[2], empty[2];
-  alignas(16) char Sn[kDVB * kP128];  // S^T (fp16) [16 value cols][128 keys]
-  alignas(16) char Db[kDVB * RC];     // D^T (fp16) [16 value cols][C tokens]
-  alignas(16) char Dd[kDVB * RC];     // (D diag(e^(G_C - G)))^T (fp16)
-  alignas(16) TO O[kCompWarps][16][kDVB];
+  } st[kStages];
+  alignas(8) uint64_t full[kStages], empty[kStages];
+  alignas(16) char Sn[2][kDVB * kP128];  // S_c^T (fp16) [16 value cols][128 keys], by parity
+  alignas(16) char Db[2][kDVB * RC];     // D_c^T (fp16) [16 value cols][C tokens], by parity
+  alignas(16) char Dd[kDVB * RC];        // (D diag(e^(G_C - G)))^T (fp16)
+  alignas(16) TO O[kOutWarps][16][kDVB];
   alignas(16) float S32[kD][kDVB + 4];  // fp32 staging of the state block
 };
 
@@ -481,21 +413,29 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
   const char *slot0 = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, 0)) * slot_bytes(C);
 
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], 1 + kOutWarps);  // the chain warps once, each output warp
     }
     mbar_fence_init();
   }
+  // state block S[:, blk*16 .. +16) -> fp32 staging (coalesced 64-byte rows)
+  for (int e = tid; e < kD * kDVB / 4; e += kRecThreads) {
+    const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
+    const float4 val =
+        p.state_in ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + 4 * c4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4 *>(&sm.S32[i][4 * c4]) = val;
+  }
   __syncthreads();
 
-  if (warp == kCompWarps) {
-    // ---- producer: stream each block's slot part into the 2-stage ring
+  if (warp == kChainWarps + kOutWarps) {
+    // ---- producer: stream each block's slot part into the ring
     if (lane == 0) {
       bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
-        const int s = c & 1;
-        if (c >= 2) ok = mbar_wait(&sm.empty[s], ((c - 2) >> 1) & 1) && ok;
+        const int s = c % kStages;
+        if (c >= kStages) ok = mbar_wait(&sm.empty[s], ((c / kStages) - 1) & 1) && ok;
         typename Smem::Stage &st = sm.st[s];
         const char *src = slot0 + (size_t)c * slot_bytes(C);
         mbar_arrive_expect_tx(&sm.full[s], kStageTx);
@@ -505,93 +445,82 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
       // the last copies are consumed before the CTA's final barrier
       if (!ok) atomicExch(p.err, 1);
     }
-  } else {
+  } else if (warp < kChainWarps) {
+    // ---- chain warp w: D for tokens 16w .. 16w+15, the state for keys 32w .. 32w+31
     const int w = warp;
-    // state block S[:, blk*16 .. +16) -> fp32 staging (coalesced 64-byte rows)
-    for (int e = tid; e < kD * kDVB / 4; e += kComp) {
-      const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
-      const float4 val =
-          p.state_in ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + 4 * c4)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-      *reinterpret_cast<float4 *>(&sm.S32[i][4 * c4]) = val;
-    }
-    bar_sync(1, kComp);
-    // S^T[j][i] for j = gid (+8), i = 32w + 8nt + 2tig (+1)
-    float Sa[4][4];
+    float Sa[4][4];  // S^T[j][i], j = gid (+8), i = 32w + 8nt + 2tig (+1)
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         Sa[nt][e] = sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)];
-    auto write_snapshot = [&]() {
+    auto write_snapshot = [&](char *Sn) {
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int j = gid + 8 * hr, i = 32 * w + 8 * nt + 2 * tig;
-          *reinterpret_cast<uint32_t *>(sm.Sn + j * kP128 + 2 * i) =
+          *reinterpret_cast<uint32_t *>(Sn + j * kP128 + 2 * i) =
               pack_f16(Sa[nt][2 * hr], Sa[nt][2 * hr + 1]);
         }
     };
-    write_snapshot();
-    bar_sync(1, kComp);
+    write_snapshot(sm.Sn[0]);
+    bar_sync(kBarChain, kChain);
+    bar_arrive(kBarSReady + 0, kPair);
 
     bool ok = true;
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1;
+      const int s = c % kStages, par = c & 1;
       typename Smem::Stage &st = sm.st[s];
-      const char *W = st.H, *Qs = st.H + slot_q_off(C), *Ks = st.H + slot_k_off(C);
-      const char *A = st.H + slot_a_off(C);
+      const char *Wt = st.H, *Ks = st.H + slot_k_off(C);
       const float *DG = reinterpret_cast<const float *>(st.H + slot_dec_off(C));
       const float *EG = DG + C, *ED = DG + 2 * C;
-      const int tok0 = bos + c * C;
-      const int L = min(C, eos - tok0);
-      ok = mbar_wait(&sm.full[s], (c >> 1) & 1) && ok;
+      ok = mbar_wait(&sm.full[s], (c / kStages) & 1) && ok;
 
-      // ---- D^T = U^T - S^T W^T and R^T = S^T Q^T for tokens 16w .. 16w+15
-      float Dc[2][4], Rc[2][4];
       if (w < MT) {
+        // D^T = U^T - S^T W^T for tokens 16w .. 16w+15, keys split in halves
+        float D0[2][4], D1[2][4];
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
             const float2 u = f16x2_to_float2(*reinterpret_cast<const uint32_t *>(
                 st.U + (gid + 8 * hr) * RC + 2 * (16 * w + 8 * a + 2 * tig)));
-            Dc[a][2 * hr] = u.x;
-            Dc[a][2 * hr + 1] = u.y;
-            Rc[a][2 * hr] = Rc[a][2 * hr + 1] = 0.f;
+            D0[a][2 * hr] = u.x;
+            D0[a][2 * hr + 1] = u.y;
+            D1[a][2 * hr] = D1[a][2 * hr + 1] = 0.f;
           }
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
-          uint32_t sf[4], nf[4], bw[4], bq[4];
-          lda_p<kP128>(sf, sm.Sn, 0, 16 * ks, lane);
+          uint32_t nf[4], bw[4];
+          lda_p<kP128>(nf, sm.Sn[par], 0, 16 * ks, lane);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) nf[e] = sf[e] ^ 0x80008000u;  // -S
-          ldb_nk_p<kP128>(bw, W, 16 * w, 16 * ks, lane);
-          ldb_nk_p<kP128>(bq, Qs, 16 * w, 16 * ks, lane);
-          mma_f16(Dc[0], nf, bw[0], bw[1]);
-          mma_f16(Dc[1], nf, bw[2], bw[3]);
-          mma_f16(Rc[0], sf, bq[0], bq[1]);
-          mma_f16(Rc[1], sf, bq[2], bq[3]);
+          for (int e = 0; e < 4; ++e) nf[e] ^= 0x80008000u;  // -S
+          ldb_kn_p<RC>(bw, Wt, 16 * ks, 16 * w, lane);
+          if (ks & 1) {
+            mma_f16(D1[0], nf, bw[0], bw[1]);
+            mma_f16(D1[1], nf, bw[2], bw[3]);
+          } else {
+            mma_f16(D0[0], nf, bw[0], bw[1]);
+            mma_f16(D0[1], nf, bw[2], bw[3]);
+          }
         }
-        // D and its carry-scaled copy (fp16) for the other warps; R scaled by e^(G_t)
+        // D (for the outputs) and its carry-scaled copy (for the state), fp16
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
             const int j = gid + 8 * hr, t = 16 * w + 8 * a + 2 * tig;
-            const float d0 = Dc[a][2 * hr], d1 = Dc[a][2 * hr + 1];
-            *reinterpret_cast<uint32_t *>(sm.Db + j * RC + 2 * t) = pack_f16(d0, d1);
-            *reinterpret_cast<uint32_t *>(sm.Dd + j * RC + 2 * t) =
-                pack_f16(d0 * ED[t], d1 * ED[t + 1]);
-            Rc[a][2 * hr] *= EG[t];
-            Rc[a][2 * hr + 1] *= EG[t + 1];
+            const float d0 = D0[a][2 * hr] + D1[a][2 * hr], d1 = D0[a][2 * hr + 1] + D1[a][2 * hr + 1];
+            *reinterpret_cast<uint32_t *>(sm.Db[par] + j * RC + 2 * t) = pack_f16(d0, d1);
+            *reinterpret_cast<uint32_t *>(sm.Dd + j * RC + 2 * t) = pack_f16(d0 * ED[t], d1 * ED[t + 1]);
           }
       }
-      bar_sync(1, kComp);
+      bar_sync(kBarChain, kChain);
+      bar_arrive(kBarDReady + par, kPair);
 
-      // ---- S^T <- e^(G_C) S^T + Dd^T K over keys 32w .. 32w+31
+      // S^T <- e^(G_C) S^T + Dd^T K over keys 32w .. 32w+31
       {
         float X[4][4];
 #pragma unroll
@@ -616,37 +545,15 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) Sa[nt][e] = fmaf(egc, Sa[nt][e], X[nt][e]);
       }
-
-      if (w < MT) {
-        // ---- O^T += D^T A^T over the causal part (A is zero above the diagonal)
-        for (int ks = 0; ks <= w; ++ks) {
-          uint32_t df[4], ba[4];
-          lda_p<RC>(df, sm.Db, 0, 16 * ks, lane);
-          ldb_nk_p<RC>(ba, A, 16 * w, 16 * ks, lane);
-          mma_f16(Rc[0], df, ba[0], ba[1]);
-          mma_f16(Rc[1], df, ba[2], ba[3]);
-        }
-        // stage O^T [t][j] and store this warp's rows that lie in the sequence
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            Elem<TO>::store(&sm.O[w][8 * a + 2 * tig + (e & 1)][gid + 8 * (e >> 1)], Rc[a][e]);
-        __syncwarp();
-        constexpr int EPG = 16 / sizeof(TO);  // elements per 16-byte granule
-        constexpr int GPR = kDVB / EPG;       // granules per output row
-        for (int e = lane; e < 16 * GPR; e += 32) {
-          const int r = e / GPR, gi = e % GPR, t = 16 * w + r;
-          if (t < L)
-            *reinterpret_cast<uint4 *>(o + ((size_t)(tok0 + t) * p.hv + h) * kD + blk * kDVB +
-                                       gi * EPG) =
-                *reinterpret_cast<const uint4 *>(&sm.O[w][r][gi * EPG]);
-        }
-      }
-      write_snapshot();
-      bar_sync(1, kComp);
+      // S_{c+1} into the other snapshot buffer once the output warps are done with block
+      // c - 1 (which read it as S_{c-1})
+      if (c >= 1) bar_sync(kBarDone + (par ^ 1), kPair);
+      write_snapshot(sm.Sn[par ^ 1]);
+      bar_sync(kBarChain, kChain);
       if (tid == 0) mbar_arrive(&sm.empty[s]);
+      bar_arrive(kBarSReady + (par ^ 1), kPair);
     }
+    if (nchunks >= 1) bar_sync(kBarDone + ((nchunks - 1) & 1), kPair);
     if (!ok && lane == 0) atomicExch(p.err, 1);
     // final state block -> fp32 staging
 #pragma unroll
@@ -654,6 +561,78 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)] = Sa[nt][e];
+  } else {
+    // ---- output warp: O^T = diag(e^G) S^T Q^T + D^T A^T for tokens 16ow .. 16ow+15
+    const int ow = warp - kChainWarps;
+    bool ok = true;
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kStages, par = c & 1;
+      typename Smem::Stage &st = sm.st[s];
+      const char *Qs = st.H + slot_q_off(C), *A = st.H + slot_a_off(C);
+      const float *EG = reinterpret_cast<const float *>(st.H + slot_dec_off(C)) + C;
+      const int tok0 = bos + c * C;
+      const int L = min(C, eos - tok0);
+      ok = mbar_wait(&sm.full[s], (c / kStages) & 1) && ok;
+      bar_sync(kBarSReady + par, kPair);
+      float R0[2][4], R1[2][4];
+      if (ow < MT) {
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) R0[a][e] = R1[a][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          uint32_t sf[4], bq[4];
+          lda_p<kP128>(sf, sm.Sn[par], 0, 16 * ks, lane);
+          ldb_nk_p<kP128>(bq, Qs, 16 * ow, 16 * ks, lane);
+          if (ks & 1) {
+            mma_f16(R1[0], sf, bq[0], bq[1]);
+            mma_f16(R1[1], sf, bq[2], bq[3]);
+          } else {
+            mma_f16(R0[0], sf, bq[0], bq[1]);
+            mma_f16(R0[1], sf, bq[2], bq[3]);
+          }
+        }
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            R0[a][e] = (R0[a][e] + R1[a][e]) * EG[16 * ow + 8 * a + 2 * tig + (e & 1)];
+      }
+      bar_sync(kBarDReady + par, kPair);
+      if (ow < MT) {
+        // O^T += D^T A^T over the causal part (A is zero above the diagonal)
+        for (int ks = 0; ks <= ow; ++ks) {
+          uint32_t df[4], ba[4];
+          lda_p<RC>(df, sm.Db[par], 0, 16 * ks, lane);
+          ldb_nk_p<RC>(ba, A, 16 * ow, 16 * ks, lane);
+          mma_f16(R0[0], df, ba[0], ba[1]);
+          mma_f16(R0[1], df, ba[2], ba[3]);
+        }
+        // stage O^T [t][j] and store this warp's rows that lie in the sequence
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            Elem<TO>::store(&sm.O[ow][8 * a + 2 * tig + (e & 1)][gid + 8 * (e >> 1)], R0[a][e]);
+        __syncwarp();
+        constexpr int EPG = 16 / sizeof(TO);  // elements per 16-byte granule
+        constexpr int GPR = kDVB / EPG;       // granules per output row
+        for (int e = lane; e < 16 * GPR; e += 32) {
+          const int r = e / GPR, gi = e % GPR, t = 16 * ow + r;
+          if (t < L)
+            *reinterpret_cast<uint4 *>(o + ((size_t)(tok0 + t) * p.hv + h) * kD + blk * kDVB +
+                                       gi * EPG) =
+                *reinterpret_cast<const uint4 *>(&sm.O[ow][r][gi * EPG]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+      bar_arrive(kBarDone + par, kPair);
+    }
+    if (nchunks >= 0) bar_sync(kBarSReady + (nchunks & 1), kPair);
+    if (!ok && lane == 0) atomicExch(p.err, 1);
   }
   __syncthreads();
   for (int e = tid; e < kD * kDVB / 4; e += kRecThreads) {

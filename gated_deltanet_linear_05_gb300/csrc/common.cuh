@@ -257,9 +257,30 @@ __device__ __forceinline__ void ldb_kn_p(uint32_t (&b)[4], const char *base, int
   ldsm_x4_t(b, pad_at<STRIDE>(base, k0 + (lane & 7) + ((lane >> 3) & 1) * 8, n0 + (lane >> 4) * 8));
 }
 
+// One B-operand (n-tile n0, k 16 wide at k0) from a tile stored [n][k]: b[0] k lo, b[1] k hi
+template <int STRIDE>
+__device__ __forceinline__ void ldb1_nk_p(uint32_t (&b)[2], const char *base, int n0, int k0,
+                                          int lane) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(b[0]), "=r"(b[1])
+               : "r"(smem_u32(pad_at<STRIDE>(base, n0 + (lane & 7), k0 + ((lane >> 3) & 1) * 8))));
+}
+// One B-operand (n-tile n0, k 16 wide at k0) from a tile stored [k][n]
+template <int STRIDE>
+__device__ __forceinline__ void ldb1_kn_p(uint32_t (&b)[2], const char *base, int k0, int n0,
+                                          int lane) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(b[0]), "=r"(b[1])
+               : "r"(smem_u32(pad_at<STRIDE>(base, k0 + (lane & 7) + ((lane >> 3) & 1) * 8, n0))));
+}
+
 // Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
 __device__ __forceinline__ void bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+// Arrive on named barrier `id` without waiting (producer side of a bar.sync by others).
+__device__ __forceinline__ void bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float x) {

@@ -33,7 +33,7 @@ struct ChunkParams {
   // block); block c of sequence n uses slot bos_n / C + n + c, which is unique and below
   // nslots = total_tokens / C + num_seqs.  A slot holds the block's operands for pass 2
   // in the padded shared-memory layout that pass reads (rows past the sequence end zero):
-  //   W   fp16 [C][128], rows of 272 B     W = (I+N)^-1 diag(beta e^G) K
+  //   W^T fp16 [128][C], rows of 2C+16 B   W = (I+N)^-1 diag(beta e^G) K, by key
   //   Q   fp16 [C][128], rows of 272 B     the block's q rows (k-head of this v-head)
   //   K   fp16 [C][128], rows of 272 B     the block's k rows
   //   A   fp16 [C][C],   rows of 2C+16 B   decay-masked causal Q K^T
@@ -48,11 +48,11 @@ struct ChunkParams {
 constexpr int kP128 = 272;
 __host__ __device__ constexpr int row_c(int C) { return 2 * C + 16; }
 // Slot layout offsets (bytes) for block length C.
-__host__ __device__ constexpr size_t slot_q_off(int C) { return (size_t)C * kP128; }
-__host__ __device__ constexpr size_t slot_k_off(int C) { return (size_t)2 * C * kP128; }
-__host__ __device__ constexpr size_t slot_a_off(int C) { return (size_t)3 * C * kP128; }
+__host__ __device__ constexpr size_t slot_q_off(int C) { return (size_t)128 * row_c(C); }
+__host__ __device__ constexpr size_t slot_k_off(int C) { return slot_q_off(C) + (size_t)C * kP128; }
+__host__ __device__ constexpr size_t slot_a_off(int C) { return slot_k_off(C) + (size_t)C * kP128; }
 __host__ __device__ constexpr size_t slot_dec_off(int C) { return slot_a_off(C) + (size_t)C * row_c(C); }
-// W | Q | K | A | DEC, contiguous: what every pass-2 CTA of the head copies
+// W^T | Q | K | A | DEC, contiguous: what every pass-2 CTA of the head copies
 __host__ __device__ constexpr size_t slot_head_bytes(int C) { return slot_dec_off(C) + (size_t)12 * C; }
 __host__ __device__ constexpr size_t slot_u_off(int C) { return slot_head_bytes(C); }
 __host__ __device__ constexpr size_t slot_bytes(int C) {
