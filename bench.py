@@ -328,7 +328,7 @@ def bench_decode(torch, gdn, gi, device, pk, args):
             "us_per_step_l2_resident": round(times["resident"] * 1e3, 3), "gpu_launches": steps}
 
 
-SCHEDULES = (("two_pass", 1), ("single_pass", 2))
+SCHEDULES = (("two_pass", 1), ("single_pass", 2), ("tensor_memory", 3))  # the last: C = 64 only
 
 
 def bench_chunked_schedules(torch, gdn, d, wl, chunk, fn, op, n, flush):
@@ -337,6 +337,8 @@ def bench_chunked_schedules(torch, gdn, d, wl, chunk, fn, op, n, flush):
     o = torch.empty_like(d["v"])
     res = {}
     for name, algo in SCHEDULES:
+        if algo == 3 and chunk != 64:
+            continue
         shape = gdn.make_shape(wl.num_seqs, wl.total_tokens, wl.num_k_heads, wl.num_v_heads,
                                chunk=chunk, algo=algo)
         ws = torch.empty(gdn.gdn_workspace_size(shape, op) + 256, dtype=torch.uint8,
@@ -347,8 +349,8 @@ def bench_chunked_schedules(torch, gdn, d, wl, chunk, fn, op, n, flush):
                chunk=chunk, workspace=ws, algo=algo)
 
         res[name] = statistics.mean(timed_steps(torch, step, n, 3, flush))
-    auto = "single_pass" if wl.num_seqs * wl.num_v_heads >= gdn.GDN_SINGLE_PASS_MIN_HEADS \
-        else "two_pass"
+    many = wl.num_seqs * wl.num_v_heads >= gdn.GDN_SINGLE_PASS_MIN_HEADS
+    auto = ("tensor_memory" if chunk == 64 else "single_pass") if many else "two_pass"
     return res, auto
 
 

@@ -23,7 +23,7 @@ GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIAS, GDN_ERR_WORKSPA
     GDN_ERR_CUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_OP_PREFILL, GDN_OP_DECODE, GDN_OP_VERIFY = 0, 1, 2
-GDN_ALGO_AUTO, GDN_ALGO_TWO_PASS, GDN_ALGO_SINGLE_PASS = 0, 1, 2
+GDN_ALGO_AUTO, GDN_ALGO_TWO_PASS, GDN_ALGO_SINGLE_PASS, GDN_ALGO_TENSOR_MEMORY = 0, 1, 2, 3
 GDN_SINGLE_PASS_MIN_HEADS = 128
 
 EXPORTS = ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_block",

@@ -98,6 +98,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   }
   return done != 0;
 }
+// Like mbar_wait, but each try suspends the thread until the phase completes or about
+// 50 us pass, so that waiting warps do not take issue slots from working ones.  Gives up
+// after 2^15 tries (over a second) and returns false.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+  uint32_t done = 0;
+  for (int it = 0; it < (1 << 15) && !done; ++it) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(50000u)
+        : "memory");
+  }
+  return done != 0;
+}
 // Bulk (TMA) copy global -> shared of `bytes` (multiple of 16, both ends 16-byte
 // aligned); completion is counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,

@@ -20,8 +20,12 @@ gdn_status check_shape(const gdn_shape *s, bool needs_chunk) {
   if (s->dk != gdn::kD || s->dv != gdn::kD) return GDN_ERR_UNSUPPORTED;
   if (s->qkv_dtype != GDN_F32 && s->qkv_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if (s->o_fp32 != 0 && s->o_fp32 != 1) return GDN_ERR_INVALID_ARG;
-  if (s->algo != GDN_ALGO_AUTO && s->algo != GDN_ALGO_TWO_PASS && s->algo != GDN_ALGO_SINGLE_PASS)
+  if (s->algo != GDN_ALGO_AUTO && s->algo != GDN_ALGO_TWO_PASS && s->algo != GDN_ALGO_SINGLE_PASS &&
+      s->algo != GDN_ALGO_TENSOR_MEMORY)
     return GDN_ERR_INVALID_ARG;
+  if (s->algo == GDN_ALGO_TENSOR_MEMORY && needs_chunk &&
+      (s->chunk != 64 || s->qkv_dtype != GDN_BF16))
+    return GDN_ERR_UNSUPPORTED;
   if (needs_chunk && s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return GDN_ERR_UNSUPPORTED;
   // grids are sized (sequences x v-heads x 8) in one dimension
   if ((long long)s->num_seqs * s->num_v_heads * 8 > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
@@ -69,7 +73,7 @@ gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_E
 
 // bf16 chunked pass: one CTA per (sequence, v-head) without workspace, or two passes
 bool single_pass(const gdn_shape *s) {
-  if (s->algo == GDN_ALGO_SINGLE_PASS) return true;
+  if (s->algo == GDN_ALGO_SINGLE_PASS || s->algo == GDN_ALGO_TENSOR_MEMORY) return true;
   if (s->algo == GDN_ALGO_TWO_PASS) return false;
   return (long long)s->num_seqs * s->num_v_heads >= GDN_SINGLE_PASS_MIN_HEADS;
 }
@@ -100,7 +104,12 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   p.o = c.o;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s->qkv_dtype == GDN_F32) return cuda_status(gdn::launch_chunk_f32(p, st));
-  if (single_pass(s)) return cuda_status(gdn::launch_chunk_fused(p, st));
+  if (single_pass(s)) {
+    // many heads, 64-token blocks: the tcgen05 schedule unless the mma.sync one was asked for
+    const bool tc = s->algo == GDN_ALGO_TENSOR_MEMORY ||
+                    (s->algo == GDN_ALGO_AUTO && s->chunk == 64);
+    return cuda_status(tc ? gdn::launch_chunk_tc(p, st) : gdn::launch_chunk_fused(p, st));
+  }
   const size_t need = chunked_workspace(s);
   if (need > 0 && (!workspace || workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))

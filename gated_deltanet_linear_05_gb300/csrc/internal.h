@@ -65,6 +65,7 @@ size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk);
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_chunk_bf16(const ChunkParams &p, cudaStream_t stream);
 cudaError_t launch_chunk_fused(const ChunkParams &p, cudaStream_t stream);
+cudaError_t launch_chunk_tc(const ChunkParams &p, cudaStream_t stream);
 cudaError_t launch_chunk_f32(const ChunkParams &p, cudaStream_t stream);
 
 }  // namespace gdn

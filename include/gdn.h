@@ -83,11 +83,21 @@ typedef enum { GDN_OP_PREFILL = 0, GDN_OP_DECODE = 1, GDN_OP_VERIFY = 2 } gdn_op
  *                blocks in order, spread over 8 CTAs per head.  Suits few heads.
  *   SINGLE_PASS  one CTA per (sequence, v-head) builds the operands and walks the
  *                blocks itself; no workspace.  Suits batches of >= ~1 head per SM.
- *   AUTO         SINGLE_PASS when num_seqs * num_v_heads >= GDN_SINGLE_PASS_MIN_HEADS,
- *                else TWO_PASS (a rule of the shape alone, so that
- *                gdn_workspace_size does not depend on the device).
- * Both give results within the same bounds; they are not bit-identical to each other. */
-typedef enum { GDN_ALGO_AUTO = 0, GDN_ALGO_TWO_PASS = 1, GDN_ALGO_SINGLE_PASS = 2 } gdn_algo;
+ *   AUTO         with num_seqs * num_v_heads >= GDN_SINGLE_PASS_MIN_HEADS: TENSOR_MEMORY for
+ *                64-token blocks of bf16 q/k/v, else SINGLE_PASS; with fewer pairs TWO_PASS
+ *                (a rule of the shape alone, so that gdn_workspace_size does not depend on
+ *                the device).
+ *   TENSOR_MEMORY one CTA per (sequence, v-head) on the tcgen05 tensor cores: the whole
+ *                state in tensor memory, every block's operands read once per head, the
+ *                next block's state-free part prepared while the current one runs; no
+ *                workspace.  Block length 64 and bf16 q/k/v only (else GDN_ERR_UNSUPPORTED).
+ * All give results within the same bounds; they are not bit-identical to each other. */
+typedef enum {
+  GDN_ALGO_AUTO = 0,
+  GDN_ALGO_TWO_PASS = 1,
+  GDN_ALGO_SINGLE_PASS = 2,
+  GDN_ALGO_TENSOR_MEMORY = 3
+} gdn_algo;
 #define GDN_SINGLE_PASS_MIN_HEADS 128
 
 typedef struct {

@@ -68,7 +68,14 @@ def test_workspace_size_follows_the_schedule(L):
         assert two > 0 and one == 0
         assert auto == (0 if n * hv >= gdn.GDN_SINGLE_PASS_MIN_HEADS else two)
     with pytest.raises(gdn.GdnError):
-        gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, algo=3), gdn.GDN_OP_PREFILL)
+        gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, algo=4), gdn.GDN_OP_PREFILL)
+    # the tensor-memory schedule: 64-token blocks of bf16 q/k/v only, no workspace
+    assert gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, chunk=64,
+                                                 algo=gdn.GDN_ALGO_TENSOR_MEMORY),
+                                  gdn.GDN_OP_PREFILL) == 0
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, chunk=16,
+                                              algo=gdn.GDN_ALGO_TENSOR_MEMORY), gdn.GDN_OP_PREFILL)
 
 
 # fake, well-aligned device addresses: every call below must fail validation first

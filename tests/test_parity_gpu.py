@@ -20,7 +20,9 @@ pytestmark = pytest.mark.gpu
 
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 # the two kernel schedules of the bf16 chunked pass (f32 q/k/v have one)
-ALGOS = {"two_pass": 1, "single_pass": 2}
+ALGOS = {"two_pass": 1, "single_pass": 2, "tensor_memory": 3}
+# schedules built for every block length (tensor_memory: 64-token blocks only)
+ALGOS_ANY_C = ["two_pass", "single_pass"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -86,6 +88,8 @@ def test_prefill_small_shapes_f32(chunk, lengths, hk, hv):
 @pytest.mark.parametrize("chunk", [16, 32, 64])
 @pytest.mark.parametrize("lengths,hk,hv", SMALL_CASES)
 def test_prefill_small_shapes_bf16(algo, chunk, lengths, hk, hv):
+    if algo not in ALGOS_ANY_C and chunk != 64:
+        pytest.skip("64-token blocks only")
     wl = gi.Workload("small", lengths, hk, hv, chunk=chunk, dtype="bf16", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=len(lengths) + chunk)
     o_ref, s_ref = _oracle(x)
@@ -94,10 +98,11 @@ def test_prefill_small_shapes_bf16(algo, chunk, lengths, hk, hv):
 
 
 @pytest.mark.parametrize("dtype,algo", [("f32", None), ("bf16", "two_pass"),
-                                        ("bf16", "single_pass")])
+                                        ("bf16", "single_pass"), ("bf16", "tensor_memory")])
 def test_prefill_zero_initial_state_and_in_place(dtype, algo):
     kw = {"algo": ALGOS[algo]} if algo else {}
-    wl = gi.Workload("small", [37, 90], 2, 2, chunk=32, dtype=dtype, s0_scale=0.1)
+    chunk = 32 if algo in (None, *ALGOS_ANY_C) else 64
+    wl = gi.Workload("small", [37, 90], 2, 2, chunk=chunk, dtype=dtype, s0_scale=0.1)
     x = gi.make_inputs(wl, seed=7)
     o_ref, s_ref = _oracle(x)
     _run_and_check(x, wl, o_ref, s_ref, "in place", inplace=True, **kw)
@@ -135,6 +140,12 @@ def test_many_heads_take_the_single_pass_schedule_by_default():
     o_a, s_a, _ = gpu_prefill(x, wl, o_fp32=True)
     o_1, s_1, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS["single_pass"])
     assert np.array_equal(o_a, o_1) and np.array_equal(s_a, s_1)
+    # 64-token blocks: the tensor-memory schedule
+    wl64 = gi.Workload("many", [5, 40, 17, 64, 130] * 8, 2, 4, chunk=64, dtype="bf16", s0_scale=0.1)
+    x64 = gi.make_inputs(wl64, seed=22)
+    o_a, s_a, _ = gpu_prefill(x64, wl64, o_fp32=True)
+    o_t, s_t, _ = gpu_prefill(x64, wl64, o_fp32=True, algo=ALGOS["tensor_memory"])
+    assert np.array_equal(o_a, o_t) and np.array_equal(s_a, s_t)
 
 
 @pytest.mark.slow
@@ -154,7 +165,7 @@ def test_varlen_N8_Hk16_Hv32_sampled(algo):
 
 # ------------------------------------------------------------------ verify
 
-@pytest.mark.parametrize("algo", list(ALGOS))
+@pytest.mark.parametrize("algo", ALGOS_ANY_C)
 def test_verify_B128_H32_T16_full(algo):
     import torch
     wl = gi.verify_b128_h32()
@@ -259,19 +270,23 @@ def test_chunked_matches_gpu_decode_loop(dtype):
 
 @pytest.mark.parametrize("algo", list(ALGOS))
 def test_chunk16_matches_chunk64_bf16(algo):
+    """The block length changes only the rounding: C = 64 under `algo` against C = 16
+    (two-pass for the schedules built for 64-token blocks only)."""
     wl = gi.Workload("c", [300, 77], 2, 2, dtype="bf16", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=4)
-    o16, s16, _ = gpu_prefill(x, wl, chunk=16, o_fp32=True, algo=ALGOS[algo])
+    a16 = algo if algo in ALGOS_ANY_C else "two_pass"
+    o16, s16, _ = gpu_prefill(x, wl, chunk=16, o_fp32=True, algo=ALGOS[a16])
     o64, s64, _ = gpu_prefill(x, wl, chunk=64, o_fp32=True, algo=ALGOS[algo])
     _check(o16, s16, o64, s64, "bf16", "C16 vs C64")
 
 
-def test_two_schedules_agree_bf16():
+@pytest.mark.parametrize("algo", ["single_pass", "tensor_memory"])
+def test_schedules_agree_bf16(algo):
     wl = gi.Workload("c", [300, 77, 1], 2, 4, dtype="bf16", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=5)
     o1, s1, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS["two_pass"])
-    o2, s2, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS["single_pass"])
-    _check(o2, s2, o1, s1, "bf16", "single vs two pass")
+    o2, s2, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS[algo])
+    _check(o2, s2, o1, s1, "bf16", "%s vs two pass" % algo)
 
 
 @pytest.mark.parametrize("algo", list(ALGOS))
@@ -296,6 +311,8 @@ def test_varlen_packed_matches_separate_runs_bf16(algo):
 @pytest.mark.parametrize("chunk", [16, 32, 64])
 def test_repeated_runs_are_bit_identical(chunk, algo):
     """Races between warps or CTAs show up as run-to-run differences."""
+    if algo not in ALGOS_ANY_C and chunk != 64:
+        pytest.skip("64-token blocks only")
     wl = gi.Workload("det", [40, 15, 130], 1, 2, chunk=chunk, dtype="bf16", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=12)
     o0, s0, _ = gpu_prefill(x, wl, o_fp32=True, algo=ALGOS[algo])
