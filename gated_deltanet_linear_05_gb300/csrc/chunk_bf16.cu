@@ -213,45 +213,82 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
 
     // ---- decay masks.  N = beta_t e^(G_t - G_j) k_t.k_j (j < t): fp32 for the diagonal
     //      blocks, -N in fp16 below them.  A = e^(G_t - G_j) q_t.k_j (j <= t): fp16 to the slot.
+    {
+      // this warp's tiles, their gates and decays read first (registers), then the masked
+      // values, then the stores -- so that no gate read waits behind a store
+      int tmt[3], tnp[3];
+      bool has[3];
 #pragma unroll
-    for (int u = 0; u < 3; ++u) {
-      int mt, np;
-      if (u < n0) {
-        mt = mt0;
-        np = np0 + u;
-      } else if (u == 2 && mt1 >= 0) {
-        mt = mt1;
-        np = 0;
-      } else {
-        continue;
+      for (int u = 0; u < 3; ++u) {
+        has[u] = u < n0 || (u == 2 && mt1 >= 0);
+        tmt[u] = u < n0 ? mt0 : mt1;
+        tnp[u] = u < n0 ? np0 + u : 0;
       }
+      float xv[3][2][2][2];  // [tile][half][row half][pair element]
 #pragma unroll
-      for (int half = 0; half < 2; ++half)
+      for (int u = 0; u < 3; ++u) {
+        if (!has[u]) continue;
+        float gt[2], bt[2], gj[2][2];
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
-          const int t = 16 * mt + gid + 8 * hr, j = 16 * np + 8 * half + 2 * tig;
-          const float gt = sm.G[t];
-          const float d0 = __expf(gt - sm.G[j]), d1 = __expf(gt - sm.G[j + 1]);
-          const float v0 = ga[2 * u + half][2 * hr], v1 = ga[2 * u + half][2 * hr + 1];
-          if (prod == 0) {
-            const float bt = sm.B[t];
-            const float x0 = (j < t) ? bt * d0 * v0 : 0.f, x1 = (j + 1 < t) ? bt * d1 * v1 : 0.f;
-            if (mt == np) {
-              sm.Nd[mt][t - 16 * mt][j - 16 * np] = x0;
-              sm.Nd[mt][t - 16 * mt][j + 1 - 16 * np] = x1;
-            } else {
-              *reinterpret_cast<uint32_t *>(sm.N16 + t * RC + 2 * j) = pack_f16(-x0, -x1);
-            }
-          } else {
-            *reinterpret_cast<uint32_t *>(a_out + t * RC + 2 * j) =
-                pack_f16((j <= t) ? d0 * v0 : 0.f, (j + 1 <= t) ? d1 * v1 : 0.f);
-          }
+          gt[hr] = sm.G[16 * tmt[u] + gid + 8 * hr];
+          bt[hr] = sm.B[16 * tmt[u] + gid + 8 * hr];
         }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          gj[half][0] = sm.G[16 * tnp[u] + 8 * half + 2 * tig];
+          gj[half][1] = sm.G[16 * tnp[u] + 8 * half + 2 * tig + 1];
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int t = 16 * tmt[u] + gid + 8 * hr, j = 16 * tnp[u] + 8 * half + 2 * tig;
+            const float v0 = ga[2 * u + half][2 * hr], v1 = ga[2 * u + half][2 * hr + 1];
+            const float d0 = __expf(gt[hr] - gj[half][0]), d1 = __expf(gt[hr] - gj[half][1]);
+            if (prod == 0) {
+              xv[u][half][hr][0] = (j < t) ? bt[hr] * d0 * v0 : 0.f;
+              xv[u][half][hr][1] = (j + 1 < t) ? bt[hr] * d1 * v1 : 0.f;
+            } else {
+              xv[u][half][hr][0] = (j <= t) ? d0 * v0 : 0.f;
+              xv[u][half][hr][1] = (j + 1 <= t) ? d1 * v1 : 0.f;
+            }
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        if (!has[u]) continue;
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int t = 16 * tmt[u] + gid + 8 * hr, j = 16 * tnp[u] + 8 * half + 2 * tig;
+            const float x0 = xv[u][half][hr][0], x1 = xv[u][half][hr][1];
+            if (prod == 0) {
+              if (tmt[u] == tnp[u]) {
+                sm.Nd[tmt[u]][t - 16 * tmt[u]][j - 16 * tnp[u]] = x0;
+                sm.Nd[tmt[u]][t - 16 * tmt[u]][j + 1 - 16 * tnp[u]] = x1;
+              } else {
+                *reinterpret_cast<uint32_t *>(sm.N16 + t * RC + 2 * j) = pack_f16(-x0, -x1);
+              }
+            } else {
+              *reinterpret_cast<uint32_t *>(a_out + t * RC + 2 * j) = pack_f16(x0, x1);
+            }
+          }
+      }
     }
-    // the A tile's upper 16x16 blocks (never computed) are zero
-    for (int e = tid; e < C * C / 2; e += NT) {
-      const int t = e / (C / 2), j = 2 * (e % (C / 2));
-      if ((j >> 4) > (t >> 4)) *reinterpret_cast<uint32_t *>(a_out + t * RC + 2 * j) = 0u;
+    // the A tile's upper 16x16 blocks (never computed) are zero: MT (MT - 1) / 2 tiles of
+    // 16 rows x two 16-byte halves
+    for (int e = tid; e < 16 * MT * (MT - 1); e += NT) {
+      const int tile = e >> 5, row = (e >> 1) & 15, hh = e & 1;
+      int mt = 0, np = 1, cnt = tile;  // tile -> (mt, np > mt), row-major over the upper part
+      while (cnt >= MT - 1 - mt) {
+        cnt -= MT - 1 - mt;
+        ++mt;
+      }
+      np = mt + 1 + cnt;
+      *reinterpret_cast<uint4 *>(a_out + (16 * mt + row) * RC + 2 * (16 * np + 8 * hh)) =
+          make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
 
@@ -278,12 +315,12 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
       }
     } else {
       const int t2 = tid - C, n2 = NT - C;
-      for (int e = t2; e < C * 64; e += n2) {  // 64 packed pairs per 128-element row
-        const int r = e >> 6, cp = e & 63;
-        reinterpret_cast<uint32_t *>(k_out + r * kP128)[cp] =
-            bf16x2_to_f16x2(reinterpret_cast<const uint32_t *>(sm.K + r * kP128)[cp]);
-        reinterpret_cast<uint32_t *>(q_out + r * kP128)[cp] =
-            bf16x2_to_f16x2(reinterpret_cast<const uint32_t *>(sm.Q + r * kP128)[cp]);
+      for (int e = t2; e < 2 * C * 16; e += n2) {  // 16 granules of 8 elements per row
+        const int which = e / (C * 16), r = (e >> 4) & (C - 1), gq = e & 15;
+        const uint4 x = *reinterpret_cast<const uint4 *>((which ? sm.Q : sm.K) + r * kP128 + 16 * gq);
+        *reinterpret_cast<uint4 *>((which ? q_out : k_out) + r * kP128 + 16 * gq) =
+            make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
+                       bf16x2_to_f16x2(x.w));
       }
       for (int t = t2; t < C; t += n2) {
         dec_out[t] = sm.G[t];
@@ -305,19 +342,33 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
       uint32_t Xf[MT][2][4];  // fp16 A fragments of the solved blocks X_j^T
 #pragma unroll
       for (int i = 0; i < MT; ++i) {
+        // R_i^T (cols x tokens) straight in the accumulator layout: ldmatrix.trans of the
+        // bf16 rows gives lane (gid, tig) the pair (t = 2tig, 2tig + 1; col = gid)
         float acc[2][2][4];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        {
+          float sc[2][2];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int t = 16 * i + 8 * nt + 2 * tig + (e & 1);
-              const int col = c0 + 16 * mt + gid + 8 * (e >> 1);
-              const float sc = kind ? sm.B[t] : sm.B[t] * sm.EG[t];
-              acc[mt][nt][e] =
-                  sc * __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(X + t * kP128 + 2 * col));
+            for (int e = 0; e < 2; ++e) {
+              const int t = 16 * i + 8 * nt + 2 * tig + e;
+              sc[nt][e] = kind ? sm.B[t] : sm.B[t] * sm.EG[t];
             }
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            uint32_t r4[4];  // (nt 0, cols lo), (nt 0, cols hi), (nt 1, lo), (nt 1, hi)
+            ldsm_x4_t(r4, X + (16 * i + (lane & 7) + 8 * (lane >> 4)) * kP128 +
+                              2 * (c0 + 16 * mt + 8 * ((lane >> 3) & 1)));
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int hi = 0; hi < 2; ++hi) {
+                const uint32_t w = r4[2 * nt + hi];
+                acc[mt][nt][2 * hi] = sc[nt][0] * __uint_as_float(w << 16);
+                acc[mt][nt][2 * hi + 1] = sc[nt][1] * __uint_as_float(w & 0xffff0000u);
+              }
+          }
+        }
 #pragma unroll
         for (int j = 0; j < i; ++j) {
           uint32_t b[4];

@@ -334,20 +334,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(ChunkParams p) {
         uint32_t Xf[4][2][4];  // fp16 A fragments of the solved blocks X_j^T
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
+          // R_i^T (cols x tokens) straight in the accumulator layout: ldmatrix.trans of the
+          // bf16 rows gives lane (gid, tig) the pair (t = 2tig, 2tig + 1; col = gid)
           float acc[2][2][4];
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
+          {
+            float sc[2][2];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int t = 16 * i + 8 * nt + 2 * tig + (e & 1);
-                const int col = c0 + 16 * mt + gid + 8 * (e >> 1);
-                const float x = kind
-                    ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm.Vb + t * kP128 + 2 * col))
-                    : __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm.KQ[b] + kq_off(t, col)));
-                acc[mt][nt][e] = (kind ? sm.pB[t] : sm.pB[t] * EG[t]) * x;
+              for (int e = 0; e < 2; ++e) {
+                const int t = 16 * i + 8 * nt + 2 * tig + e;
+                sc[nt][e] = kind ? sm.pB[t] : sm.pB[t] * EG[t];
               }
+            const int tr = 16 * i + (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              const int cr = c0 + 16 * mt + 8 * ((lane >> 3) & 1);
+              uint32_t r4[4];  // (nt 0, cols lo), (nt 0, cols hi), (nt 1, lo), (nt 1, hi)
+              ldsm_x4_t(r4, kind ? sm.Vb + tr * kP128 + 2 * cr : sm.KQ[b] + kq_off(tr, cr));
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi) {
+                  const uint32_t w = r4[2 * nt + hi];
+                  acc[mt][nt][2 * hi] = sc[nt][0] * __uint_as_float(w << 16);
+                  acc[mt][nt][2 * hi + 1] = sc[nt][1] * __uint_as_float(w & 0xffff0000u);
+                }
+            }
+          }
 #pragma unroll
           for (int j = 0; j < i; ++j) {
             uint32_t bb[4];
