@@ -161,6 +161,7 @@ def run_gdn(args):
     import gdn_inputs as gi
     import gated_deltanet_linear_05_gb300 as gdn
     from gated_deltanet_linear_05_gb300 import build as gdn_build
+    from gated_deltanet_linear_05_gb300 import shard as gdn_shard
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -177,13 +178,8 @@ def run_gdn(args):
     def flush(i):
         flush_buf.fill_(i & 0xFF)
 
-    def barrier_max(ms):
-        if world > 1:
-            t = torch.tensor([ms], device=device)
-            dist.barrier()
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-        return ms
+    def barrier_max(ms):  # the slowest rank's time (barrier first); ms itself at N = 1
+        return gdn_shard.max_over_ranks(ms, device=device)
 
     clocks = Clocks(local)
     out = {}
