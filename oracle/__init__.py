@@ -7,7 +7,9 @@ does.  It shares no code with the CUDA library.
 The arithmetic lives in ``gdn_oracle.c`` (plain C, double precision); see
 its header for what each function follows ("Qwen3.5-9B-npu" model card,
 section "How it works": the per-token recurrence, the chunkwise form,
-token_valid padding and the block-doubling triangular inverse).
+token_valid padding and the block-doubling triangular inverse; and the steps
+around the recurrence in the GDN block: the input prologue -- causal conv FIFO,
+SiLU, q/k L2 norm, gates -- and the gated RMSNorm output epilogue).
 """
 from __future__ import annotations
 
@@ -47,6 +49,12 @@ def _load():
         lib.gdn_oracle_chunked.restype = I
         lib.gdn_oracle_tril_inverse.argtypes = [I, P, P, I]
         lib.gdn_oracle_tril_inverse.restype = I
+        D = ctypes.c_double
+        lib.gdn_oracle_prologue.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, D,
+                                            P, P, P, P, P, P]
+        lib.gdn_oracle_prologue.restype = I
+        lib.gdn_oracle_gated_rmsnorm.argtypes = [I, I, P, P, P, D, P]
+        lib.gdn_oracle_gated_rmsnorm.restype = I
         _lib = lib
     return _lib
 
@@ -124,3 +132,55 @@ def tril_inverse(Nm: np.ndarray, method: str = "forward") -> np.ndarray:
     if rc:
         raise RuntimeError("gdn_oracle_tril_inverse failed")
     return X
+
+
+CONV_WIDTH = 4  # the short causal convolution of the input prologue
+
+
+def prologue(q_raw, k_raw, v_raw, a, b, conv_w, A_log, dt_bias, conv_state_in, cu_seqlens,
+             eps: float = 1e-6, conv_width: int = CONV_WIDTH):
+    """Input prologue in float64: causal conv (width W) over the raw q | k | v channels with
+    the per-sequence FIFO state, SiLU, q/k L2 norm, gates.
+
+    Shapes: q_raw, k_raw [T, Hk, dk]; v_raw [T, Hv, dv]; a, b [T, Hv]; conv_w [C, W] with
+    C = 2 Hk dk + Hv dv; A_log, dt_bias [Hv]; conv_state_in [N, C, W - 1] or None;
+    cu_seqlens [N + 1] or None (one token per sequence).
+    Returns q, k, v, g, beta, conv_state_out (float64)."""
+    q_raw, k_raw, v_raw, a, b, conv_w, A_log, dt_bias, csi = map(
+        _f32, (q_raw, k_raw, v_raw, a, b, conv_w, A_log, dt_bias, conv_state_in))
+    T, hk, dk = q_raw.shape
+    _, hv, dv = v_raw.shape
+    C = 2 * hk * dk + hv * dv
+    assert conv_w.shape == (C, conv_width) and a.shape == (T, hv) and b.shape == (T, hv)
+    if cu_seqlens is None:
+        n, cu = T, None
+    else:
+        cu = np.ascontiguousarray(cu_seqlens, np.int32)
+        n = len(cu) - 1
+        assert cu[0] == 0 and cu[-1] == T and np.all(np.diff(cu) >= 0)
+    if csi is not None:
+        assert csi.shape == (n, C, conv_width - 1)
+    q = np.zeros((T, hk, dk)); k = np.zeros((T, hk, dk)); v = np.zeros((T, hv, dv))
+    g = np.zeros((T, hv)); beta = np.zeros((T, hv))
+    cso = np.zeros((n, C, conv_width - 1))
+    rc = _load().gdn_oracle_prologue(n, T, hk, hv, dk, dv, conv_width, _ptr(cu), _ptr(q_raw),
+                                     _ptr(k_raw), _ptr(v_raw), _ptr(a), _ptr(b), _ptr(conv_w),
+                                     _ptr(A_log), _ptr(dt_bias), _ptr(csi), float(eps), _ptr(q),
+                                     _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cso))
+    if rc:
+        raise RuntimeError("gdn_oracle_prologue failed (%d)" % rc)
+    return q, k, v, g, beta, cso
+
+
+def gated_rmsnorm(o, z, weight, eps: float = 1e-6):
+    """Gated RMSNorm of each row of the last axis in float64:
+    o / sqrt(mean(o^2) + eps) * weight * SiLU(z)."""
+    o, z, weight = map(_f32, (o, z, weight))
+    d = o.shape[-1]
+    assert z.shape == o.shape and weight.shape == (d,)
+    y = np.zeros(o.shape, np.float64)
+    rc = _load().gdn_oracle_gated_rmsnorm(int(o.size // d), d, _ptr(o), _ptr(z), _ptr(weight),
+                                          float(eps), _ptr(y))
+    if rc:
+        raise RuntimeError("gdn_oracle_gated_rmsnorm failed")
+    return y

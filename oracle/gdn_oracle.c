@@ -362,3 +362,101 @@ int gdn_oracle_tril_inverse(int n, const double *Nm, double *X, int method) {
   free(tmp);
   return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * The GDN block around the recurrence.  "Qwen3.5-4B — Hexagon NPU (QHexRT) — v81"
+ * model card, introduction: each linear-attention layer is a short causal-conv FIFO +
+ * the recurrent (SSM) state + a gated RMSNorm; "Qwen3.5-0.8B on Dragon Q6A NPU via QNN
+ * EP", main changes: the gates use Softplus; "Qwen3.5-9B-npu", "How it works": the output
+ * only feeds the scale-invariant gated RMSNorm.  The pages give no formulas for these
+ * steps; the readings taken are stated at each function.
+ */
+
+static double silu_d(double u) { return u / (1.0 + exp(-u)); }
+static double softplus_d(double u) { return u > 0.0 ? u + log1p(exp(-u)) : log1p(exp(u)); }
+
+/* Input prologue.  For sequence n (tokens [cu[n], cu[n+1]); cu_seqlens == NULL: token n
+ * alone) and channel c of the concatenated raw projections
+ *   x = [q_raw (hk*dk) | k_raw (hk*dk) | v_raw (hv*dv)]:
+ *   y_t[c] = SiLU( sum_{i=0}^{W-1} w[c][i] * x_{t-(W-1)+i}[c] ),   W = conv_width,
+ * where x_p before the sequence's first token is conv_state_in[n][c][p - bos + W - 1]
+ * (the FIFO of the W-1 raw inputs before the call; zero when conv_state_in is NULL) and
+ * SiLU(u) = u / (1 + e^-u).  The q and k rows are then L2-normalised per (token, head):
+ * y / sqrt(sum y^2 + eps).  Gates per (token, v-head):
+ *   g = -exp(A_log[h]) softplus(a + dt_bias[h]),  beta = 1 / (1 + e^-b),
+ * softplus(u) = log(1 + e^u).  conv_state_out[n][c][j] = x_{eos-(W-1)+j}: the FIFO advanced
+ * by the sequence's tokens.  Returns 0 on success. */
+int gdn_oracle_prologue(int num_seqs, int total_tokens, int hk, int hv, int dk, int dv,
+                        int conv_width, const int32_t *cu_seqlens, const float *q_raw,
+                        const float *k_raw, const float *v_raw, const float *a, const float *b,
+                        const float *conv_w, const float *A_log, const float *dt_bias,
+                        const float *conv_state_in, double eps, double *q, double *k, double *v,
+                        double *g, double *beta, double *conv_state_out) {
+  const int W = conv_width, cq = hk * dk, cv = hv * dv, ch = 2 * cq + cv;
+  if (W < 1 || num_seqs < 0 || total_tokens < 0) return 1;
+  double *y = malloc(sizeof(double) * (size_t)(ch > 0 ? ch : 1));
+  if (!y) return 1;
+  for (int n = 0; n < num_seqs; ++n) {
+    const int bos = cu_seqlens ? cu_seqlens[n] : n, eos = cu_seqlens ? cu_seqlens[n + 1] : n + 1;
+    for (int t = bos; t < eos; ++t) {
+      for (int c = 0; c < ch; ++c) {
+        double acc = 0.0;
+        for (int i = 0; i < W; ++i) {
+          const int p = t - (W - 1) + i;
+          double xv;
+          if (p >= bos) {
+            xv = c < cq ? q_raw[(size_t)p * cq + c]
+               : c < 2 * cq ? k_raw[(size_t)p * cq + (c - cq)] : v_raw[(size_t)p * cv + (c - 2 * cq)];
+          } else {
+            xv = conv_state_in ? conv_state_in[((size_t)n * ch + c) * (W - 1) + (p - bos + W - 1)] : 0.0;
+          }
+          acc += (double)conv_w[(size_t)c * W + i] * xv;
+        }
+        y[c] = silu_d(acc);
+      }
+      for (int hd = 0; hd < 2 * hk; ++hd) {  /* q heads, then k heads */
+        double ss = 0.0;
+        for (int i = 0; i < dk; ++i) ss += y[hd * dk + i] * y[hd * dk + i];
+        const double sc = 1.0 / sqrt(ss + eps);
+        double *dst = hd < hk ? q + ((size_t)t * hk + hd) * dk : k + ((size_t)t * hk + hd - hk) * dk;
+        for (int i = 0; i < dk; ++i) dst[i] = y[hd * dk + i] * sc;
+      }
+      for (int j = 0; j < cv; ++j) v[(size_t)t * cv + j] = y[2 * cq + j];
+      for (int h = 0; h < hv; ++h) {
+        const size_t gi = (size_t)t * hv + h;
+        g[gi] = -exp((double)A_log[h]) * softplus_d((double)a[gi] + (double)dt_bias[h]);
+        beta[gi] = 1.0 / (1.0 + exp(-(double)b[gi]));
+      }
+    }
+    for (int c = 0; c < ch; ++c)
+      for (int j = 0; j < W - 1; ++j) {
+        const int p = eos - (W - 1) + j;
+        double xv;
+        if (p >= bos) {
+          xv = c < cq ? q_raw[(size_t)p * cq + c]
+             : c < 2 * cq ? k_raw[(size_t)p * cq + (c - cq)] : v_raw[(size_t)p * cv + (c - 2 * cq)];
+        } else {
+          xv = conv_state_in ? conv_state_in[((size_t)n * ch + c) * (W - 1) + (p - bos + W - 1)] : 0.0;
+        }
+        conv_state_out[((size_t)n * ch + c) * (W - 1) + j] = xv;
+      }
+  }
+  free(y);
+  return 0;
+}
+
+/* Output epilogue, the gated RMSNorm of each (token, v-head) row of d values:
+ *   y = o / sqrt(mean(o^2) + eps) * weight * SiLU(z),
+ * with one weight vector [d] shared by every head.  Returns 0 on success. */
+int gdn_oracle_gated_rmsnorm(int rows, int d, const float *o, const float *z, const float *weight,
+                             double eps, double *y) {
+  if (rows < 0 || d <= 0) return 1;
+  for (int r = 0; r < rows; ++r) {
+    double ss = 0.0;
+    for (int i = 0; i < d; ++i) ss += (double)o[(size_t)r * d + i] * o[(size_t)r * d + i];
+    const double sc = 1.0 / sqrt(ss / d + eps);
+    for (int i = 0; i < d; ++i)
+      y[(size_t)r * d + i] = o[(size_t)r * d + i] * sc * weight[i] * silu_d(z[(size_t)r * d + i]);
+  }
+  return 0;
+}
