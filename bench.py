@@ -235,6 +235,8 @@ def run_gdn(args):
         out["decode"] = bench_decode(torch, gdn, gi, device, pk, args)
         out["verify"] = bench_verify(torch, gdn, gi, device, pk, args, flush)
         out["varlen"] = bench_varlen(torch, gdn, gi, device, pk, args, flush)
+        out["prologue"] = bench_prologue(torch, gdn, gi, device, pk, args, flush)
+        out["gated_rmsnorm"] = bench_gated_rmsnorm(torch, gdn, gi, device, pk, args, flush)
     clk = clocks.stop()
 
     if rank != 0:
@@ -381,6 +383,74 @@ def bench_varlen(torch, gdn, gi, device, pk, args, flush):
             "roofline": roofline("hbm", byts / (ms * 1e-3) / 1e9, pk["hbm"], "GB/s"),
             "tensor_frac": round(flops / (ms * 1e-3) / 1e12 / pk["bf16"], 4),
             "gpu_launches": n * (1 if auto == "single_pass" else 2)}
+
+
+def block_dev_inputs(x, torch, device):
+    import numpy as np
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    d = {n: t(x[n + "_st"]) for n in ("q_raw", "k_raw", "v_raw", "z", "conv_state0")}
+    for n in ("a", "b", "conv_w", "A_log", "dt_bias", "norm_w", "cu_seqlens"):
+        d[n] = t(x[n])
+    return d
+
+
+def prologue_bytes(T, n, hk, hv, s=2, conv_width=4):
+    """Raw q/k/v read + q/k/v written, a/b read + g/beta written, the conv FIFO read and
+    written, the conv weights read once."""
+    C = (2 * hk + hv) * D
+    return 2 * T * C * s + 4 * T * hv * 4 + 2 * n * (conv_width - 1) * C * s + C * conv_width * 4
+
+
+def bench_prologue(torch, gdn, gi, device, pk, args, flush):
+    """Input prologue on the packed workload (8 sequences, Hk 16, Hv 32) and on the decode
+    batch (32 sequences x 16 heads, one token each, FIFO updated in place)."""
+    res = {}
+    for key, wl, per_token in (("varlen", gi.varlen_8seq_hk16_hv32(), False),
+                               ("decode", gi.decode_b32_h16(), True)):
+        d = block_dev_inputs(gi.make_block_inputs(wl), torch, device)
+        cu = None if per_token else d["cu_seqlens"]
+        outs = [torch.empty_like(d[n]) for n in ("q_raw", "k_raw", "v_raw")]
+        g = torch.empty_like(d["a"])
+        beta = torch.empty_like(d["a"])
+        cs = d["conv_state0"]
+
+        def step():
+            gdn.gdn_input_prologue(d["q_raw"], d["k_raw"], d["v_raw"], d["a"], d["b"],
+                                   d["conv_w"], d["A_log"], d["dt_bias"], cs, cs, cu, 1e-6,
+                                   *outs, g, beta)
+
+        n = max(5, min(args.steps, 50))
+        ms = statistics.mean(timed_steps(torch, step, n, 3, flush))
+        byts = prologue_bytes(wl.total_tokens, wl.num_seqs, wl.num_k_heads, wl.num_v_heads)
+        res[key] = {"workload": wl.name, "us_per_step": round(ms * 1e3, 2),
+                    "tokens_per_s": round(wl.total_tokens / (ms * 1e-3), 1),
+                    "roofline": roofline("hbm", byts / (ms * 1e-3) / 1e9, pk["hbm"], "GB/s"),
+                    "algorithmic_bytes": byts,
+                    "gpu_launches": n * (1 if per_token else 2)}
+    return res
+
+
+def bench_gated_rmsnorm(torch, gdn, gi, device, pk, args, flush):
+    """Gated RMSNorm of the packed workload's output (bf16 o, z and y)."""
+    wl = gi.varlen_8seq_hk16_hv32()
+    d = block_dev_inputs(gi.make_block_inputs(wl), torch, device)
+    o = torch.randn(d["z"].shape, device=device).to(torch.bfloat16)
+    y = torch.empty_like(d["z"])
+
+    def step():
+        gdn.gdn_gated_rmsnorm(o, d["z"], d["norm_w"], 1e-6, y)
+
+    n = max(5, min(args.steps, 50))
+    ms = statistics.mean(timed_steps(torch, step, n, 3, flush))
+    byts = 3 * o.numel() * 2 + D * 4
+    return {"workload": wl.name + "_gated_rmsnorm", "us_per_step": round(ms * 1e3, 2),
+            "rows_per_s": round(o.numel() // D / (ms * 1e-3), 1),
+            "roofline": roofline("hbm", byts / (ms * 1e-3) / 1e9, pk["hbm"], "GB/s"),
+            "algorithmic_bytes": byts, "gpu_launches": n}
 
 
 # ------------------------------------------------------------------ CPU oracle

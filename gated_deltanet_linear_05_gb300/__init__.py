@@ -26,8 +26,11 @@ GDN_OP_PREFILL, GDN_OP_DECODE, GDN_OP_VERIFY = 0, 1, 2
 GDN_ALGO_AUTO, GDN_ALGO_TWO_PASS, GDN_ALGO_SINGLE_PASS, GDN_ALGO_TENSOR_MEMORY = 0, 1, 2, 3
 GDN_SINGLE_PASS_MIN_HEADS = 128
 
+GDN_CONV_WIDTH = 4
+
 EXPORTS = ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_block",
-           "gdn_workspace_size", "gdn_status_string", "gdn_prefill_chunked_noalloc")
+           "gdn_workspace_size", "gdn_status_string", "gdn_prefill_chunked_noalloc",
+           "gdn_input_prologue", "gdn_gated_rmsnorm")
 
 
 class GdnUnavailable(RuntimeError):
@@ -76,6 +79,11 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill_chunked_noalloc.argtypes = [ctypes.POINTER(GdnShape), P, P, P, P, P, P, P,
                                                   P, P, P]
         L.gdn_prefill_chunked_noalloc.restype = ctypes.c_int
+        F = ctypes.c_float
+        L.gdn_input_prologue.argtypes = [ctypes.POINTER(GdnShape)] + [P] * 11 + [F] + [P] * 6
+        L.gdn_input_prologue.restype = ctypes.c_int
+        L.gdn_gated_rmsnorm.argtypes = [ctypes.POINTER(GdnShape), P, P, P, F, P, P]
+        L.gdn_gated_rmsnorm.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -195,3 +203,57 @@ def gdn_decode_step(q, k, v, g, beta, state_in, state_out, cu_seqlens=None, o=No
         o = _torch().empty_like(v)
     return _call("gdn_decode_step", GDN_OP_DECODE, q, k, v, g, beta, state_in, state_out,
                  cu_seqlens, o, 64, None, stream)
+
+
+def gdn_input_prologue(q_raw, k_raw, v_raw, a, b, conv_w, A_log, dt_bias, conv_state_in,
+                       conv_state_out, cu_seqlens=None, eps: float = 1e-6, q=None, k=None, v=None,
+                       g=None, beta=None, stream=None):
+    """The block's input prologue: causal conv (width GDN_CONV_WIDTH) + SiLU over the raw
+    [q | k | v] channels, q/k L2 norm, gates.  q_raw, k_raw [T, Hk, 128]; v_raw
+    [T, Hv, 128] (bf16 or fp32); a, b [T, Hv] fp32; conv_w [C, 4] fp32; A_log, dt_bias
+    [Hv] fp32; conv_state_in / conv_state_out [N, 3, C] in q_raw's dtype (either may be
+    None; they may be the same tensor); cu_seqlens [N+1] int32 or None (one token per
+    sequence).  Returns (q, k, v, g, beta)."""
+    torch = _torch()
+    _check_tensors(q_raw, k_raw, v_raw, a, b, conv_w, A_log, dt_bias, conv_state_in,
+                   conv_state_out, cu_seqlens, q, k, v, g, beta)
+    T, hk, dk = q_raw.shape
+    hv, dv = v_raw.shape[1], v_raw.shape[2]
+    n = T if cu_seqlens is None else cu_seqlens.numel() - 1
+    for cs in (conv_state_in, conv_state_out):
+        if cs is not None and (cs.dtype != q_raw.dtype or
+                               tuple(cs.shape) != (n, GDN_CONV_WIDTH - 1, 2 * hk * dk + hv * dv)):
+            raise ValueError("conv state must be [N, %d, C] in q_raw's dtype" % (GDN_CONV_WIDTH - 1))
+    shape = make_shape(n, T, hk, hv, dk, dv, 64, _dtype_code(q_raw))
+    q = torch.empty_like(q_raw) if q is None else q
+    k = torch.empty_like(k_raw) if k is None else k
+    v = torch.empty_like(v_raw) if v is None else v
+    g = torch.empty(T, hv, dtype=torch.float32, device=q_raw.device) if g is None else g
+    beta = torch.empty(T, hv, dtype=torch.float32, device=q_raw.device) if beta is None else beta
+    st = lib().gdn_input_prologue(ctypes.byref(shape), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw),
+                                  _ptr(a), _ptr(b), _ptr(conv_w), _ptr(A_log), _ptr(dt_bias),
+                                  _ptr(conv_state_in), _ptr(conv_state_out), _ptr(cu_seqlens),
+                                  float(eps), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                  _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_input_prologue")
+    return q, k, v, g, beta
+
+
+def gdn_gated_rmsnorm(o, z, weight, eps: float = 1e-6, y=None, stream=None):
+    """Gated RMSNorm of each (token, v-head) row: o / sqrt(mean(o^2) + eps) * weight * SiLU(z).
+    o [T, Hv, 128] (z's dtype, or fp32 with bf16 z); z [T, Hv, 128]; weight [128] fp32.
+    y (z's dtype) may be o or z itself.  Returns y."""
+    _check_tensors(o, z, weight, y)
+    T, hv, dv = z.shape
+    code = _dtype_code(z)
+    o_fp32 = int(code == GDN_BF16 and _dtype_code(o) == GDN_F32)
+    if code == GDN_F32 and _dtype_code(o) != GDN_F32:
+        raise TypeError("o must be float32 when z is float32")
+    shape = make_shape(0, T, 1, hv, 128, dv, 64, code, o_fp32)
+    y = _torch().empty_like(z) if y is None else y
+    st = lib().gdn_gated_rmsnorm(ctypes.byref(shape), _ptr(o), _ptr(z), _ptr(weight), float(eps),
+                                 _ptr(y), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_gated_rmsnorm")
+    return y

@@ -137,7 +137,7 @@ const char *gdn_status_string(gdn_status status) {
     case GDN_OK: return "GDN_OK";
     case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: null, misaligned or inconsistent argument";
     case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: shape, dtype or block length not built";
-    case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS: state_in and state_out overlap in a way not allowed";
+    case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS: two buffers overlap in a way not allowed";
     case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA call or kernel launch failed";
   }
@@ -206,6 +206,107 @@ gdn_status gdn_decode_step(const gdn_shape *shape, const void *q, const void *k,
   p.cu_seqlens = cu_seqlens;
   p.o = o;
   return cuda_status(gdn::launch_decode(p, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_input_prologue(const gdn_shape *shape, const void *q_raw, const void *k_raw,
+                              const void *v_raw, const float *a, const float *b,
+                              const float *conv_w, const float *A_log, const float *dt_bias,
+                              const void *conv_state_in, void *conv_state_out,
+                              const int32_t *cu_seqlens, float eps, void *q, void *k, void *v,
+                              float *g, float *beta, void *stream) {
+  gdn_status st = check_shape(shape, false);
+  if (st != GDN_OK) return st;
+  const gdn_shape *s = shape;
+  if (!(eps >= 0.f)) return GDN_ERR_INVALID_ARG;  // also rejects NaN
+  if (!cu_seqlens && s->total_tokens != s->num_seqs) return GDN_ERR_INVALID_ARG;
+  const size_t es = s->qkv_dtype == GDN_BF16 ? 2 : 4;
+  const size_t T = (size_t)s->total_tokens;
+  const size_t qk_bytes = T * s->num_k_heads * s->dk * es, v_bytes = T * s->num_v_heads * s->dv * es;
+  const size_t C = (size_t)(2 * s->num_k_heads * s->dk + s->num_v_heads * s->dv);
+  if (T > 0) {
+    const void *need[] = {q_raw, k_raw, v_raw, a, b, q, k, v, g, beta};
+    for (const void *ptr : need)
+      if (!ptr || !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+    if (!conv_w || !aligned16(conv_w) || !A_log || !dt_bias) return GDN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A_log) & 3u) || (reinterpret_cast<uintptr_t>(dt_bias) & 3u))
+      return GDN_ERR_INVALID_ARG;
+    // the outputs q, k, v must not overlap the raw inputs (other warps read rows a
+    // warp may already have written)
+    const void *ins[] = {q_raw, k_raw, v_raw};
+    const size_t in_n[] = {qk_bytes, qk_bytes, v_bytes};
+    const void *outs[] = {q, k, v};
+    const size_t out_n[] = {qk_bytes, qk_bytes, v_bytes};
+    for (int i = 0; i < 3; ++i)
+      for (int j = 0; j < 3; ++j) {
+        const uintptr_t x = reinterpret_cast<uintptr_t>(ins[i]), y = reinterpret_cast<uintptr_t>(outs[j]);
+        if (x < y + out_n[j] && y < x + in_n[i]) return GDN_ERR_ALIAS;
+      }
+  }
+  if (s->num_seqs > 0) {
+    if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return GDN_ERR_INVALID_ARG;
+    if ((conv_state_in && !aligned16(conv_state_in)) || (conv_state_out && !aligned16(conv_state_out)))
+      return GDN_ERR_INVALID_ARG;
+    const size_t cs_bytes = (size_t)s->num_seqs * (GDN_CONV_WIDTH - 1) * C * es;
+    if (conv_state_in && conv_state_out && partial_overlap(conv_state_in, conv_state_out, cs_bytes))
+      return GDN_ERR_ALIAS;
+  }
+  if (s->num_seqs == 0) return GDN_OK;
+  gdn::PrologueParams p{};
+  p.num_seqs = s->num_seqs;
+  p.total_tokens = s->total_tokens;
+  p.hk = s->num_k_heads;
+  p.hv = s->num_v_heads;
+  p.dtype = s->qkv_dtype;
+  p.eps = eps;
+  p.q_raw = q_raw;
+  p.k_raw = k_raw;
+  p.v_raw = v_raw;
+  p.a = a;
+  p.b = b;
+  p.conv_w = conv_w;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.conv_state_in = conv_state_in;
+  p.conv_state_out = conv_state_out;
+  p.cu_seqlens = cu_seqlens;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.g = g;
+  p.beta = beta;
+  return cuda_status(gdn::launch_prologue(p, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_gated_rmsnorm(const gdn_shape *shape, const void *o, const void *z,
+                             const float *weight, float eps, void *y, void *stream) {
+  gdn_status st = check_shape(shape, false);
+  if (st != GDN_OK) return st;
+  const gdn_shape *s = shape;
+  if (!(eps >= 0.f)) return GDN_ERR_INVALID_ARG;
+  const long long rows = (long long)s->total_tokens * s->num_v_heads;
+  if (rows == 0) return GDN_OK;
+  if (!o || !z || !weight || !y || !aligned16(o) || !aligned16(z) || !aligned16(weight) ||
+      !aligned16(y))
+    return GDN_ERR_INVALID_ARG;
+  const size_t es = s->qkv_dtype == GDN_BF16 ? 2 : 4;
+  const size_t eo = s->o_fp32 ? 4 : es;
+  const size_t ny = (size_t)rows * s->dv * es;
+  const size_t no = (size_t)rows * s->dv * eo;
+  const uintptr_t yo = reinterpret_cast<uintptr_t>(y), oo = reinterpret_cast<uintptr_t>(o),
+                  zo = reinterpret_cast<uintptr_t>(z);
+  // in place only onto a buffer of the same element size, exactly
+  if (yo < oo + no && oo < yo + ny && !(yo == oo && eo == es)) return GDN_ERR_ALIAS;
+  if (partial_overlap(y, z, ny)) return GDN_ERR_ALIAS;
+  gdn::NormParams p{};
+  p.rows = rows;
+  p.dtype = s->qkv_dtype;
+  p.o_fp32 = s->o_fp32;
+  p.eps = eps;
+  p.o = o;
+  p.z = z;
+  p.weight = weight;
+  p.y = y;
+  return cuda_status(gdn::launch_gated_rmsnorm(p, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -59,6 +59,36 @@ __host__ __device__ constexpr size_t slot_bytes(int C) {
   return (slot_u_off(C) + (size_t)128 * row_c(C) + 127) / 128 * 128;
 }
 
+// The block's input prologue (block_io.cu): causal conv + SiLU over [q | k | v] raw
+// channels, q/k L2 norm, gates.  conv_state_* are [num_seqs][kConvW - 1][C] in dtype.
+constexpr int kConvW = 4;
+struct PrologueParams {
+  int num_seqs, total_tokens, hk, hv;
+  gdn_dtype dtype;
+  float eps;
+  const void *q_raw, *k_raw, *v_raw;
+  const float *a, *b, *conv_w, *A_log, *dt_bias;
+  const void *conv_state_in;
+  void *conv_state_out;
+  const int32_t *cu_seqlens;  // NULL: one token per sequence
+  void *q, *k, *v;
+  float *g, *beta;
+};
+
+// Gated RMSNorm of rows of 128: y = o / sqrt(mean o^2 + eps) * w * SiLU(z).
+struct NormParams {
+  long long rows;
+  gdn_dtype dtype;  // of z and y (and of o unless o_fp32)
+  int o_fp32;
+  float eps;
+  const void *o, *z;
+  const float *weight;
+  void *y;
+};
+
+cudaError_t launch_prologue(const PrologueParams &p, cudaStream_t stream);
+cudaError_t launch_gated_rmsnorm(const NormParams &p, cudaStream_t stream);
+
 // Workspace bytes of the bf16 chunk path: a 256-byte header (status word) + slots.
 size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk);
 

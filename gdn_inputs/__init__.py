@@ -272,3 +272,42 @@ def make_inputs(wl: Workload, seed: int = 0, step: Optional[int] = None,
         out["state0"] = s0.astype(np.float32).reshape(wl.num_seqs, Hv, dk, dv)
     out["cu_seqlens"] = wl.cu_seqlens()
     return out
+
+
+def make_block_inputs(wl: Workload, seed: int = 0, step: Optional[int] = None,
+                      conv_width: int = 4) -> dict:
+    """Draw the inputs of the block steps around the layer for `wl`: the raw projections
+    before the input prologue and the gate projection after the layer.
+
+    Returns a dict of numpy arrays (storage arrays *_st as in make_inputs):
+      q_raw, k_raw  float32 [T, Hk, dk]  N(0, 1), exactly representable in wl.dtype
+      v_raw         float32 [T, Hv, dv]  N(0, 1)
+      a, b          float32 [T, Hv]      N(0, 1)
+      conv_w        float32 [C, W]       0.5 N(0, 1), C = 2 Hk dk + Hv dv
+      A_log         float32 [Hv]         log A, A uniform in [1, 16]
+      dt_bias       float32 [Hv]         log(e^dt - 1), dt log-uniform in [1e-3, 1e-1]
+      conv_state0   float32 [N, W-1, C]  N(0, 1) (oldest input first), in wl.dtype
+      z             float32 [T, Hv, dv]  N(0, 1), in wl.dtype
+      norm_w        float32 [dv]         1 + 0.1 N(0, 1)
+      cu_seqlens    int32 [N+1]
+    `step` selects a fresh draw of the per-token tensors; the weights and the initial
+    conv state do not depend on it."""
+    T, Hk, Hv, dk, dv = wl.total_tokens, wl.num_k_heads, wl.num_v_heads, wl.dk, wl.dv
+    C = 2 * Hk * dk + Hv * dv
+    sfx = "" if step is None else "/step%d" % step
+    out = {}
+    out["q_raw"], out["q_raw_st"] = round_to(normal(seed, "q_raw" + sfx, T * Hk * dk).reshape(T, Hk, dk), wl.dtype)
+    out["k_raw"], out["k_raw_st"] = round_to(normal(seed, "k_raw" + sfx, T * Hk * dk).reshape(T, Hk, dk), wl.dtype)
+    out["v_raw"], out["v_raw_st"] = round_to(normal(seed, "v_raw" + sfx, T * Hv * dv).reshape(T, Hv, dv), wl.dtype)
+    out["a"] = normal(seed, "a" + sfx, T * Hv).reshape(T, Hv).astype(np.float32)
+    out["b"] = normal(seed, "b" + sfx, T * Hv).reshape(T, Hv).astype(np.float32)
+    out["conv_w"] = (0.5 * normal(seed, "conv_w", C * conv_width)).reshape(C, conv_width).astype(np.float32)
+    out["A_log"] = np.log(1.0 + 15.0 * uniform(seed, "A", Hv)).astype(np.float32)
+    dt = np.exp(np.log(1e-3) + (np.log(1e-1) - np.log(1e-3)) * uniform(seed, "dt", Hv))
+    out["dt_bias"] = np.log(np.expm1(dt)).astype(np.float32)
+    cs = normal(seed, "conv_state0", wl.num_seqs * (conv_width - 1) * C)
+    out["conv_state0"], out["conv_state0_st"] = round_to(cs.reshape(wl.num_seqs, conv_width - 1, C), wl.dtype)
+    out["z"], out["z_st"] = round_to(normal(seed, "z" + sfx, T * Hv * dv).reshape(T, Hv, dv), wl.dtype)
+    out["norm_w"] = (1.0 + 0.1 * normal(seed, "norm_w", dv)).astype(np.float32)
+    out["cu_seqlens"] = wl.cu_seqlens()
+    return out

@@ -19,6 +19,10 @@
  *   gdn_verify_block     a prompt-lookup draft check from a state snapshot (section
  *                        "New in v2", prompt lookup decoding: the state is snapshotted
  *                        before the check, so the snapshot must stay untouched).
+ * Two more compute the steps of the block right around the layer:
+ *   gdn_input_prologue   causal conv + SiLU, q/k L2 norm and the gates, producing the
+ *                        layer's q, k, v, g, beta from the block's projections;
+ *   gdn_gated_rmsnorm    the gated RMSNorm of the layer output.
  *
  * Conventions shared by every entry point
  * ----------------------------------------
@@ -68,7 +72,7 @@ typedef enum {
   GDN_OK = 0,
   GDN_ERR_INVALID_ARG = 1,  /* null pointer, bad count, misaligned pointer   */
   GDN_ERR_UNSUPPORTED = 2,  /* a shape, dtype or block length not built       */
-  GDN_ERR_ALIAS = 3,        /* state_in / state_out overlap not allowed       */
+  GDN_ERR_ALIAS = 3,        /* two buffers overlap in a way not allowed       */
   GDN_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required     */
   GDN_ERR_CUDA = 5          /* a CUDA call or launch failed                   */
 } gdn_status;
@@ -193,6 +197,73 @@ gdn_status gdn_prefill_chunked_noalloc(const gdn_shape *shape, const void *q, co
                                        const void *v, const float *g, const float *beta,
                                        const float *state_in, float *state_out,
                                        const int32_t *cu_seqlens, void *o, void *stream);
+
+/* Width of the causal convolution built into gdn_input_prologue. */
+#define GDN_CONV_WIDTH 4
+
+/*
+ * The GDN block's input prologue, the step that produces this layer's q, k, v, g and
+ * beta from the block's projections ("Qwen3.5-9B-npu" model card, section "How it
+ * works": a short causal convolution with SiLU over the q, k, v projections,
+ * L2-normalised q and k, a softplus-form decay gate and a sigmoid write strength).
+ *
+ * Channels: the raw projections, concatenated per token as x = [q_raw | k_raw | v_raw]
+ * (C = 2 Hk dk + Hv dv channels, q heads first, then k heads, then v heads).  For each
+ * sequence n, token t and channel c, with W = GDN_CONV_WIDTH:
+ *     y_t[c] = SiLU( sum_{i<W} conv_w[c][i] * x_{t-(W-1)+i}[c] ),  SiLU(u) = u / (1 + e^-u)
+ * where an input before the sequence's first token (bos) is taken from the state FIFO:
+ * x_p = conv_state_in[n][p - bos + W - 1][c] (zero when conv_state_in is NULL).  Then
+ *     q = y_q / sqrt(sum(y_q^2) + eps), k likewise, per (token, k-head) row of dk;
+ *     v = y_v;
+ *     g    = -exp(A_log[h]) * log(1 + exp(a[t][h] + dt_bias[h]))    per (token, v-head);
+ *     beta = 1 / (1 + exp(-b[t][h])).
+ * The outputs are exactly the inputs of gdn_prefill_chunked / gdn_decode_step /
+ * gdn_verify_block (q, k, v rounded to qkv_dtype, round-to-nearest-even for bf16).
+ * conv_state_out[n][j][c] = x_{eos-(W-1)+j}[c]: the FIFO advanced by the sequence's
+ * tokens (for a sequence shorter than W - 1, partly the old FIFO).
+ *
+ * Arguments (device pointers, row-major, contiguous, 16-byte aligned; shape->chunk,
+ * o_fp32 and algo are ignored):
+ *     q_raw, k_raw  [total_tokens, Hk, dk]   qkv_dtype
+ *     v_raw         [total_tokens, Hv, dv]   qkv_dtype
+ *     a, b          [total_tokens, Hv]       float32
+ *     conv_w        [C, W]                   float32 (tap W-1 multiplies the current token)
+ *     A_log, dt_bias [Hv]                    float32 (4-byte alignment suffices)
+ *     conv_state_in, conv_state_out [num_seqs, W - 1, C]  qkv_dtype (oldest input first);
+ *                   conv_state_in may be NULL (zeros), conv_state_out may be NULL (not
+ *                   written); they may be the same buffer (in-place update), any other
+ *                   overlap is GDN_ERR_ALIAS
+ *     cu_seqlens    [num_seqs + 1] int32, or NULL: one token per sequence
+ *                   (total_tokens == num_seqs), the decode step
+ *     eps           >= 0, added to the sum of squares of each q / k row (1e-6 typical)
+ *     q, k, v, g, beta  outputs, shaped as the same-named inputs of gdn_prefill_chunked;
+ *                   none may overlap an input (q, k, v overlapping q_raw, k_raw, v_raw is
+ *                   GDN_ERR_ALIAS; other overlaps give unspecified results).
+ * dk = dv = 128 are built.  Errors, streams and ownership as for the other entry points;
+ * no workspace.  One launch (two with cu_seqlens and conv_state_out).
+ */
+gdn_status gdn_input_prologue(const gdn_shape *shape, const void *q_raw, const void *k_raw,
+                              const void *v_raw, const float *a, const float *b,
+                              const float *conv_w, const float *A_log, const float *dt_bias,
+                              const void *conv_state_in, void *conv_state_out,
+                              const int32_t *cu_seqlens, float eps, void *q, void *k, void *v,
+                              float *g, float *beta, void *stream);
+
+/*
+ * The GDN block's output epilogue: the gated RMSNorm of each (token, v-head) row of the
+ * layer output ("Qwen3.5-9B-npu" model card, section "How it works"):
+ *     y = o / sqrt(mean(o^2) + eps) * weight * SiLU(z),   mean over the dv values of a row,
+ * one weight vector [dv] shared by every head, the norm taken in float32.
+ *     o       [total_tokens, Hv, dv]  qkv_dtype, or float32 when shape->o_fp32
+ *     z       [total_tokens, Hv, dv]  qkv_dtype (the block's gate projection)
+ *     weight  [dv]                    float32
+ *     y       [total_tokens, Hv, dv]  qkv_dtype; may be o or z exactly (in place, when the
+ *                                     dtypes agree), other overlap is GDN_ERR_ALIAS
+ * Device pointers, 16-byte aligned.  Only total_tokens, num_v_heads, dv, qkv_dtype and
+ * o_fp32 of `shape` are read (num_k_heads must still be valid).  One launch.
+ */
+gdn_status gdn_gated_rmsnorm(const gdn_shape *shape, const void *o, const void *z,
+                             const float *weight, float eps, void *y, void *stream);
 
 /* Workspace bytes `op` (a gdn_op) needs for `shape` (0 when none); (size_t)-1 for an
  * invalid shape or op. */

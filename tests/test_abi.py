@@ -135,3 +135,62 @@ def test_empty_batch_is_a_no_op(L):
     for name in ("gdn_prefill_chunked", "gdn_verify_block", "gdn_decode_step"):
         assert _call(L, name, sh, q=None, k=None, v=None, g=None, beta=None, s_in=None,
                      s_out=None, cu=None, o=None) == gdn.GDN_OK
+
+
+def _pro_args(**kw):
+    """gdn_input_prologue arguments at disjoint fake addresses (1 MiB apart)."""
+    names = ["q_raw", "k_raw", "v_raw", "a", "b", "conv_w", "A_log", "dt_bias", "cs_in", "cs_out",
+             "cu", "q", "k", "v", "g", "beta"]
+    args = {n: A + (i << 20) for i, n in enumerate(names)}
+    args.update(kw)
+    return args
+
+
+def _prologue(L, shape, eps=1e-6, **kw):
+    a = _pro_args(**kw)
+    return L.gdn_input_prologue(
+        ctypes.byref(shape) if shape is not None else None, a["q_raw"], a["k_raw"], a["v_raw"],
+        a["a"], a["b"], a["conv_w"], a["A_log"], a["dt_bias"], a["cs_in"], a["cs_out"], a["cu"],
+        eps, a["q"], a["k"], a["v"], a["g"], a["beta"], None)
+
+
+def test_prologue_validation(L):
+    ok = gdn.make_shape(2, 10, 1, 2)
+    assert _prologue(L, None) == gdn.GDN_ERR_INVALID_ARG
+    assert _prologue(L, gdn.make_shape(2, 10, 1, 2, dk=64)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _prologue(L, gdn.make_shape(2, 10, 2, 3)) == gdn.GDN_ERR_INVALID_ARG
+    for name in ("q_raw", "v_raw", "a", "b", "conv_w", "A_log", "dt_bias", "q", "k", "g", "beta"):
+        assert _prologue(L, ok, **{name: None}) == gdn.GDN_ERR_INVALID_ARG, name
+    for name in ("q_raw", "k", "beta", "conv_w", "cs_in", "cs_out"):
+        assert _prologue(L, ok, **{name: A + (1 << 30) + 8}) == gdn.GDN_ERR_INVALID_ARG, name
+    assert _prologue(L, ok, A_log=A + (1 << 30) + 2) == gdn.GDN_ERR_INVALID_ARG
+    assert _prologue(L, ok, cu=A + (1 << 30) + 2) == gdn.GDN_ERR_INVALID_ARG
+    assert _prologue(L, ok, eps=-1.0) == gdn.GDN_ERR_INVALID_ARG
+    assert _prologue(L, ok, eps=float("nan")) == gdn.GDN_ERR_INVALID_ARG
+    # one token per sequence without cu_seqlens
+    assert _prologue(L, ok, cu=None) == gdn.GDN_ERR_INVALID_ARG
+    # outputs overlapping the raw inputs; conv states overlapping partly
+    assert _prologue(L, ok, q=A) == gdn.GDN_ERR_ALIAS
+    assert _prologue(L, ok, v=A + (1 << 20) + 256) == gdn.GDN_ERR_ALIAS   # inside k_raw
+    assert _prologue(L, ok, cs_out=A + (8 << 20) + 16) == gdn.GDN_ERR_ALIAS
+    # an empty batch launches nothing
+    assert _prologue(L, gdn.make_shape(0, 0, 1, 2), q_raw=None, q=None) == gdn.GDN_OK
+
+
+def _norm(L, shape, o=A, z=A + (1 << 24), w=A + (2 << 24), y=A + (3 << 24), eps=1e-6):
+    return L.gdn_gated_rmsnorm(ctypes.byref(shape) if shape is not None else None, o, z, w, eps,
+                               y, None)
+
+
+def test_gated_rmsnorm_validation(L):
+    ok = gdn.make_shape(0, 10, 1, 2)
+    assert _norm(L, None) == gdn.GDN_ERR_INVALID_ARG
+    assert _norm(L, gdn.make_shape(0, 10, 1, 2, dv=64)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _norm(L, ok, o=None) == gdn.GDN_ERR_INVALID_ARG
+    assert _norm(L, ok, w=A + 4) == gdn.GDN_ERR_INVALID_ARG
+    assert _norm(L, ok, eps=-1e-3) == gdn.GDN_ERR_INVALID_ARG
+    assert _norm(L, ok, y=A + 512) == gdn.GDN_ERR_ALIAS                 # partly over o
+    assert _norm(L, ok, y=A + (1 << 24) + 16) == gdn.GDN_ERR_ALIAS      # partly over z
+    # in place over an fp32 o with a bf16 y is not the same element size
+    assert _norm(L, gdn.make_shape(0, 10, 1, 2, o_fp32=1), y=A) == gdn.GDN_ERR_ALIAS
+    assert _norm(L, gdn.make_shape(0, 0, 1, 2), o=None, z=None, w=None, y=None) == gdn.GDN_OK
