@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GDN prefill tokens/s (%TC roofline); decode state GB/s (%HBM peak)"
 D = 128
+EXTRA_ROWS = ("decode", "verify", "varlen", "prologue", "gated_rmsnorm")
 
 
 def parse():
@@ -41,6 +42,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--only", choices=EXTRA_ROWS, action="append",
+                    help="run only these extra rows after the headline (repeatable)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
@@ -232,11 +235,14 @@ def run_gdn(args):
     e2e_ms = barrier_max(statistics.mean(e2e_times))
 
     if not args.no_extra:
-        out["decode"] = bench_decode(torch, gdn, gi, device, pk, args)
-        out["verify"] = bench_verify(torch, gdn, gi, device, pk, args, flush)
-        out["varlen"] = bench_varlen(torch, gdn, gi, device, pk, args, flush)
-        out["prologue"] = bench_prologue(torch, gdn, gi, device, pk, args, flush)
-        out["gated_rmsnorm"] = bench_gated_rmsnorm(torch, gdn, gi, device, pk, args, flush)
+        rows = {"decode": lambda: bench_decode(torch, gdn, gi, device, pk, args),
+                "verify": lambda: bench_verify(torch, gdn, gi, device, pk, args, flush),
+                "varlen": lambda: bench_varlen(torch, gdn, gi, device, pk, args, flush),
+                "prologue": lambda: bench_prologue(torch, gdn, gi, device, pk, args, flush),
+                "gated_rmsnorm": lambda: bench_gated_rmsnorm(torch, gdn, gi, device, pk, args, flush)}
+        for name in EXTRA_ROWS:
+            if not args.only or name in args.only:
+                out[name] = rows[name]()
     clk = clocks.stop()
 
     if rank != 0:

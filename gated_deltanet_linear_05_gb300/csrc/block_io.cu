@@ -1,9 +1,11 @@
-// The steps of the GDN block right before and right after the delta-rule layer
-// ("Qwen3.5-9B-npu" model card, section "How it works": the block's short causal
-// convolution with SiLU on the q, k, v projections, L2-normalised q and k, the
-// softplus-form decay gate and sigmoid write strength; then the gated RMSNorm of the
-// layer output).  Both are streaming, HBM-bound steps: every byte is read once and
-// written once.
+// The steps of the GDN block right before and right after the delta-rule layer: the
+// block's short causal-conv FIFO before the recurrent state and the gated RMSNorm
+// after it ("Qwen3.5-4B — Hexagon NPU (QHexRT) — v81" model card, introduction), gates
+// built with Softplus ("Qwen3.5-0.8B on Dragon Q6A NPU via QNN EP", main changes), and
+// the layer output feeding only the scale-invariant gated RMSNorm ("Qwen3.5-9B-npu"
+// model card, "How it works", fp16 precision of the DeltaNet output).  The pages give
+// no formulas for these steps; the kernels compute the formulas stated in gdn.h.  Both
+// are streaming, HBM-bound steps: every byte is read once and written once.
 //
 // Both kernels are persistent and pipelined per warp: a warp walks units of work with a
 // stride of the whole grid and keeps the inputs of its next units in flight as cp.async

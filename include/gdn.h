@@ -203,9 +203,11 @@ gdn_status gdn_prefill_chunked_noalloc(const gdn_shape *shape, const void *q, co
 
 /*
  * The GDN block's input prologue, the step that produces this layer's q, k, v, g and
- * beta from the block's projections ("Qwen3.5-9B-npu" model card, section "How it
- * works": a short causal convolution with SiLU over the q, k, v projections,
- * L2-normalised q and k, a softplus-form decay gate and a sigmoid write strength).
+ * beta from the block's projections: the short causal-conv FIFO that precedes the
+ * recurrent state ("Qwen3.5-4B — Hexagon NPU (QHexRT) — v81" model card, introduction)
+ * and the Softplus-built gates ("Qwen3.5-0.8B on Dragon Q6A NPU via QNN EP", main
+ * changes).  The pages print no formulas for this step; the ones below (SiLU after the
+ * conv, L2-normalised q and k, the gate forms) are the block's standard definitions.
  *
  * Channels: the raw projections, concatenated per token as x = [q_raw | k_raw | v_raw]
  * (C = 2 Hk dk + Hv dv channels, q heads first, then k heads, then v heads).  For each
@@ -251,7 +253,9 @@ gdn_status gdn_input_prologue(const gdn_shape *shape, const void *q_raw, const v
 
 /*
  * The GDN block's output epilogue: the gated RMSNorm of each (token, v-head) row of the
- * layer output ("Qwen3.5-9B-npu" model card, section "How it works"):
+ * layer output ("Qwen3.5-4B — Hexagon NPU (QHexRT) — v81" model card, introduction;
+ * "Qwen3.5-9B-npu" model card, "How it works": the output feeds only this
+ * scale-invariant norm):
  *     y = o / sqrt(mean(o^2) + eps) * weight * SiLU(z),   mean over the dv values of a row,
  * one weight vector [dv] shared by every head, the norm taken in float32.
  *     o       [total_tokens, Hv, dv]  qkv_dtype, or float32 when shape->o_fp32
