@@ -45,6 +45,8 @@ def _load():
         I = ctypes.c_int
         lib.gdn_oracle_recurrent.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, I, I]
         lib.gdn_oracle_recurrent.restype = I
+        lib.gdn_oracle_recurrent_deltas.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, I]
+        lib.gdn_oracle_recurrent_deltas.restype = I
         lib.gdn_oracle_chunked.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, I, I, I, I]
         lib.gdn_oracle_chunked.restype = I
         lib.gdn_oracle_tril_inverse.argtypes = [I, P, P, I]
@@ -106,6 +108,42 @@ def recurrent(q, k, v, g, beta, state_in, cu_seqlens,
     if rc:
         raise RuntimeError("gdn_oracle_recurrent failed (%d)" % rc)
     return o, s_out
+
+
+def recurrent_deltas(q, k, v, g, beta, state_in, cu_seqlens, threads: Optional[int] = None):
+    """The per-token rule in float64, also returning each token's delta
+    delta_t = beta_t (v_t - S'^T k_t) (S' the decayed state before the write).
+
+    Returns (o [T, Hv, dv], state_out [N, Hv, dk, dv], delta [T, Hv, dv]), float64."""
+    q, k, v, g, beta, s_in, cu, _, o, s_out, (n, hk, hv, dk, dv) = \
+        _prep(q, k, v, g, beta, state_in, cu_seqlens, None)
+    delta = np.zeros_like(o)
+    rc = _load().gdn_oracle_recurrent_deltas(
+        n, hk, hv, dk, dv, _ptr(cu), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s_in),
+        _ptr(o), _ptr(s_out), _ptr(delta), threads or default_threads())
+    if rc:
+        raise RuntimeError("gdn_oracle_recurrent_deltas failed (%d)" % rc)
+    return o, s_out, delta
+
+
+def state_after_prefix(q, k, v, g, beta, state_in, cu_seqlens, prefix_len,
+                       threads: Optional[int] = None):
+    """The state of every (sequence, v-head) after the first prefix_len[n] tokens of
+    sequence n (clamped to its length), by running the per-token rule over those
+    tokens only.  Returns [N, Hv, dk, dv] float64."""
+    cu = np.asarray(cu_seqlens, np.int64)
+    n = len(cu) - 1
+    keep = []
+    lens = []
+    for s in range(n):
+        a = int(min(max(int(prefix_len[s]), 0), cu[s + 1] - cu[s]))
+        keep.extend(range(int(cu[s]), int(cu[s]) + a))
+        lens.append(a)
+    keep = np.asarray(keep, np.int64)
+    cu_p = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    sub = [np.asarray(x)[keep] for x in (q, k, v, g, beta)]
+    _, s_out = recurrent(*sub, state_in, cu_p, threads=threads)
+    return s_out
 
 
 def chunked(q, k, v, g, beta, state_in, cu_seqlens, chunk: int, solve: str = "forward",

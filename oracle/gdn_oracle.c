@@ -41,6 +41,7 @@ typedef struct {
   int solve;             /* 0: forward substitution, 1: block doubling */
   int next;              /* shared work counter */
   int err;
+  double *delta_out;     /* per-token deltas [T, Hv, dv], or NULL */
 } job_t;
 
 static void chain_of(const job_t *J, int idx, int *n, int *h) {
@@ -91,6 +92,7 @@ static void recurrent_chain(const job_t *J, int n, int h, double *S, double *kv,
       kv[j] = acc;
     }
     for (int j = 0; j < dv; ++j) delta[j] = ((double)vt[j] - kv[j]) * b;
+    if (J->delta_out) memcpy(J->delta_out + ((size_t)t * hv + h) * dv, delta, sizeof(double) * dv);
     for (int i = 0; i < dk; ++i)
       for (int j = 0; j < dv; ++j) S[i * dv + j] += (double)kt[i] * delta[j];
     double *ot = J->o + ((size_t)t * hv + h) * dv;
@@ -327,7 +329,21 @@ int gdn_oracle_recurrent(int num_seqs, int hk, int hv, int dk, int dv,
                          const float *state_in, double *o, double *state_out,
                          const int32_t *pairs, int num_pairs, int threads) {
   job_t J = {num_seqs, hk, hv, dk, dv, cu_seqlens, q, k, v, g, beta, state_in, o, state_out,
-             pairs, num_pairs, 0, 0, 0, 0};
+             pairs, num_pairs, 0, 0, 0, 0, NULL};
+  return run(&J, recurrent_worker, threads);
+}
+
+/* The same recurrence, also writing each token's delta
+ *   delta_t = (v_t - S'^T k_t) * beta_t      (S' the decayed state before the write)
+ * to delta_out [T, Hv, dv]: the rows D of the chunkwise form ("How it works": the
+ * per-token deltas), from which the state after any prefix of a block follows. */
+int gdn_oracle_recurrent_deltas(int num_seqs, int hk, int hv, int dk, int dv,
+                                const int32_t *cu_seqlens, const float *q, const float *k,
+                                const float *v, const float *g, const float *beta,
+                                const float *state_in, double *o, double *state_out,
+                                double *delta_out, int threads) {
+  job_t J = {num_seqs, hk, hv, dk, dv, cu_seqlens, q, k, v, g, beta, state_in, o, state_out,
+             NULL, 0, 0, 0, 0, 0, delta_out};
   return run(&J, recurrent_worker, threads);
 }
 
@@ -339,7 +355,7 @@ int gdn_oracle_chunked(int num_seqs, int hk, int hv, int dk, int dv, const int32
                        const int32_t *pairs, int num_pairs, int chunk, int solve, int threads) {
   if (chunk <= 0) return 1;
   job_t J = {num_seqs, hk, hv, dk, dv, cu_seqlens, q, k, v, g, beta, state_in, o, state_out,
-             pairs, num_pairs, chunk, solve, 0, 0};
+             pairs, num_pairs, chunk, solve, 0, 0, NULL};
   return run(&J, chunked_worker, threads);
 }
 
