@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GDN prefill tokens/s (%TC roofline); decode state GB/s (%HBM peak)"
 D = 128
-EXTRA_ROWS = ("decode", "verify", "varlen", "prologue", "gated_rmsnorm")
+EXTRA_ROWS = ("decode", "verify", "varlen", "prologue", "gated_rmsnorm", "accept")
 
 
 def parse():
@@ -239,7 +239,8 @@ def run_gdn(args):
                 "verify": lambda: bench_verify(torch, gdn, gi, device, pk, args, flush),
                 "varlen": lambda: bench_varlen(torch, gdn, gi, device, pk, args, flush),
                 "prologue": lambda: bench_prologue(torch, gdn, gi, device, pk, args, flush),
-                "gated_rmsnorm": lambda: bench_gated_rmsnorm(torch, gdn, gi, device, pk, args, flush)}
+                "gated_rmsnorm": lambda: bench_gated_rmsnorm(torch, gdn, gi, device, pk, args, flush),
+                "accept": lambda: bench_accept(torch, gdn, gi, device, pk, args, flush)}
         for name in EXTRA_ROWS:
             if not args.only or name in args.only:
                 out[name] = rows[name]()
@@ -457,6 +458,42 @@ def bench_gated_rmsnorm(torch, gdn, gi, device, pk, args, flush):
             "rows_per_s": round(o.numel() // D / (ms * 1e-3), 1),
             "roofline": roofline("hbm", byts / (ms * 1e-3) / 1e9, pk["hbm"], "GB/s"),
             "algorithmic_bytes": byts, "gpu_launches": n}
+
+
+def bench_accept(torch, gdn, gi, device, pk, args, flush):
+    """Draft-verify accept step on the verify workload (128 x 32 heads, 16-token drafts):
+    the verify block that captures the per-token deltas, and the rollback of every state
+    to its accepted prefix (accepted lengths spread over 0..16)."""
+    import numpy as np
+    wl = gi.verify_b128_h32()
+    d = dev_inputs(gi.make_inputs(wl), torch, device)
+    s_out = torch.empty_like(d["state0"])
+    o = torch.empty_like(d["v"])
+    delta = torch.empty(d["v"].shape, dtype=torch.float32, device=device)
+    acc = (gi.raw_u64(0, "accept", wl.num_seqs) % np.uint64(17)).astype(np.int32)
+    acc_d = torch.from_numpy(acc).to(device)
+    s_rb = torch.empty_like(d["state0"])
+    n = max(5, min(args.steps, 50))
+
+    def capture():
+        gdn.gdn_verify_block_capture(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"],
+                                     s_out, d["cu"], o, delta, chunk=16)
+
+    def rollback():
+        gdn.gdn_state_rollback(d["k"], d["g"], delta, d["state0"], acc_d, s_rb, d["cu"])
+
+    ms_cap = statistics.mean(timed_steps(torch, capture, n, 3, flush))
+    ms_rb = statistics.mean(timed_steps(torch, rollback, n, 3, flush))
+    pairs = wl.num_seqs * wl.num_v_heads
+    rb_bytes = pairs * 2 * D * D * 4 + int(acc.sum()) * wl.num_v_heads * (2 * D + 4 * D + 4)
+    _, v_bytes = prefill_work(wl.lengths, wl.num_k_heads, wl.num_v_heads, 16)
+    cap_bytes = v_bytes + wl.total_tokens * wl.num_v_heads * D * 4
+    return {"workload": wl.name + "_accept",
+            "capture_us": round(ms_cap * 1e3, 2),
+            "capture_roofline": roofline("hbm", cap_bytes / (ms_cap * 1e-3) / 1e9, pk["hbm"], "GB/s"),
+            "rollback_us": round(ms_rb * 1e3, 2),
+            "rollback_roofline": roofline("hbm", rb_bytes / (ms_rb * 1e-3) / 1e9, pk["hbm"], "GB/s"),
+            "accepted_tokens": int(acc.sum()), "gpu_launches": 2 * n}
 
 
 # ------------------------------------------------------------------ CPU oracle

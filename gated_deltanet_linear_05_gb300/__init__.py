@@ -30,7 +30,8 @@ GDN_CONV_WIDTH = 4
 
 EXPORTS = ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_block",
            "gdn_workspace_size", "gdn_status_string", "gdn_prefill_chunked_noalloc",
-           "gdn_input_prologue", "gdn_gated_rmsnorm")
+           "gdn_input_prologue", "gdn_gated_rmsnorm", "gdn_verify_block_capture",
+           "gdn_state_rollback", "gdn_conv_state_rollback")
 
 
 class GdnUnavailable(RuntimeError):
@@ -84,6 +85,12 @@ def lib() -> ctypes.CDLL:
         L.gdn_input_prologue.restype = ctypes.c_int
         L.gdn_gated_rmsnorm.argtypes = [ctypes.POINTER(GdnShape), P, P, P, F, P, P]
         L.gdn_gated_rmsnorm.restype = ctypes.c_int
+        L.gdn_verify_block_capture.argtypes = [ctypes.POINTER(GdnShape)] + [P] * 11
+        L.gdn_verify_block_capture.restype = ctypes.c_int
+        L.gdn_state_rollback.argtypes = [ctypes.POINTER(GdnShape)] + [P] * 8
+        L.gdn_state_rollback.restype = ctypes.c_int
+        L.gdn_conv_state_rollback.argtypes = [ctypes.POINTER(GdnShape)] + [P] * 8
+        L.gdn_conv_state_rollback.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -257,3 +264,52 @@ def gdn_gated_rmsnorm(o, z, weight, eps: float = 1e-6, y=None, stream=None):
     if st != GDN_OK:
         raise GdnError(st, "gdn_gated_rmsnorm")
     return y
+
+
+def gdn_verify_block_capture(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,
+                             delta=None, chunk: int = 16, stream=None):
+    """Draft-verify block (state_in left unchanged) that also writes each token's delta
+    [T, Hv, 128] fp32.  Returns (o, state_out, delta)."""
+    torch = _torch()
+    if o is None:
+        o = torch.empty_like(v)
+    if delta is None:
+        delta = torch.empty(v.shape, dtype=torch.float32, device=v.device)
+    _check_tensors(q, k, v, g, beta, state_in, state_out, cu_seqlens, o, delta)
+    shape = _shape_of(q, v, o, state_out, cu_seqlens, chunk, GDN_ALGO_AUTO)
+    st = lib().gdn_verify_block_capture(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(beta), _ptr(state_in), _ptr(state_out),
+                                        _ptr(cu_seqlens), _ptr(o), _ptr(delta), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_verify_block_capture")
+    return o, state_out, delta
+
+
+def gdn_state_rollback(k, g, delta, state_in, prefix_len, state_out, cu_seqlens, stream=None):
+    """State after the first prefix_len[n] tokens of each sequence's verified block,
+    from the snapshot state_in and the captured deltas.  state_out may be state_in."""
+    _check_tensors(k, g, delta, state_in, prefix_len, state_out, cu_seqlens)
+    T, hk, dk = k.shape
+    hv = g.shape[1]
+    shape = make_shape(cu_seqlens.numel() - 1, T, hk, hv, dk, 128, 64, _dtype_code(k))
+    st = lib().gdn_state_rollback(ctypes.byref(shape), _ptr(k), _ptr(g), _ptr(delta),
+                                  _ptr(state_in), _ptr(prefix_len), _ptr(state_out),
+                                  _ptr(cu_seqlens), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_state_rollback")
+    return state_out
+
+
+def gdn_conv_state_rollback(q_raw, k_raw, v_raw, conv_state_in, prefix_len, conv_state_out,
+                            cu_seqlens, stream=None):
+    """Conv FIFO after the first prefix_len[n] draft tokens of each sequence."""
+    _check_tensors(q_raw, k_raw, v_raw, conv_state_in, prefix_len, conv_state_out, cu_seqlens)
+    T, hk, dk = q_raw.shape
+    hv, dv = v_raw.shape[1], v_raw.shape[2]
+    shape = make_shape(cu_seqlens.numel() - 1, T, hk, hv, dk, dv, 64, _dtype_code(q_raw))
+    st = lib().gdn_conv_state_rollback(ctypes.byref(shape), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw),
+                                       _ptr(conv_state_in), _ptr(prefix_len),
+                                       _ptr(conv_state_out), _ptr(cu_seqlens), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_conv_state_rollback")
+    return conv_state_out

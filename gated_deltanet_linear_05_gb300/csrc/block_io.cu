@@ -362,7 +362,8 @@ __global__ void __launch_bounds__(kIoThreads, 2) prologue_kernel(PrologueParams 
 }
 
 // FIFO after the call for packed sequences: entry j of sequence n is the raw input
-// eos - 3 + j (a raw row, or the old FIFO's entry when the sequence is shorter than 3).
+// eos - 3 + j (a raw row, or the old FIFO's entry when the sequence is shorter than 3);
+// with prefix_len, eos is the end of the sequence's first prefix_len[n] tokens.
 // One warp per (sequence, head); every lane reads its three entries before writing.
 template <typename T>
 __global__ void __launch_bounds__(kIoThreads) conv_state_kernel(PrologueParams p) {
@@ -375,7 +376,8 @@ __global__ void __launch_bounds__(kIoThreads) conv_state_kernel(PrologueParams p
   const int C = heads * kD, ch = head * kD + lane * 4;
   const int Tt = p.total_tokens;
   const int bos = clampi(p.cu_seqlens[n], 0, Tt);
-  const int eos = clampi(p.cu_seqlens[n + 1], bos, Tt);
+  int eos = clampi(p.cu_seqlens[n + 1], bos, Tt);
+  if (p.prefix_len) eos = bos + clampi(p.prefix_len[n], 0, eos - bos);  // accepted prefix
   const T *src;
   int hh, hidx;
   if (head < p.hk) {
@@ -520,16 +522,19 @@ cudaError_t launch_prologue(const PrologueParams &p, cudaStream_t stream) {
 #undef GDN_PRO
     if (e != cudaSuccess) return e;
   }
-  if (p.cu_seqlens && p.conv_state_out && p.num_seqs > 0) {
-    const long long units = (long long)p.num_seqs * heads;
-    const unsigned blocks = (unsigned)((units + kIoWarps - 1) / kIoWarps);
-    if (p.dtype == GDN_BF16)
-      conv_state_kernel<__nv_bfloat16><<<blocks, kIoThreads, 0, stream>>>(p);
-    else
-      conv_state_kernel<float><<<blocks, kIoThreads, 0, stream>>>(p);
-    return cudaGetLastError();
-  }
+  if (p.cu_seqlens && p.conv_state_out && p.num_seqs > 0) return launch_conv_state(p, stream);
   return cudaSuccess;
+}
+
+cudaError_t launch_conv_state(const PrologueParams &p, cudaStream_t stream) {
+  const long long units = (long long)p.num_seqs * (2 * p.hk + p.hv);
+  if (units == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((units + kIoWarps - 1) / kIoWarps);
+  if (p.dtype == GDN_BF16)
+    conv_state_kernel<__nv_bfloat16><<<blocks, kIoThreads, 0, stream>>>(p);
+  else
+    conv_state_kernel<float><<<blocks, kIoThreads, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gated_rmsnorm(const NormParams &p, cudaStream_t stream) {

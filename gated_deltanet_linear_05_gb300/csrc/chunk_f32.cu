@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(kF32Threads) chunk_f32_kernel(ChunkParams p) {
       for (int i = 0; i < kD; ++i) qs += sm.Q[t][i] * sm.S[i][c];
       for (int j = 0; j <= t; ++j) ad += sm.A[t][j] * sm.R[j][c];
       o[((size_t)(tok0 + t) * p.hv + h) * kD + c0 + c] = sm.EG[t] * qs + ad;
+      if (p.delta) p.delta[((size_t)(tok0 + t) * p.hv + h) * kD + c0 + c] = sm.R[t][c];
     }
     __syncthreads();
 

@@ -448,6 +448,16 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
         }
       }
     }
+    if (p.delta) {  // the block's per-token deltas (fp32, before any rounding)
+#pragma unroll
+      for (int nt = 0; nt < NTC; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 8 * nt + 2 * tig + (e & 1);
+          if (t < L)
+            p.delta[((size_t)(tok0 + t) * p.hv + h) * kD + j0 + gid + 8 * (e >> 1)] = Dc[nt][e];
+        }
+    }
     // O^T = exp(G) R^T + D^T A^T over the causal part
 #pragma unroll
     for (int nt = 0; nt < NTC; ++nt)

@@ -83,9 +83,11 @@ size_t chunked_workspace(const gdn_shape *s) {
   return gdn::chunk_workspace_bytes(s->total_tokens, s->num_seqs, s->num_v_heads, s->chunk);
 }
 
-gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes, void *stream) {
+gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes, void *stream,
+                       float *delta = nullptr) {
   const gdn_shape *s = c.s;
   ChunkParams p{};
+  p.delta = delta;
   p.num_seqs = s->num_seqs;
   p.total_tokens = s->total_tokens;
   p.hk = s->num_k_heads;
@@ -104,6 +106,7 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   p.o = c.o;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s->qkv_dtype == GDN_F32) return cuda_status(gdn::launch_chunk_f32(p, st));
+  if (delta) return cuda_status(gdn::launch_chunk_fused(p, st));  // the capturing schedule
   if (single_pass(s)) {
     // many heads, 64-token blocks: the tcgen05 schedule unless the mma.sync one was asked for
     const bool tc = s->algo == GDN_ALGO_TENSOR_MEMORY ||
@@ -307,6 +310,92 @@ gdn_status gdn_gated_rmsnorm(const gdn_shape *shape, const void *o, const void *
   p.weight = weight;
   p.y = y;
   return cuda_status(gdn::launch_gated_rmsnorm(p, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_verify_block_capture(const gdn_shape *shape, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    const float *state_in, float *state_out,
+                                    const int32_t *cu_seqlens, void *o, float *delta,
+                                    void *stream) {
+  gdn_status st = check_shape(shape, true);
+  if (st != GDN_OK) return st;
+  if (shape->algo != GDN_ALGO_AUTO && shape->algo != GDN_ALGO_SINGLE_PASS) return GDN_ERR_UNSUPPORTED;
+  Common c{shape, q, k, v, g, beta, state_in, state_out, cu_seqlens, o};
+  if ((st = check_buffers(c, true)) != GDN_OK) return st;
+  if (shape->total_tokens > 0 && (!delta || !aligned16(delta))) return GDN_ERR_INVALID_ARG;
+  if (shape->num_seqs == 0) return GDN_OK;
+  if (!state_in) return GDN_ERR_INVALID_ARG;
+  const size_t n = state_bytes(shape);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(state_in), b = reinterpret_cast<uintptr_t>(state_out);
+  if (a < b + n && b < a + n) return GDN_ERR_ALIAS;
+  return run_chunked(c, nullptr, 0, stream, delta);
+}
+
+gdn_status gdn_state_rollback(const gdn_shape *shape, const void *k, const float *g,
+                              const float *delta, const float *state_in,
+                              const int32_t *prefix_len, float *state_out,
+                              const int32_t *cu_seqlens, void *stream) {
+  gdn_status st = check_shape(shape, false);
+  if (st != GDN_OK) return st;
+  const gdn_shape *s = shape;
+  if (s->num_seqs == 0) return GDN_OK;
+  if (!prefix_len || !cu_seqlens || !state_out || !aligned16(state_out) ||
+      (reinterpret_cast<uintptr_t>(prefix_len) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+    return GDN_ERR_INVALID_ARG;
+  if (state_in && !aligned16(state_in)) return GDN_ERR_INVALID_ARG;
+  if (s->total_tokens > 0 && (!k || !g || !delta || !aligned16(k) || !aligned16(g) || !aligned16(delta)))
+    return GDN_ERR_INVALID_ARG;
+  if (state_in && partial_overlap(state_in, state_out, state_bytes(s))) return GDN_ERR_ALIAS;
+  gdn::RollbackParams p{};
+  p.num_seqs = s->num_seqs;
+  p.total_tokens = s->total_tokens;
+  p.hk = s->num_k_heads;
+  p.hv = s->num_v_heads;
+  p.dtype = s->qkv_dtype;
+  p.k = k;
+  p.g = g;
+  p.delta = delta;
+  p.state_in = state_in;
+  p.prefix_len = prefix_len;
+  p.cu_seqlens = cu_seqlens;
+  p.state_out = state_out;
+  return cuda_status(gdn::launch_rollback(p, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_conv_state_rollback(const gdn_shape *shape, const void *q_raw, const void *k_raw,
+                                   const void *v_raw, const void *conv_state_in,
+                                   const int32_t *prefix_len, void *conv_state_out,
+                                   const int32_t *cu_seqlens, void *stream) {
+  gdn_status st = check_shape(shape, false);
+  if (st != GDN_OK) return st;
+  const gdn_shape *s = shape;
+  if (s->num_seqs == 0) return GDN_OK;
+  if (!prefix_len || !cu_seqlens || !conv_state_out || !aligned16(conv_state_out) ||
+      (reinterpret_cast<uintptr_t>(prefix_len) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+    return GDN_ERR_INVALID_ARG;
+  if (conv_state_in && !aligned16(conv_state_in)) return GDN_ERR_INVALID_ARG;
+  if (s->total_tokens > 0 && (!q_raw || !k_raw || !v_raw || !aligned16(q_raw) || !aligned16(k_raw) ||
+                              !aligned16(v_raw)))
+    return GDN_ERR_INVALID_ARG;
+  const size_t es = s->qkv_dtype == GDN_BF16 ? 2 : 4;
+  const size_t C = (size_t)(2 * s->num_k_heads * s->dk + s->num_v_heads * s->dv);
+  if (conv_state_in &&
+      partial_overlap(conv_state_in, conv_state_out, (size_t)s->num_seqs * (GDN_CONV_WIDTH - 1) * C * es))
+    return GDN_ERR_ALIAS;
+  gdn::PrologueParams p{};
+  p.num_seqs = s->num_seqs;
+  p.total_tokens = s->total_tokens;
+  p.hk = s->num_k_heads;
+  p.hv = s->num_v_heads;
+  p.dtype = s->qkv_dtype;
+  p.q_raw = q_raw;
+  p.k_raw = k_raw;
+  p.v_raw = v_raw;
+  p.conv_state_in = conv_state_in;
+  p.conv_state_out = conv_state_out;
+  p.cu_seqlens = cu_seqlens;
+  p.prefix_len = prefix_len;
+  return cuda_status(gdn::launch_conv_state(p, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -29,6 +29,7 @@ struct ChunkParams {
   float *state_out;
   const int32_t *cu_seqlens;
   void *o;
+  float *delta;  // per-token deltas [T, Hv, 128] fp32, or NULL (single-pass and fp32 kernels)
   // Workspace of the two-pass bf16 path (chunk_bf16.cu): one slot per (v-head,
   // block); block c of sequence n uses slot bos_n / C + n + c, which is unique and below
   // nslots = total_tokens / C + num_seqs.  A slot holds the block's operands for pass 2
@@ -73,7 +74,22 @@ struct PrologueParams {
   const int32_t *cu_seqlens;  // NULL: one token per sequence
   void *q, *k, *v;
   float *g, *beta;
+  const int32_t *prefix_len;  // conv_state_kernel only: FIFO after the first prefix_len[n]
+                              // tokens of sequence n instead of after all of them
 };
+
+// State after a prefix of each sequence's block from the captured per-token deltas:
+// S_a = e^{G_a} S_in + sum_{t<a} e^{G_a - G_t} k_t delta_t^T (rollback.cu).
+struct RollbackParams {
+  int num_seqs, total_tokens, hk, hv;
+  gdn_dtype dtype;  // of k
+  const void *k;
+  const float *g, *delta, *state_in;
+  const int32_t *prefix_len, *cu_seqlens;
+  float *state_out;
+};
+cudaError_t launch_rollback(const RollbackParams &p, cudaStream_t stream);
+cudaError_t launch_conv_state(const PrologueParams &p, cudaStream_t stream);
 
 // Gated RMSNorm of rows of 128: y = o / sqrt(mean o^2 + eps) * w * SiLU(z).
 struct NormParams {

@@ -166,6 +166,59 @@ gdn_status gdn_verify_block(const gdn_shape *shape, const void *q, const void *k
                             size_t workspace_bytes, void *stream);
 
 /*
+ * Draft-verify block that also captures each token's delta ("New in v2", prompt lookup
+ * decoding; the deltas are the rows D of the chunkwise form in "How it works"):
+ *     delta_t = beta_t * (v_t - S'^T k_t),   S' the decayed state before token t's write.
+ * Same arguments and results as gdn_verify_block, plus
+ *     delta  [total_tokens, Hv, dv] float32, 16-byte aligned (written for every token).
+ * With the deltas, gdn_state_rollback gives the state after any accepted prefix of the
+ * draft without re-feeding the accepted tokens.  Runs the single-pass schedule (bf16) or
+ * the fp32 kernel; shape->algo must be GDN_ALGO_AUTO or GDN_ALGO_SINGLE_PASS (else
+ * GDN_ERR_UNSUPPORTED).  Needs no workspace.
+ */
+gdn_status gdn_verify_block_capture(const gdn_shape *shape, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    const float *state_in, float *state_out,
+                                    const int32_t *cu_seqlens, void *o, float *delta,
+                                    void *stream);
+
+/*
+ * State after the accepted prefix of each sequence's verified block:
+ *     S_a = exp(G_a) S_in + sum_{t<a} exp(G_a - G_t) k_t delta_t^T,
+ * G_t the inclusive cumsum of g over the sequence's tokens, a = prefix_len[n] clamped to
+ * [0, the sequence's length] -- the chunkwise form's end-of-block state ("How it works")
+ * cut after a tokens, equal to the per-token rule run over those a tokens.
+ *     k          [total_tokens, Hk, dk]   qkv_dtype (the verified block's keys)
+ *     g          [total_tokens, Hv]       float32
+ *     delta      [total_tokens, Hv, dv]   float32, from gdn_verify_block_capture
+ *     state_in   [num_seqs, Hv, dk, dv]   float32, the snapshot the block started from
+ *                                         (NULL: zero)
+ *     prefix_len [num_seqs]               int32, on the device (accepted tokens)
+ *     state_out  [num_seqs, Hv, dk, dv]   float32; may equal state_in exactly (in place),
+ *                                         other overlap is GDN_ERR_ALIAS
+ *     cu_seqlens [num_seqs + 1]           int32, the verified block's
+ * shape->chunk, o_fp32 and algo are ignored.  One launch; reads and writes each state
+ * once.
+ */
+gdn_status gdn_state_rollback(const gdn_shape *shape, const void *k, const float *g,
+                              const float *delta, const float *state_in,
+                              const int32_t *prefix_len, float *state_out,
+                              const int32_t *cu_seqlens, void *stream);
+
+/*
+ * Conv FIFO after the accepted prefix of each sequence's draft: conv_state_out[n][j] is
+ * the raw input at position a - (W-1) + j of sequence n (a = prefix_len[n], clamped to
+ * the sequence's length; positions before the draft come from conv_state_in, the FIFO
+ * the draft's prologue started from).  q_raw, k_raw, v_raw are the draft's raw
+ * projections as given to gdn_input_prologue; conv states [num_seqs, W-1, C] in
+ * qkv_dtype; conv_state_out may equal conv_state_in exactly.  One launch.
+ */
+gdn_status gdn_conv_state_rollback(const gdn_shape *shape, const void *q_raw, const void *k_raw,
+                                   const void *v_raw, const void *conv_state_in,
+                                   const int32_t *prefix_len, void *conv_state_out,
+                                   const int32_t *cu_seqlens, void *stream);
+
+/*
  * Scratch size built into gdn_prefill_chunked_noalloc (64 MiB).
  */
 #define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)

@@ -1,6 +1,8 @@
 """The C-ABI library: it loads, exports every entry point the header declares, and
 rejects bad arguments on the host before launching anything.  No GPU needed: every
-call here fails validation (or is a pure query), so no kernel is ever launched."""
+call here fails validation (or is a pure query), so no kernel is ever launched.  The
+calls pass made-up device addresses, so the module runs only where no GPU is visible:
+a mistake in one of these tests must never reach a kernel launch on a real device."""
 import ctypes
 import os
 import re
@@ -11,6 +13,17 @@ import gated_deltanet_linear_05_gb300 as gdn
 from gated_deltanet_linear_05_gb300 import build as gdn_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _gpu_visible():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+pytestmark = pytest.mark.skipif(_gpu_visible(), reason="fake device addresses: CPU-only checks")
 
 
 @pytest.fixture(scope="module")
@@ -194,3 +207,53 @@ def test_gated_rmsnorm_validation(L):
     # in place over an fp32 o with a bf16 y is not the same element size
     assert _norm(L, gdn.make_shape(0, 10, 1, 2, o_fp32=1), y=A) == gdn.GDN_ERR_ALIAS
     assert _norm(L, gdn.make_shape(0, 0, 1, 2), o=None, z=None, w=None, y=None) == gdn.GDN_OK
+
+
+def test_capture_and_rollback_validation(L):
+    sh = gdn.make_shape(2, 10, 1, 2, chunk=16)
+    cap = L.gdn_verify_block_capture
+    # q, k, v, g, beta, state_in, state_out, cu_seqlens, o (then delta, stream)
+    base = [A, A + (1 << 20), A + (2 << 20), A + (3 << 20), A + (4 << 20), A + (5 << 24),
+            A + (6 << 24), A + (7 << 20), A + (8 << 20)]
+    assert len(base) + 3 == len(cap.argtypes)
+
+    def c(shape, delta=A + (10 << 20), **kw):
+        args = list(base)
+        for i, v in kw.items():
+            args[int(i[1:])] = v
+        return cap(ctypes.byref(shape), *args, delta, None)
+    assert c(sh, delta=None) == gdn.GDN_ERR_INVALID_ARG
+    assert c(sh, delta=A + (10 << 20) + 4) == gdn.GDN_ERR_INVALID_ARG
+    assert c(gdn.make_shape(2, 10, 1, 2, chunk=16, algo=gdn.GDN_ALGO_TWO_PASS)) == gdn.GDN_ERR_UNSUPPORTED
+    assert c(gdn.make_shape(2, 10, 1, 2, chunk=64, algo=gdn.GDN_ALGO_TENSOR_MEMORY)) == gdn.GDN_ERR_UNSUPPORTED
+    assert c(sh, a5=None) == gdn.GDN_ERR_INVALID_ARG                       # no snapshot
+    assert c(sh, a6=A + (5 << 24) + 4096) == gdn.GDN_ERR_ALIAS             # overlaps the snapshot
+    rb = L.gdn_state_rollback
+    # k, g, delta, state_in, prefix_len, state_out, cu_seqlens (then stream)
+    ok = [A, A + (1 << 20), A + (2 << 20), A + (3 << 24), A + (4 << 20), A + (5 << 24), A + (6 << 20)]
+    assert len(ok) + 2 == len(rb.argtypes)
+
+    def r(shape, **kw):
+        args = list(ok)
+        for i, v in kw.items():
+            args[int(i[1:])] = v
+        return rb(ctypes.byref(shape) if shape is not None else None, *args, None)
+    assert r(None) == gdn.GDN_ERR_INVALID_ARG
+    assert r(gdn.make_shape(2, 10, 1, 2, dk=64)) == gdn.GDN_ERR_UNSUPPORTED
+    assert r(sh, a4=None) == gdn.GDN_ERR_INVALID_ARG                       # prefix_len
+    assert r(sh, a6=None) == gdn.GDN_ERR_INVALID_ARG                       # cu_seqlens
+    assert r(sh, a2=A + (2 << 20) + 8) == gdn.GDN_ERR_INVALID_ARG          # delta misaligned
+    assert r(sh, a5=A + (3 << 24) + 1024) == gdn.GDN_ERR_ALIAS             # partial state overlap
+    assert r(gdn.make_shape(0, 0, 1, 2), a0=None, a1=None, a2=None) == gdn.GDN_OK
+    cs = L.gdn_conv_state_rollback
+    assert len(cs.argtypes) == 9
+
+    def cr(shape, **kw):
+        args = [A, A + (1 << 20), A + (2 << 20), A + (3 << 20), A + (4 << 20), A + (5 << 20),
+                A + (6 << 20)]
+        for i, v in kw.items():
+            args[int(i[1:])] = v
+        return cs(ctypes.byref(shape), *args, None)
+    assert cr(sh, a4=None) == gdn.GDN_ERR_INVALID_ARG
+    assert cr(sh, a0=A + 8) == gdn.GDN_ERR_INVALID_ARG
+    assert cr(sh, a5=A + (3 << 20) + 16) == gdn.GDN_ERR_ALIAS
