@@ -233,3 +233,42 @@ def test_block_prologue_layer_epilogue():
     # y is stored in bf16: the bound applies beyond its own rounding
     excess = np.maximum(np.abs(y_np - y_ref) - half_ulp_bf16(y_np), 0.0)
     assert excess.max() / np.sqrt(np.mean(y_ref ** 2)) <= 2e-2
+
+
+def test_prefix_reuse_two_turns_equal_one_pass():
+    """Prefix reuse: turn 2 run from the conv FIFO and state kept after turn 1 gives the
+    outputs and final state of one pass over both turns (against the oracle's one pass)."""
+    import torch
+    import gated_deltanet_linear_05_gb300 as gdn
+    turn1, turn2 = [70, 5, 33], [40, 17, 1]
+    both = [a + b for a, b in zip(turn1, turn2)]
+    wl = gi.Workload("reuse", both, 1, 2)
+    x = gi.make_block_inputs(wl, seed=31)
+    cu = x["cu_seqlens"]
+    idx1 = np.concatenate([np.arange(cu[n], cu[n] + turn1[n]) for n in range(3)])
+    idx2 = np.concatenate([np.arange(cu[n] + turn1[n], cu[n + 1]) for n in range(3)])
+    s0 = (0.1 * gi.normal(5, "s0", 3 * 2 * 128 * 128)).astype(np.float32).reshape(3, 2, 128, 128)
+    w = {n: to_dev(x[n], "f32") for n in ("conv_w", "A_log", "dt_bias")}
+    cs = to_dev(x["conv_state0_st"], "bf16")
+    s = to_dev(s0, "f32")
+    outs = []
+    for idx, lens in ((idx1, turn1), (idx2, turn2)):
+        raw = {n: to_dev(np.ascontiguousarray(x[n + "_st"][idx]), "bf16")
+               for n in ("q_raw", "k_raw", "v_raw")}
+        ab = {n: to_dev(np.ascontiguousarray(x[n][idx]), "f32") for n in ("a", "b")}
+        cu_t = to_dev(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32), "i32")
+        q, k, v, g, beta = gdn.gdn_input_prologue(raw["q_raw"], raw["k_raw"], raw["v_raw"],
+                                                  ab["a"], ab["b"], w["conv_w"], w["A_log"],
+                                                  w["dt_bias"], cs, cs, cu_t)
+        o = torch.empty(v.shape, dtype=torch.float32, device="cuda")
+        gdn.gdn_prefill_chunked(q, k, v, g, beta, s, s, cu_t, o, chunk=64)
+        torch.cuda.synchronize()
+        outs.append(to_np(o))
+    rq, rk, rv, rg, rb, rcs = _oracle_prologue(x, x["conv_state0"], cu)
+    rq, rk, rv = (gi.round_to(a, "bf16")[0] for a in (rq, rk, rv))
+    o_ref, s_ref = oracle.recurrent(rq, rk, rv, rg, rb, s0, cu)
+    assert np.array_equal(to_np(cs), rcs)
+    for got, idx in zip(outs, (idx1, idx2)):
+        ref = o_ref[idx]
+        assert np.max(np.abs(got - ref)) / np.sqrt(np.mean(ref ** 2)) <= 2e-2
+    assert np.max(np.abs(to_np(s) - s_ref)) / np.sqrt(np.mean(s_ref ** 2)) <= 2e-2
