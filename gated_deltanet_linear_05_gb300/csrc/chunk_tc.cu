@@ -39,6 +39,7 @@ constexpr int kTcC = 64;                 // block length of this kernel
 constexpr int kTcThreads = 32 * 13;      // 4 E + 8 P warps + the MMA issuer warp
 constexpr int kTcE = 128, kTcP = 256;    // threads of the E and P groups
 constexpr int kBarE = 1, kBarP = 2;      // named barriers of the groups
+constexpr int kTcLptSeqs = 64;           // longest-first CTA order up to this many sequences
 
 // tensor-memory columns (512 allocated)
 constexpr int kTmS = 0;      // S^T fp32 [128 value cols][128 keys]
@@ -81,7 +82,7 @@ struct TcSmem {
   float dec[2][3][kTcC];                  // G, e^G, e^(G_T - G) by block parity
   float gRaw[2][kTcC], bRaw[2][kTcC];
   float pB[kTcC];                         // beta of the block being prepared
-  alignas(8) uint64_t in_ready, gram_done, gram_free, prep_done, dec_ready[2];
+  alignas(8) uint64_t gram_done, gram_free, prep_done, dec_ready[2];
   alignas(8) uint64_t p1_done, p2_done, p4_done, d_ready, s_ready, r_free, p4_buf[2];
   alignas(8) uint64_t kq_full[2], v_full;  // cp.async completions (one arrive per E thread)
   uint32_t tmem;
@@ -101,8 +102,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(ChunkParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   TcSmem &sm = *reinterpret_cast<TcSmem *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = blockIdx.x / p.hv;
-  const int h = blockIdx.x - n * p.hv;
+  // Longest sequences first: with more (sequence, head) chains than SMs, CTAs start in
+  // index order as SMs free up, so the long chains should not be the last to start.
+  // CTA b takes head b % Hv of the (b / Hv)-th longest sequence (ties by index), for up
+  // to kTcLptSeqs sequences; beyond that, in sequence order.
+  const int rank = blockIdx.x / p.hv;
+  const int h = blockIdx.x - rank * p.hv;
+  int n = rank;
+  if (p.num_seqs <= kTcLptSeqs) {
+    __shared__ int s_pick;
+    if (tid < p.num_seqs) {
+      int bi, ei;
+      seq_range(p.cu_seqlens, tid, p.total_tokens, bi, ei);
+      int r = 0;
+      for (int m = 0; m < p.num_seqs; ++m) {
+        int bm, em;
+        seq_range(p.cu_seqlens, m, p.total_tokens, bm, em);
+        r += (em - bm > ei - bi) || (em - bm == ei - bi && m < tid);
+      }
+      if (r == rank) s_pick = tid;
+    }
+    __syncthreads();
+    n = s_pick;
+  }
   const int kh = h / (p.hv / p.hk);
   const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
@@ -122,7 +144,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(ChunkParams p) {
 
   if (warp == 0) tc::alloc<512>(&sm.tmem);
   if (tid == 32) {
-    mbar_init(&sm.in_ready, 1);
     mbar_init(&sm.gram_done, 1);
     mbar_init(&sm.gram_free, 1);
     mbar_init(&sm.prep_done, 1);
@@ -186,7 +207,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(ChunkParams p) {
       if (ok) ok = mbar_wait_sleep(&sm.kq_full[b], (c >> 1) & 1);  // q, k, gates of block c
       tc::fence_proxy_async();
       bar_sync(kBarP, kTcP);
-      if (pt == 0) mbar_arrive(&sm.in_ready);
 
       // in-block inclusive cumsum of g (padding contributes 0), e^G, e^(G_T - G), beta
       if (pw == 0) {
@@ -563,13 +583,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(ChunkParams p) {
       }
       tc::commit(&sm.gram_done);
     };
-    wait(&sm.in_ready, 0);
+    // The Gram MMA of a block needs only its q and k tiles and a free Gram accumulator,
+    // so it is issued as soon as both hold: one block ahead of the chain, while the prep
+    // warps are still busy with the current block.
+    wait(&sm.kq_full[0], 0);
+    tc::fence_proxy_async();  // the cp.async writes, as seen by the tensor cores
     tc::fence_after();
     gram(0);
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
       const uint32_t sQt = smem_u32(sm.Qt[c & 1]), sK = smem_u32(sm.K16[c & 1]);
       const uint32_t sAt = smem_u32(sm.At[c & 1]);
+      if (c + 1 < nchunks) {
+        wait(&sm.kq_full[(c + 1) & 1], ((c + 1) >> 1) & 1);
+        wait(&sm.gram_free, c & 1);
+        tc::fence_proxy_async();
+        tc::fence_after();
+        gram(c + 1);
+      }
       wait(&sm.prep_done, c & 1);
       wait(&sm.s_ready, c & 1);
       tc::fence_after();
@@ -582,12 +613,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(ChunkParams p) {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         tc::mma_ts(tmem + kTmR, tmem + kTmST + 8 * kk, tc::sdesc(sQt + kk * 2048, 1024, 128), idP3, kk > 0);
-      if (c + 1 < nchunks) {
-        wait(&sm.in_ready, (c + 1) & 1);
-        wait(&sm.gram_free, c & 1);
-        tc::fence_after();
-        gram(c + 1);
-      }
       wait(&sm.d_ready, c & 1);
       tc::fence_after();
 #pragma unroll
