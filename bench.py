@@ -354,6 +354,8 @@ def bench_chunked_schedules(torch, gdn, d, wl, chunk, fn, op, n, flush):
                chunk=chunk, workspace=ws, algo=algo)
 
         res[name] = statistics.mean(timed_steps(torch, step, n, 3, flush))
+        del ws  # the two-pass workspace of the packed workload is ~2 GB: give it back
+        torch.cuda.empty_cache()
     many = wl.num_seqs * wl.num_v_heads >= gdn.GDN_SINGLE_PASS_MIN_HEADS
     auto = ("tensor_memory" if chunk == 64 else "single_pass") if many else "two_pass"
     return res, auto
