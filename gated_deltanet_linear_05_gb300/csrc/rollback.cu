@@ -61,17 +61,6 @@ __global__ void __launch_bounds__(kRbThreads) rollback_kernel(RollbackParams p) 
   __shared__ float s_c[kTile];
   __shared__ float s_ga;
 
-  // the state's loads go out first; pass 1 and the first tile's loads overlap them
-  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD;
-  float4 S[8];
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const int i = s * 16 + warp * 4 + rsub;
-    S[s] = p.state_in
-               ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + col0)
-               : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-
   // pass 1: G_a, the cumsum over the whole prefix
   if (warp == 0) {
     float carry = 0.f;
@@ -84,10 +73,18 @@ __global__ void __launch_bounds__(kRbThreads) rollback_kernel(RollbackParams p) 
   }
   __syncthreads();
   const float ga = s_ga;
+
+  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD;
   const float ega = expf(ga);
+  float4 S[8];
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    S[s].x *= ega; S[s].y *= ega; S[s].z *= ega; S[s].w *= ega;
+    const int i = s * 16 + warp * 4 + rsub;
+    float4 v = p.state_in
+                   ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + col0)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    v.x *= ega; v.y *= ega; v.z *= ega; v.w *= ega;
+    S[s] = v;
   }
 
   // pass 2: the rank-a update, a tile of tokens at a time

@@ -92,6 +92,7 @@ PROLOGUE_CASES = [
     ([1, 2, 3, 5, 40, 0, 130], 2, 4),          # short sequences, an empty one, runs crossing
     ([0, 16, 16, 15, 1, 0], 1, 2),             # boundaries on and off the 16-token runs
     ([300, 257], 4, 8),
+    ([40, 3, 19], 3, 3),                       # odd head count: a q/k pair, a lone last head
 ]
 
 
@@ -120,7 +121,7 @@ def test_prologue_without_states():
 
 
 @pytest.mark.parametrize("inplace", [False, True])
-@pytest.mark.parametrize("n,hk,hv", [(1, 1, 1), (37, 2, 4), (512, 16, 32)])
+@pytest.mark.parametrize("n,hk,hv", [(1, 1, 1), (37, 2, 4), (9, 3, 3), (512, 16, 32)])
 def test_prologue_decode_step(n, hk, hv, inplace):
     """One token per sequence (no cu_seqlens), the FIFO updated in place or not."""
     wl = gi.Workload("pro_dec", [1] * n, hk, hv)
