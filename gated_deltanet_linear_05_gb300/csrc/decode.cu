@@ -22,7 +22,7 @@ constexpr int kDecThreads = 128;
 constexpr int kDecCols = 32;  // value columns per CTA
 
 template <typename T, typename TO>
-__global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, 8) decode_kernel(DecodeParams p) {
   const int quarter = blockIdx.x & 3;
   const int nh = blockIdx.x >> 2;
   const int n = nh / p.hv;
