@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
           for (int hr = 0; hr < 2; ++hr) {
             const int t = 16 * tmt[u] + gid + 8 * hr, j = 16 * tnp[u] + 8 * half + 2 * tig;
             const float v0 = ga[2 * u + half][2 * hr], v1 = ga[2 * u + half][2 * hr + 1];
-            const float d0 = __expf(gt[hr] - gj[half][0]), d1 = __expf(gt[hr] - gj[half][1]);
+            const float d0 = decay_exp(gt[hr] - gj[half][0]), d1 = decay_exp(gt[hr] - gj[half][1]);
             if (prod == 0) {
               xv[u][half][hr][0] = (j < t) ? bt[hr] * d0 * v0 : 0.f;
               xv[u][half][hr][1] = (j + 1 < t) ? bt[hr] * d1 * v1 : 0.f;

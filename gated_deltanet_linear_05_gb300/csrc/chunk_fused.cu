@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
         for (int hr = 0; hr < 2; ++hr) {
           const int t = 16 * mt + gid + 8 * hr, j = 16 * np + 8 * half + 2 * tig;
           const float gt = sm.G[t];
-          const float d0 = __expf(gt - sm.G[j]), d1 = __expf(gt - sm.G[j + 1]);
+          const float d0 = decay_exp(gt - sm.G[j]), d1 = decay_exp(gt - sm.G[j + 1]);
           const float v0 = ga[2 * u + half][2 * hr], v1 = ga[2 * u + half][2 * hr + 1];
           if (prod == 0) {
             const float bt = sm.B[t];

@@ -88,15 +88,6 @@ struct TcSmem {
   uint32_t tmem;
 };
 
-// e^d for the in-block decays (d <= 0 on every entry that is kept): the change-of-base
-// identity e^d = 2^(d log2 e) on the hardware base-2 exponential (PTX ex2.approx.ftz;
-// relative error a few 1e-7 plus |d| 6e-8, results below 2^-126 flushed to zero).
-__device__ __forceinline__ float decay_exp(float d) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(d * 1.4426950408889634f));
-  return r;
-}
-
 // A fragment (16 rows x 16 k) as fp16 from two 16x8 mma.sync accumulator tiles
 __device__ __forceinline__ void acc_to_f16x(const float (&x)[4], const float (&y)[4], uint32_t (&a)[4]) {
   a[0] = pack_f16(x[0], x[1]);

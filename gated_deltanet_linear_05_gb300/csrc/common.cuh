@@ -298,6 +298,16 @@ __device__ __forceinline__ void bar_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
+// e^d by the change-of-base identity e^d = 2^(d log2 e) on the hardware base-2
+// exponential (PTX ex2.approx.ftz): relative error a few 1e-7 plus |d| 6e-8, results
+// below 2^-126 flushed to zero.  Used for the in-block decays and the SiLU gate, where
+// it replaced a measurably slower exponential.
+__device__ __forceinline__ float decay_exp(float d) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(d * 1.4426950408889634f));
+  return r;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
