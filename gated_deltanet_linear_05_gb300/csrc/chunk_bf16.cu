@@ -299,20 +299,10 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
     if (tid < C) {
       const int blk = tid >> 4, cc = tid & 15;
       float x[16];
+      unit_tril_inverse_col(&sm.Nd[blk][0][0], 17, cc, x);
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < r; ++m) {  // x[m] = 0 above the column's diagonal
-          if (m & 1)
-            a1 = fmaf(sm.Nd[blk][r][m], x[m], a1);
-          else
-            a0 = fmaf(sm.Nd[blk][r][m], x[m], a0);
-        }
-        const float val = (r == cc) ? 1.f : (r < cc ? 0.f : -(a0 + a1));
-        x[r] = val;
-        *reinterpret_cast<__half *>(sm.T16[blk] + r * 48 + 2 * cc) = __float2half_rn(val);
-      }
+      for (int r = 0; r < 16; ++r)
+        *reinterpret_cast<__half *>(sm.T16[blk] + r * 48 + 2 * cc) = __float2half_rn(x[r]);
     } else {
       const int t2 = tid - C, n2 = NT - C;
       for (int e = t2; e < 2 * C * 16; e += n2) {  // 16 granules of 8 elements per row

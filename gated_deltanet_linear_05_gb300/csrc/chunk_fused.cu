@@ -288,20 +288,9 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
     if (tid < C) {
       const int base = (tid >> 4) * 16, cc = tid & 15;
       float x[16];
+      unit_tril_inverse_col(&Nm[base][base], LD, cc, x);
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < r; ++m) {
-          if (m & 1)
-            a1 = fmaf(Nm[base + r][base + m], x[m], a1);
-          else
-            a0 = fmaf(Nm[base + r][base + m], x[m], a0);
-        }
-        const float val = (r == cc) ? 1.f : (r < cc ? 0.f : -(a0 + a1));
-        x[r] = val;
-        Tm[base + r][base + cc] = val;
-      }
+      for (int r = 0; r < 16; ++r) Tm[base + r][base + cc] = x[r];
     } else {
       const int t2 = tid - C, n2 = NT - C;
       for (int e = t2; e < C * 64; e += n2) {  // 64 packed pairs per 128-element row

@@ -308,6 +308,25 @@ __device__ __forceinline__ float decay_exp(float d) {
   return r;
 }
 
+// Column cc of (I + N)^-1 for a strictly lower triangular 16 x 16 block N (N(r, m) at
+// N0[r * stride + m]): x[r] = 0 above the diagonal, 1 on it and
+// -sum_{cc <= m < r} N(r, m) x[m] below, by column-oriented forward substitution: each
+// x[m] is pushed into every later row's sum as soon as it is known, so the dependent
+// chain is one fused multiply-add per row.
+__device__ __forceinline__ void unit_tril_inverse_col(const float *N0, int stride, int cc,
+                                                      float (&x)[16]) {
+  float acc[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const float xm = (m < cc) ? 0.f : (m == cc ? 1.f : -acc[m]);
+    x[m] = xm;
+#pragma unroll
+    for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(N0[r * stride + m], xm, acc[r]);
+  }
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
