@@ -86,6 +86,9 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
   const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
   if (blockIdx.x == 0 && tid == 0) *p.err = 0;
+  // pass 2 may be scheduled now (programmatic dependent launch): its CTAs set up on SMs
+  // that pass 1 has left and wait for pass 1's completion before reading any slot
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   int bos, eos;
   seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
@@ -469,6 +472,9 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
     *reinterpret_cast<float4 *>(&sm.S32[i][4 * c4]) = val;
   }
   __syncthreads();
+  // pass 1 complete and its slot writes visible (returns at once without a pending
+  // prerequisite grid)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
   if (warp == kChainWarps + kOutWarps) {
     // ---- producer: stream each block's slot part into the ring
@@ -689,8 +695,19 @@ cudaError_t launch_recur(const ChunkParams &p, long long heads, cudaStream_t str
   cudaError_t err = cudaFuncSetAttribute(recur_kernel<C, TO>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (err != cudaSuccess) return err;
-  recur_kernel<C, TO><<<(unsigned)(heads * (kD / kDVB)), kRecThreads, s2, stream>>>(p);
-  return cudaGetLastError();
+  // launched as a programmatic dependent of pass 1, so that its launch and set-up overlap
+  // the tail of pass 1
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(heads * (kD / kDVB)));
+  cfg.blockDim = dim3(kRecThreads);
+  cfg.dynamicSmemBytes = s2;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, recur_kernel<C, TO>, p);
 }
 
 template <int C>
