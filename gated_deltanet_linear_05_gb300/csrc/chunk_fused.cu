@@ -49,6 +49,9 @@ struct FusedSmem {
   // output staging [8][C][16]
   alignas(16) char NTO[kNTBytes > kOBytes ? kNTBytes : kOBytes];
   float M[32 * 33];
+  // 16-token blocks (the draft-verify size): the whole state staged here, so that it moves
+  // between global and shared memory in 16-byte pieces along its rows
+  alignas(16) float SS[C == 16 ? kD : 1][kD + 4];
   float G[C], EG[C], ED[C], B[C];
   float gRaw[2][C], bRaw[2][C];
 };
@@ -132,17 +135,36 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
     }
   };
   if (nchunks > 0) issue_loads(0, 0);
+  if constexpr (C == 16) {  // the state rides along with block 0's copies
+    if (p.state_in)
+      for (int e = tid; e < kD * kD / 4; e += NT) {
+        const int r = e >> 5, c4 = e & 31;
+        cp_async16(&sm.SS[r][4 * c4], p.state_in + sbase + (size_t)r * kD + 4 * c4, 16);
+      }
+  }
   cp_async_commit();
 
   // S^T[j][i] for j = j0 + gid (+8), i = 8nt + 2tig (+1): 16 accumulator tiles
   float S[16][4];
+  if constexpr (C == 16) {
+    cp_async_wait<0>();
+    __syncthreads();
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt)
+    for (int nt = 0; nt < 16; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = 8 * nt + 2 * tig + (e & 1), j = j0 + gid + 8 * (e >> 1);
-      S[nt][e] = p.state_in ? p.state_in[sbase + (size_t)i * kD + j] : 0.f;
-    }
+      for (int e = 0; e < 4; ++e) {
+        const int i = 8 * nt + 2 * tig + (e & 1), j = j0 + gid + 8 * (e >> 1);
+        S[nt][e] = p.state_in ? sm.SS[i][j] : 0.f;
+      }
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 8 * nt + 2 * tig + (e & 1), j = j0 + gid + 8 * (e >> 1);
+        S[nt][e] = p.state_in ? p.state_in[sbase + (size_t)i * kD + j] : 0.f;
+      }
+  }
 
   // Gram tiles of this warp: warps 0-3 take K K^T, warps 4-7 Q K^T, each a balanced share
   // of the causal 16x16 tiles (mt, np <= mt): np0 .. np0+n0-1 of row mt0, and for one
@@ -505,13 +527,30 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
     }
   }
 
+  if constexpr (C == 16) {  // back through the staging area, 16-byte stores along rows
+    __syncthreads();  // (defensive: nothing else uses the staging area after the start)
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt)
+    for (int nt = 0; nt < 16; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = 8 * nt + 2 * tig + (e & 1), j = j0 + gid + 8 * (e >> 1);
-      p.state_out[sbase + (size_t)i * kD + j] = S[nt][e];
+      for (int e = 0; e < 4; ++e) {
+        const int i = 8 * nt + 2 * tig + (e & 1), j = j0 + gid + 8 * (e >> 1);
+        sm.SS[i][j] = S[nt][e];
+      }
+    __syncthreads();
+    for (int e = tid; e < kD * kD / 4; e += NT) {
+      const int r = e >> 5, c4 = e & 31;
+      *reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)r * kD + 4 * c4) =
+          *reinterpret_cast<const float4 *>(&sm.SS[r][4 * c4]);
     }
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 8 * nt + 2 * tig + (e & 1), j = j0 + gid + 8 * (e >> 1);
+        p.state_out[sbase + (size_t)i * kD + j] = S[nt][e];
+      }
+  }
 }
 
 template <int C, typename TO>
