@@ -11,10 +11,10 @@
 //
 // One CTA of 128 threads per (sequence, v-head, 32 value columns), laid out like the
 // decode step: each thread holds 8 rows x 4 columns of S in registers, so the state is
-// read once and written once with 128-bit accesses.  Tokens go in tiles of 32: warp 0
-// forms the tile's cumsum by a warp scan (the same scan, in the same order, in both
-// passes, so G_a - G_{a-1} is exactly 0), the tile's keys and deltas are staged in
-// shared memory, and every thread adds the tile's rank-32 update to its entries.
+// read once and written once with 128-bit accesses.  Tokens go in tiles of 32 (a draft
+// block is one tile): the tile's keys, deltas and gates are staged in shared memory by
+// cp.async, issued together with the state's loads; warp 0 forms the tile's cumsum by a
+// warp scan, and every thread adds the tile's rank-32 update to its entries.
 #include "common.cuh"
 #include "internal.h"
 
@@ -28,11 +28,9 @@ constexpr int kTile = 32;    // tokens per tile
 
 __device__ __forceinline__ int clampi(int x, int lo, int hi) { return min(max(x, lo), hi); }
 
-// Inclusive scan of g over the tile's tokens [t0, t0 + n) of head h, plus `carry`,
-// by warp 0; lane l gets G at token t0 + l (tokens past n repeat the last value).
-__device__ __forceinline__ float tile_scan(const RollbackParams &p, int h, int t0, int n,
-                                           float carry, int lane) {
-  float x = lane < n ? p.g[(size_t)(t0 + lane) * p.hv + h] : 0.f;
+// Inclusive warp scan of the tile's g values (lane l: token l of the tile, 0 past cnt),
+// plus `carry`; lane l gets G at token l (lanes past cnt repeat the last value).
+__device__ __forceinline__ float warp_scan(float x, float carry, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float y = __shfl_up_sync(0xffffffffu, x, o);
@@ -56,55 +54,89 @@ __global__ void __launch_bounds__(kRbThreads) rollback_kernel(RollbackParams p) 
   seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
   const int a = clampi(p.prefix_len[n], 0, eos - bos);
 
-  __shared__ float s_k[kTile][kD];
-  __shared__ __align__(16) float s_d[kTile][kRbCols];
-  __shared__ float s_c[kTile];
+  __shared__ __align__(16) T s_k[kTile][kD];           // the tile's key rows, as stored
+  __shared__ __align__(16) float s_d[kTile][kRbCols];  // the tile's deltas, this CTA's columns
+  __shared__ float s_g[kTile], s_c[kTile];
   __shared__ float s_ga;
+  const T *k = static_cast<const T *>(p.k);
 
-  // pass 1: G_a, the cumsum over the whole prefix
+  // keys, deltas and gates of tokens bos + t0 .. bos + t0 + cnt - 1, by cp.async
+  auto load_tile = [&](int t0, int cnt) {
+    constexpr int EG = 16 / (int)sizeof(T), KG = kD / EG;  // 16-byte granules of a key row
+    for (int e = tid; e < kTile * KG; e += kRbThreads) {
+      const int t = e / KG, gq = e - t * KG;
+      const bool ok = t < cnt;
+      const size_t tok = (size_t)bos + t0 + (ok ? t : 0);
+      cp_async16(&s_k[t][gq * EG], k + (tok * p.hk + kh) * kD + gq * EG, ok ? 16 : 0);
+    }
+    for (int e = tid; e < kTile * (kRbCols / 4); e += kRbThreads) {
+      const int t = e / (kRbCols / 4), gq = e - t * (kRbCols / 4);
+      const bool ok = t < cnt;
+      const size_t tok = (size_t)bos + t0 + (ok ? t : 0);
+      cp_async16(&s_d[t][gq * 4], p.delta + (tok * p.hv + h) * kD + quarter * kRbCols + gq * 4,
+                 ok ? 16 : 0);
+    }
+    if (tid < kTile) {
+      const bool ok = tid < cnt;
+      cp_async4(&s_g[tid], p.g + ((size_t)bos + t0 + (ok ? tid : 0)) * p.hv + h, ok ? 4 : 0);
+    }
+    cp_async_commit();
+  };
+
+  // the first tile's copies and the state's loads go out together
+  if (a > 0) load_tile(0, min(kTile, a));
+  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD;
+  float4 S[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int i = s * 16 + warp * 4 + rsub;
+    S[s] = p.state_in
+               ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + col0)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  // G_a, the cumsum over the whole prefix: from the staged first tile when the prefix
+  // fits in one tile (a draft block), else scanned tile by tile from global memory; the
+  // same scan, in the same order, gives the G_t of pass 2, so G_a - G_{a-1} is exactly 0
+  cp_async_wait<0>();
+  __syncthreads();
   if (warp == 0) {
     float carry = 0.f;
-    for (int t0 = 0; t0 < a; t0 += kTile) {
-      const int cnt = min(kTile, a - t0);
-      const float G = tile_scan(p, h, bos + t0, cnt, carry, lane);
-      carry = __shfl_sync(0xffffffffu, G, cnt - 1);
+    if (a <= kTile) {
+      const float G = warp_scan(lane < a ? s_g[lane] : 0.f, 0.f, lane);
+      if (a > 0) carry = __shfl_sync(0xffffffffu, G, a - 1);
+    } else {
+      for (int t0 = 0; t0 < a; t0 += kTile) {
+        const int cnt = min(kTile, a - t0);
+        const float x = lane < cnt ? p.g[((size_t)bos + t0 + lane) * p.hv + h] : 0.f;
+        const float G = warp_scan(x, carry, lane);
+        carry = __shfl_sync(0xffffffffu, G, cnt - 1);
+      }
     }
     if (lane == 0) s_ga = carry;
   }
   __syncthreads();
   const float ga = s_ga;
-
-  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD;
   const float ega = expf(ga);
-  float4 S[8];
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    const int i = s * 16 + warp * 4 + rsub;
-    float4 v = p.state_in
-                   ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + col0)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-    v.x *= ega; v.y *= ega; v.z *= ega; v.w *= ega;
-    S[s] = v;
+    S[s].x *= ega; S[s].y *= ega; S[s].z *= ega; S[s].w *= ega;
   }
 
-  // pass 2: the rank-a update, a tile of tokens at a time
-  const T *k = static_cast<const T *>(p.k);
+  // pass 2: the rank-a update, a tile of tokens at a time (the first tile already staged)
   float carry = 0.f;
   for (int t0 = 0; t0 < a; t0 += kTile) {
     const int cnt = min(kTile, a - t0);
+    if (t0 > 0) {
+      __syncthreads();  // the previous tile's shared memory is free
+      load_tile(t0, cnt);
+      cp_async_wait<0>();
+      __syncthreads();
+    }
     if (warp == 0) {
-      const float G = tile_scan(p, h, bos + t0, cnt, carry, lane);
+      const float G = warp_scan(lane < cnt ? s_g[lane] : 0.f, carry, lane);
       s_c[lane] = lane < cnt ? expf(ga - G) : 0.f;
       carry = __shfl_sync(0xffffffffu, G, cnt - 1);
-    }
-    for (int e = tid; e < kTile * kD; e += kRbThreads) {
-      const int t = e / kD, i = e - t * kD;
-      s_k[t][i] = t < cnt ? Elem<T>::load(k + ((size_t)(bos + t0 + t) * p.hk + kh) * kD + i) : 0.f;
-    }
-    for (int e = tid; e < kTile * kRbCols; e += kRbThreads) {
-      const int t = e / kRbCols, j = e - t * kRbCols;
-      s_d[t][j] = t < cnt ? p.delta[((size_t)(bos + t0 + t) * p.hv + h) * kD + quarter * kRbCols + j]
-                          : 0.f;
     }
     __syncthreads();
     for (int t = 0; t < cnt; ++t) {
@@ -113,14 +145,13 @@ __global__ void __launch_bounds__(kRbThreads) rollback_kernel(RollbackParams p) 
       const float dx = c * d.x, dy = c * d.y, dz = c * d.z, dw = c * d.w;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const float ki = s_k[t][s * 16 + warp * 4 + rsub];
+        const float ki = Elem<T>::load(&s_k[t][s * 16 + warp * 4 + rsub]);
         S[s].x = fmaf(ki, dx, S[s].x);
         S[s].y = fmaf(ki, dy, S[s].y);
         S[s].z = fmaf(ki, dz, S[s].z);
         S[s].w = fmaf(ki, dw, S[s].w);
       }
     }
-    __syncthreads();  // the tile's shared memory is rewritten by the next one
   }
 
 #pragma unroll
