@@ -13,7 +13,7 @@ Timing: CUDA events on the launching stream, L2 flushed (a 512 MiB write)
 before every timed step and outside the events; decode rotates over 8 state
 sets (268 MB > 2x L2) so each step streams its state from HBM.
 
---impl reference times the float64 CPU oracle (the reference arm of this build)
+--impl reference times the float64 CPU oracle (the reference arm)
 on a bounded sample of the same workload on the host cores.
 """
 from __future__ import annotations
