@@ -127,11 +127,156 @@ __global__ void __launch_bounds__(kDecThreads, 8) decode_kernel(DecodeParams p) 
   }
 }
 
+// One token per sequence: the whole batch's state is read in a single wave.  Holding a
+// 32-column slice (16 KB) in registers caps residency at 8 slices per SM, so a batch of
+// 512 heads (2048 slices) ran in 1.7 waves with a tail.  Here a slice takes 64 threads:
+// rows 0-63 of the slice stay in registers (8 float4 per thread) and rows 64-127 are
+// staged in 8 KB of shared memory by cp.async, so 14 slices fit on an SM (2128 on 152
+// SMs).  Each slice is read once and written once, as in the token loop above.
+// Launched as a programmatic dependent: the next step's CTAs are scheduled while this
+// one drains and wait (griddepcontrol.wait) before touching memory.
+constexpr int kDec1Threads = 64;
+
+template <typename T, typename TO>
+__global__ void __launch_bounds__(kDec1Threads, 14) decode1_kernel(DecodeParams p) {
+  const int quarter = blockIdx.x & 3;
+  const int nh = blockIdx.x >> 2;
+  const int n = nh / p.hv;
+  const int h = nh - n * p.hv;
+  const int kh = h / (p.hv / p.hk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rsub = lane >> 3;  // row within the warp's group of 4
+  const int cg = lane & 7;     // column group of 4
+  const int col0 = quarter * kDecCols + cg * 4;
+
+  __shared__ __align__(16) float4 s_S[64][kDecCols / 4];  // rows 64-127 of the slice
+  __shared__ float s_q[kD], s_k[kD], s_v[kDecCols];
+  __shared__ float s_red[2][2][kDecCols];
+
+  // the previous step (a programmatic primary) has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
+  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD + quarter * kDecCols;
+  if (p.state_in) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = tid + kDec1Threads * j, r = e >> 3, g4 = e & 7;
+      cp_async16(&s_S[r][g4], p.state_in + sbase + (size_t)(64 + r) * kD + 4 * g4, 16);
+    }
+    cp_async_commit();
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = tid + kDec1Threads * j;
+      s_S[e >> 3][e & 7] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  float4 S[8];  // rows s * 8 + warp * 4 + rsub, s = 0..7
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int i = s * 8 + warp * 4 + rsub;
+    S[s] = p.state_in
+               ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + 4 * cg)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const T *q = static_cast<const T *>(p.q);
+  const T *k = static_cast<const T *>(p.k);
+  const T *v = static_cast<const T *>(p.v);
+  const size_t t = n;  // token n is sequence n
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    s_q[tid + 64 * e] = Elem<T>::load(q + (t * p.hk + kh) * kD + tid + 64 * e);
+    s_k[tid + 64 * e] = Elem<T>::load(k + (t * p.hk + kh) * kD + tid + 64 * e);
+  }
+  if (tid < kDecCols) s_v[tid] = Elem<T>::load(v + (t * p.hv + h) * kD + quarter * kDecCols + tid);
+  const float d = expf(p.g[t * p.hv + h]);
+  const float b = p.beta[t * p.hv + h];
+  if (p.state_in) cp_async_wait<0>();
+  __syncthreads();
+
+  float qk = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) qk += s_q[lane * 4 + e] * s_k[lane * 4 + e];
+  qk = warp_sum(qk);
+
+  // partial column sums of S^T k and S^T q over this thread's 16 rows
+  float u[4] = {0.f, 0.f, 0.f, 0.f}, w[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < 16; ++s) {
+    const int i = s * 8 + warp * 4 + rsub;
+    const float4 x = s < 8 ? S[s & 7] : s_S[i - 64][cg];
+    const float ki = s_k[i], qi = s_q[i];
+    u[0] += x.x * ki; u[1] += x.y * ki; u[2] += x.z * ki; u[3] += x.w * ki;
+    w[0] += x.x * qi; w[1] += x.y * qi; w[2] += x.z * qi; w[3] += x.w * qi;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    u[e] += __shfl_xor_sync(0xffffffffu, u[e], 8);
+    u[e] += __shfl_xor_sync(0xffffffffu, u[e], 16);
+    w[e] += __shfl_xor_sync(0xffffffffu, w[e], 8);
+    w[e] += __shfl_xor_sync(0xffffffffu, w[e], 16);
+  }
+  if (rsub == 0) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s_red[0][warp][cg * 4 + e] = u[e];
+      s_red[1][warp][cg * 4 + e] = w[e];
+    }
+  }
+  __syncthreads();
+
+  float delta[4];
+  TO *o = static_cast<TO *>(p.o);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int c = cg * 4 + e;
+    const float uu = s_red[0][0][c] + s_red[0][1][c];
+    const float ww = s_red[1][0][c] + s_red[1][1][c];
+    delta[e] = b * (s_v[c] - d * uu);
+    if (warp == 0 && rsub == 0)
+      Elem<TO>::store(o + (t * p.hv + h) * kD + col0 + e, d * ww + qk * delta[e]);
+  }
+  // S' = d S + k delta^T, written straight from the update
+#pragma unroll
+  for (int s = 0; s < 16; ++s) {
+    const int i = s * 8 + warp * 4 + rsub;
+    float4 x = s < 8 ? S[s & 7] : s_S[i - 64][cg];
+    const float ki = s_k[i];
+    x.x = d * x.x + ki * delta[0];
+    x.y = d * x.y + ki * delta[1];
+    x.z = d * x.z + ki * delta[2];
+    x.w = d * x.w + ki * delta[3];
+    *reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)i * kD + 4 * cg) = x;
+  }
+}
+
+template <typename T, typename TO>
+cudaError_t launch_decode1(const DecodeParams &p, unsigned units, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(units);
+  cfg.blockDim = dim3(kDec1Threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode1_kernel<T, TO>, p);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream) {
   const long long units = (long long)p.num_seqs * p.hv * 4;
   if (units == 0) return cudaSuccess;
+  if (!p.cu_seqlens) {  // one token per sequence
+    if (p.dtype == GDN_BF16 && !p.o_fp32)
+      return launch_decode1<__nv_bfloat16, __nv_bfloat16>(p, (unsigned)units, stream);
+    if (p.dtype == GDN_BF16) return launch_decode1<__nv_bfloat16, float>(p, (unsigned)units, stream);
+    return launch_decode1<float, float>(p, (unsigned)units, stream);
+  }
   if (p.dtype == GDN_BF16 && !p.o_fp32)
     decode_kernel<__nv_bfloat16, __nv_bfloat16><<<(unsigned)units, kDecThreads, 0, stream>>>(p);
   else if (p.dtype == GDN_BF16)

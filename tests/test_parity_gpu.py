@@ -207,6 +207,32 @@ def test_decode_one_token_per_sequence(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_one_token_zero_state_and_token_loop(dtype):
+    """One token per sequence from no state (state_in None: zero state), against the
+    oracle; and the one-token kernel (cu_seqlens None) against the token-loop kernel
+    (cu_seqlens = 0, 1, ..., N) on the same batch, both against the oracle."""
+    import torch
+    import gated_deltanet_linear_05_gb300 as gdn
+    wl = gi.Workload("dec0", [1] * 7, 2, 4, dtype=dtype, s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=8)
+    d = device_inputs(x, dtype)
+    s_out = torch.full_like(d["state0"], float("nan"))
+    o32 = torch.empty(d["v"].shape, dtype=torch.float32, device="cuda")
+    gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], None, s_out, None, o32)
+    torch.cuda.synchronize()
+    o_ref, s_ref = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                    np.zeros_like(x["state0"]), x["cu_seqlens"])
+    _check(to_np(o32), to_np(s_out), o_ref, s_ref, dtype, "decode from zero state")
+    o_ref, s_ref = _oracle(x)
+    for cu in (None, d["cu_seqlens"]):
+        s2 = torch.full_like(d["state0"], float("nan"))
+        o2 = torch.empty(d["v"].shape, dtype=torch.float32, device="cuda")
+        gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s2, cu, o2)
+        torch.cuda.synchronize()
+        _check(to_np(o2), to_np(s2), o_ref, s_ref, dtype, "cu_seqlens %s" % (cu is not None))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_decode_token_loop_varlen(dtype):
     """With cu_seqlens the decode kernel walks every sequence token by token."""
     import torch
