@@ -338,7 +338,8 @@ def bench_decode(torch, gdn, gi, device, pk, args):
             "us_per_step_l2_resident": round(times["resident"] * 1e3, 3), "gpu_launches": steps}
 
 
-SCHEDULES = (("two_pass", 1), ("single_pass", 2), ("tensor_memory", 3))  # the last: C = 64 only
+SCHEDULES = (("two_pass", 1), ("single_pass", 2), ("tensor_memory", 3),  # C = 64 only
+             ("recurrent", 4))
 
 
 def bench_chunked_schedules(torch, gdn, d, wl, chunk, fn, op, n, flush):

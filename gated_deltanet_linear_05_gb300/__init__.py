@@ -24,6 +24,7 @@ GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIAS, GDN_ERR_WORKSPA
 GDN_F32, GDN_BF16 = 0, 1
 GDN_OP_PREFILL, GDN_OP_DECODE, GDN_OP_VERIFY = 0, 1, 2
 GDN_ALGO_AUTO, GDN_ALGO_TWO_PASS, GDN_ALGO_SINGLE_PASS, GDN_ALGO_TENSOR_MEMORY = 0, 1, 2, 3
+GDN_ALGO_RECURRENT = 4
 GDN_SINGLE_PASS_MIN_HEADS = 128
 
 GDN_CONV_WIDTH = 4
@@ -267,16 +268,17 @@ def gdn_gated_rmsnorm(o, z, weight, eps: float = 1e-6, y=None, stream=None):
 
 
 def gdn_verify_block_capture(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,
-                             delta=None, chunk: int = 16, stream=None):
+                             delta=None, chunk: int = 16, stream=None, algo: int = GDN_ALGO_AUTO):
     """Draft-verify block (state_in left unchanged) that also writes each token's delta
-    [T, Hv, 128] fp32.  Returns (o, state_out, delta)."""
+    [T, Hv, 128] fp32.  algo: GDN_ALGO_AUTO, GDN_ALGO_SINGLE_PASS or GDN_ALGO_RECURRENT.
+    Returns (o, state_out, delta)."""
     torch = _torch()
     if o is None:
         o = torch.empty_like(v)
     if delta is None:
         delta = torch.empty(v.shape, dtype=torch.float32, device=v.device)
     _check_tensors(q, k, v, g, beta, state_in, state_out, cu_seqlens, o, delta)
-    shape = _shape_of(q, v, o, state_out, cu_seqlens, chunk, GDN_ALGO_AUTO)
+    shape = _shape_of(q, v, o, state_out, cu_seqlens, chunk, algo)
     st = lib().gdn_verify_block_capture(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                         _ptr(beta), _ptr(state_in), _ptr(state_out),
                                         _ptr(cu_seqlens), _ptr(o), _ptr(delta), _stream(stream))

@@ -5,12 +5,16 @@
 // which equals the four-line per-token rule (decay, read, write, output from the
 // updated state).
 //
-// One CTA of 128 threads owns a quarter of one head's state: S[0:128, 32c:32c+32]
-// (value columns are independent: every reduction runs over the key index only).
-// Each thread keeps 8 rows x 4 columns of S in registers for the whole sequence, so
-// the state is read from HBM once and written once, with 128-bit accesses; per token
-// the column sums k^T S and q^T S are formed in one pass, reduced across the 4 rows a
-// warp covers by shuffles and across the 4 warps through shared memory.
+// Token loop (decode_kernel, any number of tokens per sequence): one CTA of 128 threads
+// owns a quarter of one head's state, S[0:128, 32c:32c+32] (value columns are
+// independent: every reduction runs over the key index only).  Each thread keeps 8 rows
+// x 4 columns of S in registers for the whole sequence, so the state is read from HBM
+// once and written once, with 128-bit accesses.  The sequence's tokens are staged in
+// shared memory 16 at a time by cp.async (the first tile issued together with the state
+// loads); per token the column sums k^T S and q^T S are formed in one pass, reduced
+// across the 4 rows a warp covers by shuffles and across the 4 warps through shared
+// memory, with one barrier per token.  It optionally writes each token's delta (the
+// capture of the draft-verify accept step).
 #include "common.cuh"
 #include "internal.h"
 
@@ -20,6 +24,8 @@ namespace {
 
 constexpr int kDecThreads = 128;
 constexpr int kDecCols = 32;  // value columns per CTA
+
+constexpr int kDecTile = 16;  // tokens staged per tile
 
 template <typename T, typename TO>
 __global__ void __launch_bounds__(kDecThreads, 8) decode_kernel(DecodeParams p) {
@@ -41,9 +47,44 @@ __global__ void __launch_bounds__(kDecThreads, 8) decode_kernel(DecodeParams p) 
     eos = n + 1;
   }
 
-  __shared__ float s_q[kD], s_k[kD], s_v[kDecCols];
-  __shared__ float s_red[2][4][kDecCols];
+  // a tile of tokens: q, k rows and this CTA's v columns as stored, gates
+  __shared__ __align__(16) T s_q[kDecTile][kD], s_k[kDecTile][kD];
+  __shared__ __align__(16) T s_v[kDecTile][kDecCols];
+  __shared__ float s_g[kDecTile], s_b[kDecTile];
+  __shared__ float s_red[2][2][4][kDecCols];  // [token parity][u, w][warp][column]
+  const T *q = static_cast<const T *>(p.q);
+  const T *k = static_cast<const T *>(p.k);
+  const T *v = static_cast<const T *>(p.v);
+  TO *o = static_cast<TO *>(p.o);
 
+  // tokens t0 .. t0 + cnt - 1 (cnt >= 1) by cp.async; rows past cnt are zero-filled
+  auto load_tile = [&](int t0, int cnt) {
+    constexpr int EG = 16 / (int)sizeof(T), KG = kD / EG, VG = kDecCols / EG;
+    for (int e = tid; e < kDecTile * KG; e += kDecThreads) {
+      const int r = e / KG, gq = e - r * KG;
+      const bool ok = r < cnt;
+      const size_t tok = (size_t)t0 + (ok ? r : 0);
+      cp_async16(&s_q[r][gq * EG], q + (tok * p.hk + kh) * kD + gq * EG, ok ? 16 : 0);
+      cp_async16(&s_k[r][gq * EG], k + (tok * p.hk + kh) * kD + gq * EG, ok ? 16 : 0);
+    }
+    for (int e = tid; e < kDecTile * VG; e += kDecThreads) {
+      const int r = e / VG, gq = e - r * VG;
+      const bool ok = r < cnt;
+      const size_t tok = (size_t)t0 + (ok ? r : 0);
+      cp_async16(&s_v[r][gq * EG], v + (tok * p.hv + h) * kD + quarter * kDecCols + gq * EG,
+                 ok ? 16 : 0);
+    }
+    if (tid < kDecTile) {
+      const bool ok = tid < cnt;
+      const size_t gi = ((size_t)t0 + (ok ? tid : 0)) * p.hv + h;
+      cp_async4(&s_g[tid], p.g + gi, ok ? 4 : 0);
+      cp_async4(&s_b[tid], p.beta + gi, ok ? 4 : 0);
+    }
+    cp_async_commit();
+  };
+
+  // the first tile's copies and the state's loads go out together
+  if (eos > bos) load_tile(bos, min(kDecTile, eos - bos));
   const size_t sbase = ((size_t)n * p.hv + h) * kD * kD;
   float4 S[8];
 #pragma unroll
@@ -54,70 +95,75 @@ __global__ void __launch_bounds__(kDecThreads, 8) decode_kernel(DecodeParams p) 
                : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
-  const T *q = static_cast<const T *>(p.q);
-  const T *k = static_cast<const T *>(p.k);
-  const T *v = static_cast<const T *>(p.v);
-  TO *o = static_cast<TO *>(p.o);
-
-  for (int t = bos; t < eos; ++t) {
-    s_q[tid] = Elem<T>::load(q + ((size_t)t * p.hk + kh) * kD + tid);
-    s_k[tid] = Elem<T>::load(k + ((size_t)t * p.hk + kh) * kD + tid);
-    if (tid < kDecCols)
-      s_v[tid] = Elem<T>::load(v + ((size_t)t * p.hv + h) * kD + quarter * kDecCols + tid);
-    const float d = expf(p.g[(size_t)t * p.hv + h]);
-    const float b = p.beta[(size_t)t * p.hv + h];
+  int par = 0;
+  for (int t0 = bos; t0 < eos; t0 += kDecTile) {
+    const int cnt = min(kDecTile, eos - t0);
+    cp_async_wait<0>();
     __syncthreads();
+    for (int r = 0; r < cnt; ++r, par ^= 1) {
+      const size_t t = (size_t)t0 + r;
+      // q.k: every warp forms it (4 products per lane, then a butterfly)
+      float qk = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        qk += Elem<T>::load(&s_q[r][lane * 4 + e]) * Elem<T>::load(&s_k[r][lane * 4 + e]);
+      qk = warp_sum(qk);
+      const float d = expf(s_g[r]), b = s_b[r];
 
-    // q.k: every warp forms it (4 products per lane, then a butterfly)
-    float qk = 0.f;
+      // partial column sums of S^T k and S^T q over this thread's 8 rows
+      float u[4] = {0.f, 0.f, 0.f, 0.f}, w[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) qk += s_q[lane * 4 + e] * s_k[lane * 4 + e];
-    qk = warp_sum(qk);
-
-    // partial column sums of S^T k and S^T q over this thread's 8 rows
-    float u[4] = {0.f, 0.f, 0.f, 0.f}, w[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int i = s * 16 + warp * 4 + rsub;
-      const float ki = s_k[i], qi = s_q[i];
-      u[0] += S[s].x * ki; u[1] += S[s].y * ki; u[2] += S[s].z * ki; u[3] += S[s].w * ki;
-      w[0] += S[s].x * qi; w[1] += S[s].y * qi; w[2] += S[s].z * qi; w[3] += S[s].w * qi;
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      u[e] += __shfl_xor_sync(0xffffffffu, u[e], 8);
-      u[e] += __shfl_xor_sync(0xffffffffu, u[e], 16);
-      w[e] += __shfl_xor_sync(0xffffffffu, w[e], 8);
-      w[e] += __shfl_xor_sync(0xffffffffu, w[e], 16);
-    }
-    if (rsub == 0) {
+      for (int s = 0; s < 8; ++s) {
+        const int i = s * 16 + warp * 4 + rsub;
+        const float ki = Elem<T>::load(&s_k[r][i]), qi = Elem<T>::load(&s_q[r][i]);
+        u[0] += S[s].x * ki; u[1] += S[s].y * ki; u[2] += S[s].z * ki; u[3] += S[s].w * ki;
+        w[0] += S[s].x * qi; w[1] += S[s].y * qi; w[2] += S[s].z * qi; w[3] += S[s].w * qi;
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        s_red[0][warp][cg * 4 + e] = u[e];
-        s_red[1][warp][cg * 4 + e] = w[e];
+        u[e] += __shfl_xor_sync(0xffffffffu, u[e], 8);
+        u[e] += __shfl_xor_sync(0xffffffffu, u[e], 16);
+        w[e] += __shfl_xor_sync(0xffffffffu, w[e], 8);
+        w[e] += __shfl_xor_sync(0xffffffffu, w[e], 16);
+      }
+      if (rsub == 0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s_red[par][0][warp][cg * 4 + e] = u[e];
+          s_red[par][1][warp][cg * 4 + e] = w[e];
+        }
+      }
+      // one barrier per token: the partial sums alternate between two buffers, and a
+      // buffer is rewritten only after every thread has passed the next token's barrier
+      __syncthreads();
+
+      float delta[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = cg * 4 + e;
+        const float uu = s_red[par][0][0][c] + s_red[par][0][1][c] + s_red[par][0][2][c] +
+                         s_red[par][0][3][c];
+        const float ww = s_red[par][1][0][c] + s_red[par][1][1][c] + s_red[par][1][2][c] +
+                         s_red[par][1][3][c];
+        delta[e] = b * (Elem<T>::load(&s_v[r][c]) - d * uu);
+        if (warp == 0 && rsub == 0) {
+          Elem<TO>::store(o + (t * p.hv + h) * kD + col0 + e, d * ww + qk * delta[e]);
+          if (p.delta) p.delta[(t * p.hv + h) * kD + col0 + e] = delta[e];
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const float ki = Elem<T>::load(&s_k[r][s * 16 + warp * 4 + rsub]);
+        S[s].x = d * S[s].x + ki * delta[0];
+        S[s].y = d * S[s].y + ki * delta[1];
+        S[s].z = d * S[s].z + ki * delta[2];
+        S[s].w = d * S[s].w + ki * delta[3];
       }
     }
-    __syncthreads();
-
-    float delta[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int c = cg * 4 + e;
-      const float uu = s_red[0][0][c] + s_red[0][1][c] + s_red[0][2][c] + s_red[0][3][c];
-      const float ww = s_red[1][0][c] + s_red[1][1][c] + s_red[1][2][c] + s_red[1][3][c];
-      delta[e] = b * (s_v[c] - d * uu);
-      if (warp == 0 && rsub == 0)
-        Elem<TO>::store(o + ((size_t)t * p.hv + h) * kD + col0 + e, d * ww + qk * delta[e]);
+    if (t0 + kDecTile < eos) {
+      __syncthreads();  // every thread is done with this tile
+      load_tile(t0 + kDecTile, min(kDecTile, eos - t0 - kDecTile));
     }
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const float ki = s_k[s * 16 + warp * 4 + rsub];
-      S[s].x = d * S[s].x + ki * delta[0];
-      S[s].y = d * S[s].y + ki * delta[1];
-      S[s].z = d * S[s].z + ki * delta[2];
-      S[s].w = d * S[s].w + ki * delta[3];
-    }
-    __syncthreads();  // s_q / s_k / s_v / s_red are rewritten by the next token
   }
 
 #pragma unroll
@@ -271,7 +317,7 @@ cudaError_t launch_decode1(const DecodeParams &p, unsigned units, cudaStream_t s
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream) {
   const long long units = (long long)p.num_seqs * p.hv * 4;
   if (units == 0) return cudaSuccess;
-  if (!p.cu_seqlens) {  // one token per sequence
+  if (!p.cu_seqlens && !p.delta) {  // one token per sequence
     if (p.dtype == GDN_BF16 && !p.o_fp32)
       return launch_decode1<__nv_bfloat16, __nv_bfloat16>(p, (unsigned)units, stream);
     if (p.dtype == GDN_BF16) return launch_decode1<__nv_bfloat16, float>(p, (unsigned)units, stream);

@@ -21,7 +21,7 @@ gdn_status check_shape(const gdn_shape *s, bool needs_chunk) {
   if (s->qkv_dtype != GDN_F32 && s->qkv_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if (s->o_fp32 != 0 && s->o_fp32 != 1) return GDN_ERR_INVALID_ARG;
   if (s->algo != GDN_ALGO_AUTO && s->algo != GDN_ALGO_TWO_PASS && s->algo != GDN_ALGO_SINGLE_PASS &&
-      s->algo != GDN_ALGO_TENSOR_MEMORY)
+      s->algo != GDN_ALGO_TENSOR_MEMORY && s->algo != GDN_ALGO_RECURRENT)
     return GDN_ERR_INVALID_ARG;
   if (s->algo == GDN_ALGO_TENSOR_MEMORY && needs_chunk &&
       (s->chunk != 64 || s->qkv_dtype != GDN_BF16))
@@ -79,13 +79,33 @@ bool single_pass(const gdn_shape *s) {
 }
 
 size_t chunked_workspace(const gdn_shape *s) {
-  if (s->qkv_dtype == GDN_F32 || single_pass(s)) return 0;
+  if (s->qkv_dtype == GDN_F32 || s->algo == GDN_ALGO_RECURRENT || single_pass(s)) return 0;
   return gdn::chunk_workspace_bytes(s->total_tokens, s->num_seqs, s->num_v_heads, s->chunk);
 }
 
 gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes, void *stream,
                        float *delta = nullptr) {
   const gdn_shape *s = c.s;
+  if (s->algo == GDN_ALGO_RECURRENT) {  // the token loop
+    DecodeParams d{};
+    d.num_seqs = s->num_seqs;
+    d.total_tokens = s->total_tokens;
+    d.hk = s->num_k_heads;
+    d.hv = s->num_v_heads;
+    d.dtype = s->qkv_dtype;
+    d.o_fp32 = s->o_fp32 != 0;
+    d.q = c.q;
+    d.k = c.k;
+    d.v = c.v;
+    d.g = c.g;
+    d.beta = c.beta;
+    d.state_in = c.state_in;
+    d.state_out = c.state_out;
+    d.cu_seqlens = c.cu_seqlens;
+    d.o = c.o;
+    d.delta = delta;
+    return cuda_status(gdn::launch_decode(d, static_cast<cudaStream_t>(stream)));
+  }
   ChunkParams p{};
   p.delta = delta;
   p.num_seqs = s->num_seqs;
@@ -319,7 +339,9 @@ gdn_status gdn_verify_block_capture(const gdn_shape *shape, const void *q, const
                                     void *stream) {
   gdn_status st = check_shape(shape, true);
   if (st != GDN_OK) return st;
-  if (shape->algo != GDN_ALGO_AUTO && shape->algo != GDN_ALGO_SINGLE_PASS) return GDN_ERR_UNSUPPORTED;
+  if (shape->algo != GDN_ALGO_AUTO && shape->algo != GDN_ALGO_SINGLE_PASS &&
+      shape->algo != GDN_ALGO_RECURRENT)
+    return GDN_ERR_UNSUPPORTED;
   Common c{shape, q, k, v, g, beta, state_in, state_out, cu_seqlens, o};
   if ((st = check_buffers(c, true)) != GDN_OK) return st;
   if (shape->total_tokens > 0 && (!delta || !aligned16(delta))) return GDN_ERR_INVALID_ARG;

@@ -18,6 +18,7 @@ struct DecodeParams {
   float *state_out;
   const int32_t *cu_seqlens;  // NULL: one token per sequence
   void *o;
+  float *delta;  // per-token deltas [T, Hv, 128] fp32, or NULL
 };
 
 struct ChunkParams {

@@ -95,12 +95,21 @@ typedef enum { GDN_OP_PREFILL = 0, GDN_OP_DECODE = 1, GDN_OP_VERIFY = 2 } gdn_op
  *                state in tensor memory, every block's operands read once per head, the
  *                next block's state-free part prepared while the current one runs; no
  *                workspace.  Block length 64 and bf16 q/k/v only (else GDN_ERR_UNSUPPORTED).
+ *   RECURRENT    the per-token rule itself, token by token (the token loop of
+ *                gdn_decode_step): one CTA per (sequence, v-head, 32 value columns) with
+ *                its state slice in registers for the whole sequence and the tokens staged
+ *                16 at a time; fp32 arithmetic on CUDA cores (no product is rounded to
+ *                16 bits), no workspace, any valid shape->chunk (not used).  The most
+ *                accurate schedule and the slowest: the per-token reductions over the keys
+ *                cost several times the chunk schedules' tensor-core work from 16 tokens
+ *                up.  AUTO never picks it.
  * All give results within the same bounds; they are not bit-identical to each other. */
 typedef enum {
   GDN_ALGO_AUTO = 0,
   GDN_ALGO_TWO_PASS = 1,
   GDN_ALGO_SINGLE_PASS = 2,
-  GDN_ALGO_TENSOR_MEMORY = 3
+  GDN_ALGO_TENSOR_MEMORY = 3,
+  GDN_ALGO_RECURRENT = 4
 } gdn_algo;
 #define GDN_SINGLE_PASS_MIN_HEADS 128
 
@@ -173,8 +182,9 @@ gdn_status gdn_verify_block(const gdn_shape *shape, const void *q, const void *k
  *     delta  [total_tokens, Hv, dv] float32, 16-byte aligned (written for every token).
  * With the deltas, gdn_state_rollback gives the state after any accepted prefix of the
  * draft without re-feeding the accepted tokens.  Runs the single-pass schedule (bf16) or
- * the fp32 kernel; shape->algo must be GDN_ALGO_AUTO or GDN_ALGO_SINGLE_PASS (else
- * GDN_ERR_UNSUPPORTED).  Needs no workspace.
+ * the fp32 kernel, or with GDN_ALGO_RECURRENT the token loop; shape->algo must be
+ * GDN_ALGO_AUTO, GDN_ALGO_SINGLE_PASS or GDN_ALGO_RECURRENT (else GDN_ERR_UNSUPPORTED).
+ * Needs no workspace.
  */
 gdn_status gdn_verify_block_capture(const gdn_shape *shape, const void *q, const void *k,
                                     const void *v, const float *g, const float *beta,

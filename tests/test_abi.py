@@ -81,7 +81,12 @@ def test_workspace_size_follows_the_schedule(L):
         assert two > 0 and one == 0
         assert auto == (0 if n * hv >= gdn.GDN_SINGLE_PASS_MIN_HEADS else two)
     with pytest.raises(gdn.GdnError):
-        gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, algo=4), gdn.GDN_OP_PREFILL)
+        gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, algo=5), gdn.GDN_OP_PREFILL)
+    # the token loop (recurrent schedule) needs none, for any block length
+    for chunk in (16, 32, 64):
+        for op in (gdn.GDN_OP_PREFILL, gdn.GDN_OP_VERIFY):
+            assert gdn.gdn_workspace_size(gdn.make_shape(8, 4096, 16, 32, chunk=chunk,
+                                                         algo=gdn.GDN_ALGO_RECURRENT), op) == 0
     # the tensor-memory schedule: 64-token blocks of bf16 q/k/v only, no workspace
     assert gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, chunk=64,
                                                  algo=gdn.GDN_ALGO_TENSOR_MEMORY),

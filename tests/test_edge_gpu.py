@@ -11,7 +11,7 @@ from gdn_testlib import device_inputs, gpu_prefill, rel_err, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = {"two_pass": 1, "single_pass": 2, "tensor_memory": 3}
+ALGOS = {"two_pass": 1, "single_pass": 2, "tensor_memory": 3, "recurrent": 4}
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -19,10 +19,10 @@ from gdn_testlib import device_inputs, gpu_prefill, half_ulp_bf16, rel_err, to_n
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": 1e-4, "bf16": 2e-2}
-# the two kernel schedules of the bf16 chunked pass (f32 q/k/v have one)
-ALGOS = {"two_pass": 1, "single_pass": 2, "tensor_memory": 3}
+# the schedules of the bf16 chunked pass (f32 q/k/v: the fp32 kernel, or the token loop)
+ALGOS = {"two_pass": 1, "single_pass": 2, "tensor_memory": 3, "recurrent": 4}
 # schedules built for every block length (tensor_memory: 64-token blocks only)
-ALGOS_ANY_C = ["two_pass", "single_pass"]
+ALGOS_ANY_C = ["two_pass", "single_pass", "recurrent"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -98,7 +98,8 @@ def test_prefill_small_shapes_bf16(algo, chunk, lengths, hk, hv):
 
 
 @pytest.mark.parametrize("dtype,algo", [("f32", None), ("bf16", "two_pass"),
-                                        ("bf16", "single_pass"), ("bf16", "tensor_memory")])
+                                        ("bf16", "single_pass"), ("bf16", "tensor_memory"),
+                                        ("bf16", "recurrent"), ("f32", "recurrent")])
 def test_prefill_zero_initial_state_and_in_place(dtype, algo):
     kw = {"algo": ALGOS[algo]} if algo else {}
     chunk = 32 if algo in (None, *ALGOS_ANY_C) else 64
@@ -306,7 +307,7 @@ def test_chunk16_matches_chunk64_bf16(algo):
     _check(o16, s16, o64, s64, "bf16", "C16 vs C64")
 
 
-@pytest.mark.parametrize("algo", ["single_pass", "tensor_memory"])
+@pytest.mark.parametrize("algo", ["single_pass", "tensor_memory", "recurrent"])
 def test_schedules_agree_bf16(algo):
     wl = gi.Workload("c", [300, 77, 1], 2, 4, dtype="bf16", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=5)

@@ -22,7 +22,7 @@ def _built():
     build.build()
 
 
-def _capture(x, wl, chunk=16):
+def _capture(x, wl, chunk=16, algo=0):
     import torch
     import gated_deltanet_linear_05_gb300 as gdn
     d = device_inputs(x, wl.dtype)
@@ -30,7 +30,8 @@ def _capture(x, wl, chunk=16):
     o = torch.full(d["v"].shape, float("nan"), device="cuda",
                    dtype=torch.float32 if wl.dtype == "f32" else torch.float32)
     o, s, delta = gdn.gdn_verify_block_capture(d["q"], d["k"], d["v"], d["g"], d["beta"],
-                                               d["state0"], s_out, d["cu_seqlens"], o, chunk=chunk)
+                                               d["state0"], s_out, d["cu_seqlens"], o, chunk=chunk,
+                                               algo=algo)
     torch.cuda.synchronize()
     return d, o, s, delta
 
@@ -39,11 +40,12 @@ CASES = [([16] * 6, 2, 4, "bf16", 16), ([16, 3, 1, 16, 9], 1, 2, "f32", 16),
          ([40, 17, 64], 2, 2, "bf16", 16), ([70, 5], 1, 1, "bf16", 64), ([33, 16], 1, 2, "f32", 32)]
 
 
+@pytest.mark.parametrize("algo", [0, 4])  # AUTO (the single-pass schedule), the token loop
 @pytest.mark.parametrize("lengths,hk,hv,dtype,chunk", CASES)
-def test_capture_outputs_and_deltas(lengths, hk, hv, dtype, chunk):
+def test_capture_outputs_and_deltas(lengths, hk, hv, dtype, chunk, algo):
     wl = gi.Workload("cap", lengths, hk, hv, chunk=chunk, dtype=dtype, s0_scale=0.1)
     x = gi.make_inputs(wl, seed=len(lengths))
-    d, o, s, delta = _capture(x, wl, chunk)
+    d, o, s, delta = _capture(x, wl, chunk, algo)
     o_ref, s_ref, d_ref = oracle.recurrent_deltas(x["q"], x["k"], x["v"], x["g"], x["beta"],
                                                   x["state0"], x["cu_seqlens"])
     for name, a, r in (("o", to_np(o), o_ref), ("state", to_np(s), s_ref),
