@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kIoThreads, 2) prologue_kernel(PrologueParams 
       float ss = conv(x[0], x[1], x[2], x[3], y);
       if (normed) {
         ss = warp_sum(ss);
-        const float sc = 1.f / sqrtf(ss + p.eps);
+        const float sc = rsqrtf(ss + p.eps);  // the same rounding on every path
 #pragma unroll
         for (int c = 0; c < 4; ++c) y[c] *= sc;
       }
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kIoThreads, 2) prologue_kernel(PrologueParams 
           float ss = conv(win[0], win[1], win[2], x, y);
           if (normed) {
             ss = warp_sum(ss);
-            const float sc = 1.f / sqrtf(ss + p.eps);
+            const float sc = rsqrtf(ss + p.eps);
 #pragma unroll
             for (int c = 0; c < 4; ++c) y[c] *= sc;
           }

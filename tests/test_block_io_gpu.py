@@ -105,6 +105,30 @@ def test_prologue_packed_sequences(dtype, lengths, hk, hv):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_prologue_packing_does_not_change_a_bit(dtype):
+    """A token's outputs (and its sequence's advanced FIFO) are the same bits whether the
+    sequence runs packed behind others or alone: the kernel's 16-token units and their
+    boundary path fall on different tokens in the two runs."""
+    lengths = [37, 5, 90, 16, 3, 21]
+    wl = gi.Workload("pack", lengths, 2, 4, dtype=dtype)
+    x = gi.make_block_inputs(wl, seed=12)
+    packed, cs_packed = _gpu_prologue(x, wl)
+    cu = x["cu_seqlens"]
+    for n, L in enumerate(lengths):
+        a, b = int(cu[n]), int(cu[n + 1])
+        xn = dict(x)
+        for name in ("q_raw", "k_raw", "v_raw"):
+            xn[name], xn[name + "_st"] = x[name][a:b], x[name + "_st"][a:b]
+        xn["a"], xn["b"] = x["a"][a:b], x["b"][a:b]
+        xn["conv_state0"], xn["conv_state0_st"] = x["conv_state0"][n:n + 1], x["conv_state0_st"][n:n + 1]
+        xn["cu_seqlens"] = np.array([0, L], np.int32)
+        alone, cs_alone = _gpu_prologue(xn, gi.Workload("one", [L], 2, 4, dtype=dtype))
+        for i, name in enumerate(("q", "k", "v", "g", "beta")):
+            assert np.array_equal(packed[i][a:b], alone[i]), (n, name)
+        assert np.array_equal(cs_packed[n:n + 1], cs_alone), n
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_prologue_in_place_state(dtype):
     wl = gi.Workload("pro", [5, 1, 70, 2, 33], 2, 4, dtype=dtype)
     x = gi.make_block_inputs(wl, seed=11)
