@@ -135,20 +135,21 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
     }
   };
   if (nchunks > 0) issue_loads(0, 0);
-  if constexpr (C == 16) {  // the state rides along with block 0's copies
+  cp_async_commit();  // block 0's q, k, v and gates
+  if constexpr (C == 16) {
+    // the state in a group of its own: block 0's state-free work (Grams, T, W, U) runs
+    // while it lands, and the chain waits for it only before its first product
     if (p.state_in)
       for (int e = tid; e < kD * kD / 4; e += NT) {
         const int r = e >> 5, c4 = e & 31;
         cp_async16(&sm.SS[r][4 * c4], p.state_in + sbase + (size_t)r * kD + 4 * c4, 16);
       }
+    cp_async_commit();
   }
-  cp_async_commit();
 
   // S^T[j][i] for j = j0 + gid (+8), i = 8nt + 2tig (+1): 16 accumulator tiles
   float S[16][4];
-  if constexpr (C == 16) {
-    cp_async_wait<0>();
-    __syncthreads();
+  auto state_from_staging = [&]() {
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt)
 #pragma unroll
@@ -156,6 +157,13 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
         const int i = 8 * nt + 2 * tig + (e & 1), j = j0 + gid + 8 * (e >> 1);
         S[nt][e] = p.state_in ? sm.SS[i][j] : 0.f;
       }
+  };
+  if constexpr (C == 16) {
+    if (nchunks == 0) {  // an empty sequence passes its state through
+      cp_async_wait<0>();
+      __syncthreads();
+      state_from_staging();
+    }
   } else {
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt)
@@ -195,7 +203,12 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
     // T starts at zero: the doubling products read whole 32x32 blocks of T, whose upper
     // parts are never written
     for (int e = tid; e < C * LD; e += NT) (&Tm[0][0])[e] = 0.f;
-    cp_async_wait<1>();  // this block's group has landed
+    // this block's group has landed (block 0 of 16-token blocks: the state's group,
+    // issued after it, may still be in flight)
+    if (C == 16 && c == 0)
+      cp_async_wait<2>();
+    else
+      cp_async_wait<1>();
     __syncthreads();
     char *Kb = sm.K[buf], *Qb = sm.Q[buf], *Vb = sm.V[buf];
 
@@ -413,7 +426,11 @@ __global__ void __launch_bounds__(kFThreads, C == 16 ? 2 : 1) fused_kernel(Chunk
           }
       }
     }
+    if (C == 16 && c == 0) cp_async_wait<1>();  // the state has landed as well
     __syncthreads();
+    if constexpr (C == 16) {
+      if (c == 0) state_from_staging();
+    }
 
     // ================= per-warp state chain for value columns j0 .. j0+15
     // D^T = V^T T_u^T  (U^T), then minus S^T W^T
