@@ -112,6 +112,22 @@ def test_prefill_zero_initial_state_and_in_place(dtype, algo):
     _run_and_check(x0, wl, o_ref0, s_ref0, "zero state", state_in=False, **kw)
 
 
+@pytest.mark.parametrize("verify", [False, True])
+@pytest.mark.parametrize("inplace", [False, True])
+def test_single_pass_16_token_blocks_many_units(verify, inplace):
+    """16-token blocks on the single-pass schedule: each CTA walks several (sequence, head)
+    units (400 here, more than one per SM) and prefetches the next unit's first block and
+    state while it computes; empty sequences among them pass their state through."""
+    if verify and inplace:
+        pytest.skip("the verify block keeps its snapshot: no in-place state")
+    lengths = [(0, 1, 16, 17, 40, 5, 0, 33)[i % 8] for i in range(200)]
+    wl = gi.Workload("many16", lengths, 1, 2, chunk=16, dtype="bf16", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=21)
+    o_ref, s_ref = _oracle(x)
+    _run_and_check(x, wl, o_ref, s_ref, "many units", inplace=inplace, verify=verify,
+                   algo=ALGOS["single_pass"])
+
+
 @pytest.mark.parametrize("algo", list(ALGOS))
 def test_prefill_slow_decay_bf16(algo):
     """g = -0.01 softplus(.): the state carries across many blocks."""
