@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GDN prefill tokens/s (%TC roofline); decode state GB/s (%HBM peak)"
 D = 128
-EXTRA_ROWS = ("decode", "verify", "varlen", "prologue", "gated_rmsnorm", "accept")
+EXTRA_ROWS = ("decode", "verify", "varlen", "prologue", "gated_rmsnorm", "accept", "split")
 
 
 def parse():
@@ -240,7 +240,8 @@ def run_gdn(args):
                 "varlen": lambda: bench_varlen(torch, gdn, gi, device, pk, args, flush),
                 "prologue": lambda: bench_prologue(torch, gdn, gi, device, pk, args, flush),
                 "gated_rmsnorm": lambda: bench_gated_rmsnorm(torch, gdn, gi, device, pk, args, flush),
-                "accept": lambda: bench_accept(torch, gdn, gi, device, pk, args, flush)}
+                "accept": lambda: bench_accept(torch, gdn, gi, device, pk, args, flush),
+                "split": lambda: bench_split(torch, gdn, gi, device, pk, args, flush)}
         for name in EXTRA_ROWS:
             if not args.only or name in args.only:
                 out[name] = rows[name]()
@@ -466,6 +467,44 @@ def bench_gated_rmsnorm(torch, gdn, gi, device, pk, args, flush):
             "rows_per_s": round(o.numel() // D / (ms * 1e-3), 1),
             "roofline": roofline("hbm", byts / (ms * 1e-3) / 1e9, pk["hbm"], "GB/s"),
             "algorithmic_bytes": byts, "gpu_launches": n}
+
+
+def bench_split(torch, gdn, gi, device, pk, args, flush):
+    """Few heads and one long sequence (N=1, H=2, T=65,536): the chunked pass (AUTO: two
+    passes) against the sequence-split pass at a few segment lengths."""
+    wl = gi.long_t65536_h2()
+    d = dev_inputs(gi.make_inputs(wl), torch, device)
+    s_out = torch.empty_like(d["state0"])
+    o = torch.empty_like(d["v"])
+    n = max(3, min(args.steps, 20))
+    shape = gdn.make_shape(wl.num_seqs, wl.total_tokens, wl.num_k_heads, wl.num_v_heads, chunk=64)
+    ws = torch.empty(gdn.gdn_workspace_size(shape, gdn.GDN_OP_PREFILL) + 256, dtype=torch.uint8,
+                     device=device)
+
+    def plain():
+        gdn.gdn_prefill_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
+                                d["cu"], o, chunk=64, workspace=ws)
+
+    res = {"chunked": statistics.mean(timed_steps(torch, plain, n, 2, flush))}
+    del ws
+    for seg in (2048, 4096, 7296):  # 33, 17 and 9 segments
+        sws = torch.empty(gdn.gdn_prefill_split_workspace_size(shape, seg) + 256,
+                          dtype=torch.uint8, device=device)
+
+        def split():
+            gdn.gdn_prefill_split(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
+                                  d["cu"], o, segment_len=seg, chunk=64, workspace=sws)
+
+        res["split_%d" % seg] = statistics.mean(timed_steps(torch, split, n, 2, flush))
+        del sws
+    torch.cuda.empty_cache()
+    best = min((v, k) for k, v in res.items() if k.startswith("split"))
+    flops, byts = prefill_work(wl.lengths, wl.num_k_heads, wl.num_v_heads, 64)
+    return {"workload": wl.name, "us_per_step_by_schedule": {k: round(v * 1e3, 2) for k, v in res.items()},
+            "best_split": best[1], "tokens_per_s": round(wl.total_tokens / (best[0] * 1e-3), 1),
+            "speedup_over_chunked": round(res["chunked"] / best[0], 3),
+            "roofline": roofline("hbm", byts / (best[0] * 1e-3) / 1e9, pk["hbm"], "GB/s"),
+            "gpu_launches": n * (2 + 3 * 9)}
 
 
 def bench_accept(torch, gdn, gi, device, pk, args, flush):

@@ -32,7 +32,8 @@ GDN_CONV_WIDTH = 4
 EXPORTS = ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_block",
            "gdn_workspace_size", "gdn_status_string", "gdn_prefill_chunked_noalloc",
            "gdn_input_prologue", "gdn_gated_rmsnorm", "gdn_verify_block_capture",
-           "gdn_state_rollback", "gdn_conv_state_rollback")
+           "gdn_state_rollback", "gdn_conv_state_rollback", "gdn_prefill_split",
+           "gdn_prefill_split_workspace_size")
 
 
 class GdnUnavailable(RuntimeError):
@@ -92,6 +93,11 @@ def lib() -> ctypes.CDLL:
         L.gdn_state_rollback.restype = ctypes.c_int
         L.gdn_conv_state_rollback.argtypes = [ctypes.POINTER(GdnShape)] + [P] * 8
         L.gdn_conv_state_rollback.restype = ctypes.c_int
+        I32 = ctypes.c_int32
+        L.gdn_prefill_split.argtypes = [ctypes.POINTER(GdnShape)] + [P] * 9 + [I32, P, S, P]
+        L.gdn_prefill_split.restype = ctypes.c_int
+        L.gdn_prefill_split_workspace_size.argtypes = [ctypes.POINTER(GdnShape), I32]
+        L.gdn_prefill_split_workspace_size.restype = ctypes.c_size_t
         _lib = L
     return _lib
 
@@ -111,6 +117,13 @@ def gdn_workspace_size(shape: GdnShape, op: int) -> int:
     n = lib().gdn_workspace_size(ctypes.byref(shape), int(op))
     if n == ctypes.c_size_t(-1).value:
         raise GdnError(GDN_ERR_INVALID_ARG, "gdn_workspace_size")
+    return n
+
+
+def gdn_prefill_split_workspace_size(shape: GdnShape, segment_len: int) -> int:
+    n = lib().gdn_prefill_split_workspace_size(ctypes.byref(shape), int(segment_len))
+    if n == ctypes.c_size_t(-1).value:
+        raise GdnError(GDN_ERR_INVALID_ARG, "gdn_prefill_split_workspace_size")
     return n
 
 
@@ -193,6 +206,31 @@ def gdn_prefill_chunked(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=Non
         o = _torch().empty_like(v)
     return _call("gdn_prefill_chunked", GDN_OP_PREFILL, q, k, v, g, beta, state_in, state_out,
                  cu_seqlens, o, chunk, workspace, stream, algo)
+
+
+def gdn_prefill_split(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,
+                      segment_len: int = 1024, chunk: int = 64, workspace=None, stream=None,
+                      algo: int = GDN_ALGO_AUTO):
+    """Sequence-split prompt pass: the results of gdn_prefill_chunked, each sequence cut
+    into segments of segment_len tokens (a multiple of chunk) that run side by side.
+    Returns (o, state_out)."""
+    torch = _torch()
+    if o is None:
+        o = torch.empty_like(v)
+    _check_tensors(q, k, v, g, beta, state_in, state_out, cu_seqlens, o, workspace)
+    shape = _shape_of(q, v, o, state_out, cu_seqlens, chunk, algo)
+    need = gdn_prefill_split_workspace_size(shape, segment_len)
+    if workspace is None:
+        workspace = torch.empty(need + 256, dtype=torch.uint8, device=q.device)
+    base = workspace.data_ptr()
+    aligned = (base + 255) & ~255
+    st = lib().gdn_prefill_split(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                 _ptr(beta), _ptr(state_in), _ptr(state_out), _ptr(cu_seqlens),
+                                 _ptr(o), int(segment_len), aligned,
+                                 workspace.numel() - (aligned - base), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_prefill_split")
+    return o, state_out
 
 
 def gdn_verify_block(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,

@@ -534,8 +534,8 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
           for (int hr = 0; hr < 2; ++hr) {
             const float2 u = f16x2_to_float2(*reinterpret_cast<const uint32_t *>(
                 st.U + (gid + 8 * hr) * RC + 2 * (16 * w + 8 * a + 2 * tig)));
-            D0[a][2 * hr] = u.x;
-            D0[a][2 * hr + 1] = u.y;
+            D0[a][2 * hr] = p.u_zero ? 0.f : u.x;
+            D0[a][2 * hr + 1] = p.u_zero ? 0.f : u.y;
             D1[a][2 * hr] = D1[a][2 * hr + 1] = 0.f;
           }
 #pragma unroll
@@ -723,7 +723,7 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
   long long per_head = (8LL * sms + heads - 1) / heads;
   per_head = max(1LL, min(per_head, max(1LL, max_chunks)));
 
-  if (p.total_tokens > 0) {
+  if (p.total_tokens > 0 && p.passes != 2) {
     const size_t s1 = sizeof(PrepSmem<C>);
     err = cudaFuncSetAttribute(prep_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     if (err != cudaSuccess) return err;
@@ -731,6 +731,7 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
+  if (p.passes == 1) return cudaSuccess;
   return p.o_fp32 ? launch_recur<C, float>(p, heads, stream)
                   : launch_recur<C, __nv_bfloat16>(p, heads, stream);
 }

@@ -84,7 +84,7 @@ size_t chunked_workspace(const gdn_shape *s) {
 }
 
 gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes, void *stream,
-                       float *delta = nullptr) {
+                       float *delta = nullptr, int passes = 0, int u_zero = 0) {
   const gdn_shape *s = c.s;
   if (s->algo == GDN_ALGO_RECURRENT) {  // the token loop
     DecodeParams d{};
@@ -108,6 +108,8 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   }
   ChunkParams p{};
   p.delta = delta;
+  p.passes = passes;
+  p.u_zero = u_zero;
   p.num_seqs = s->num_seqs;
   p.total_tokens = s->total_tokens;
   p.hk = s->num_k_heads;
@@ -144,7 +146,131 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   return cuda_status(gdn::launch_chunk_bf16(p, st));
 }
 
+// Sequence-split prefill: the workspace regions (each 256-byte aligned), in order:
+// segment boundaries, first segment of each sequence, a zero v, scratch outputs, the
+// identity states (overwritten by the maps M_s), the local states L_s, the segments'
+// incoming states, and the inner chunked pass's own workspace.
+struct SplitLayout {
+  int max_segs;
+  size_t cu_seg, seg_first, v_zero, o_scratch, ident, local, seg_in, inner, total;
+  gdn_shape inner_shape;
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+SplitLayout split_layout(const gdn_shape *s, int seg_len) {
+  SplitLayout L{};
+  L.max_segs = (s->total_tokens + seg_len - 1) / seg_len + s->num_seqs;
+  L.inner_shape = *s;
+  L.inner_shape.num_seqs = L.max_segs;
+  const size_t es = s->qkv_dtype == GDN_F32 ? 4 : 2;
+  const size_t eo = (s->qkv_dtype == GDN_F32 || s->o_fp32) ? 4 : 2;
+  const size_t vals = (size_t)s->total_tokens * s->num_v_heads * s->dv;
+  const size_t states = (size_t)L.max_segs * s->num_v_heads * s->dk * s->dv * sizeof(float);
+  size_t off = 0;
+  L.cu_seg = off;    off += align256(sizeof(int32_t) * (L.max_segs + 1));
+  L.seg_first = off; off += align256(sizeof(int32_t) * (s->num_seqs + 1));
+  L.v_zero = off;    off += align256(vals * es);
+  L.o_scratch = off; off += align256(vals * eo);
+  L.ident = off;     off += align256(states);
+  L.local = off;     off += align256(states);
+  L.seg_in = off;    off += align256(states);
+  L.inner = off;     off += align256(chunked_workspace(&L.inner_shape));
+  L.total = off;
+  return L;
+}
+
+gdn_status check_split(const gdn_shape *s, int32_t seg_len) {
+  gdn_status st = check_shape(s, true);
+  if (st != GDN_OK) return st;
+  if (seg_len <= 0 || seg_len % s->chunk != 0) return GDN_ERR_INVALID_ARG;
+  if (s->algo == GDN_ALGO_RECURRENT) return GDN_ERR_UNSUPPORTED;
+  const long long max_segs = ((long long)s->total_tokens + seg_len - 1) / seg_len + s->num_seqs;
+  if (max_segs * s->num_v_heads * 8 > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  if ((long long)s->num_seqs * s->num_v_heads * 32 > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
 }  // namespace
+
+extern "C" {
+
+size_t gdn_prefill_split_workspace_size(const gdn_shape *shape, int32_t segment_len) {
+  if (check_split(shape, segment_len) != GDN_OK) return (size_t)-1;
+  return split_layout(shape, segment_len).total;
+}
+
+gdn_status gdn_prefill_split(const gdn_shape *shape, const void *q, const void *k,
+                             const void *v, const float *g, const float *beta,
+                             const float *state_in, float *state_out,
+                             const int32_t *cu_seqlens, void *o, int32_t segment_len,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+  gdn_status st = check_split(shape, segment_len);
+  if (st != GDN_OK) return st;
+  Common c{shape, q, k, v, g, beta, state_in, state_out, cu_seqlens, o};
+  if ((st = check_buffers(c, true)) != GDN_OK) return st;
+  if (state_in && partial_overlap(state_in, state_out, state_bytes(shape))) return GDN_ERR_ALIAS;
+  if (shape->num_seqs == 0) return GDN_OK;
+  const SplitLayout L = split_layout(shape, segment_len);
+  if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return GDN_ERR_WORKSPACE;
+  char *ws = static_cast<char *>(workspace);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  int32_t *cu_seg = reinterpret_cast<int32_t *>(ws + L.cu_seg);
+  int32_t *seg_first = reinterpret_cast<int32_t *>(ws + L.seg_first);
+  float *ident = reinterpret_cast<float *>(ws + L.ident);
+  float *local = reinterpret_cast<float *>(ws + L.local);
+  float *seg_in = reinterpret_cast<float *>(ws + L.seg_in);
+  void *inner_ws = ws + L.inner;
+  const size_t inner_bytes = L.total - L.inner;
+
+  gdn::SplitPlanParams pp{};
+  pp.num_seqs = shape->num_seqs;
+  pp.total_tokens = shape->total_tokens;
+  pp.seg_len = segment_len;
+  pp.max_segs = L.max_segs;
+  pp.cu_seqlens = cu_seqlens;
+  pp.cu_seg = cu_seg;
+  pp.seg_first = seg_first;
+  if (gdn::launch_split_plan(pp, cs) != cudaSuccess) return GDN_ERR_CUDA;
+  if (gdn::launch_identity(ident, (long long)L.max_segs * shape->num_v_heads, cs) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  // On the bf16 two-pass schedule the three runs share one pass 1 (its slots depend on q,
+  // k, v, g, beta only), and the map run's pass 2 takes U as zero; other schedules run in
+  // full, the map run on a zero v.
+  const bool shared = shape->qkv_dtype == GDN_BF16 && !single_pass(&L.inner_shape);
+  Common a{&L.inner_shape, q, k, v, g, beta, nullptr, local, cu_seg, ws + L.o_scratch};
+  Common b{&L.inner_shape, q, k, ws + L.v_zero, g, beta, ident, ident, cu_seg, ws + L.o_scratch};
+  Common d{&L.inner_shape, q, k, v, g, beta, seg_in, seg_in, cu_seg, o};
+  const int run = shared ? 2 : 0;
+  if (shared) {
+    if ((st = run_chunked(a, inner_ws, inner_bytes, stream, nullptr, 1)) != GDN_OK) return st;
+  } else {
+    if (cudaMemsetAsync(ws + L.v_zero, 0, L.o_scratch - L.v_zero, cs) != cudaSuccess)
+      return GDN_ERR_CUDA;
+  }
+  // 1. every segment from a zero state: its local final state
+  if ((st = run_chunked(a, inner_ws, inner_bytes, stream, nullptr, run)) != GDN_OK) return st;
+  // 2. every segment with v = 0 from the identity: its map M_s (in place over the identity)
+  if ((st = run_chunked(b, inner_ws, inner_bytes, stream, nullptr, run, shared ? 1 : 0)) != GDN_OK)
+    return st;
+  // 3. the segments' incoming states in order, and each sequence's final state
+  gdn::SplitCombineParams cp{};
+  cp.num_seqs = shape->num_seqs;
+  cp.hv = shape->num_v_heads;
+  cp.seg_first = seg_first;
+  cp.state_in = state_in;
+  cp.map = ident;
+  cp.local = local;
+  cp.seg_in = seg_in;
+  cp.state_out = state_out;
+  if (gdn::launch_split_combine(cp, cs) != cudaSuccess) return GDN_ERR_CUDA;
+  // 4. every segment from its incoming state: the outputs (its final state, in place, is
+  //    not needed again)
+  return run_chunked(d, inner_ws, inner_bytes, stream, nullptr, run);
+}
+
+}  // extern "C"
 
 extern "C" {
 
@@ -315,8 +441,7 @@ gdn_status gdn_gated_rmsnorm(const gdn_shape *shape, const void *o, const void *
   const size_t eo = s->o_fp32 ? 4 : es;
   const size_t ny = (size_t)rows * s->dv * es;
   const size_t no = (size_t)rows * s->dv * eo;
-  const uintptr_t yo = reinterpret_cast<uintptr_t>(y), oo = reinterpret_cast<uintptr_t>(o),
-                  zo = reinterpret_cast<uintptr_t>(z);
+  const uintptr_t yo = reinterpret_cast<uintptr_t>(y), oo = reinterpret_cast<uintptr_t>(o);
   // in place only onto a buffer of the same element size, exactly
   if (yo < oo + no && oo < yo + ny && !(yo == oo && eo == es)) return GDN_ERR_ALIAS;
   if (partial_overlap(y, z, ny)) return GDN_ERR_ALIAS;

@@ -44,6 +44,10 @@ struct ChunkParams {
   int nslots;
   char *slot_ws;      // Hv * nslots slots of slot_bytes(C) bytes, 128-byte aligned
   int *err;           // device status word: nonzero if a kernel wait timed out
+  // Two-pass path only: which passes to run (1: pass 1, 2: pass 2, else both), and
+  // whether pass 2 takes U as zero (the slots of a pass 1 run with these q, k, g, beta)
+  int passes;
+  int u_zero;
 };
 
 // Padded row bytes of 16-bit tiles: 128-element rows and C-element rows.
@@ -105,6 +109,26 @@ struct NormParams {
 
 cudaError_t launch_prologue(const PrologueParams &p, cudaStream_t stream);
 cudaError_t launch_gated_rmsnorm(const NormParams &p, cudaStream_t stream);
+
+// Sequence-split prefill (split.cu): segment boundaries, identity states, the combine.
+struct SplitPlanParams {
+  int num_seqs, total_tokens, seg_len, max_segs;
+  const int32_t *cu_seqlens;
+  int32_t *cu_seg;     // [max_segs + 1] segment boundaries (unused segments empty, at the end)
+  int32_t *seg_first;  // [num_seqs + 1] index of each sequence's first segment; [N]: count
+};
+struct SplitCombineParams {
+  int num_seqs, hv;
+  const int32_t *seg_first;
+  const float *state_in;  // [N, Hv, 128, 128] or NULL (zero)
+  const float *map;       // [segments, Hv, 128, 128] M_s (row index: key)
+  const float *local;     // [segments, Hv, 128, 128] L_s, the final state from zero
+  float *seg_in;          // [segments, Hv, 128, 128] each segment's incoming state
+  float *state_out;       // [N, Hv, 128, 128] the sequence's final state
+};
+cudaError_t launch_split_plan(const SplitPlanParams &p, cudaStream_t stream);
+cudaError_t launch_identity(float *state, long long states, cudaStream_t stream);
+cudaError_t launch_split_combine(const SplitCombineParams &p, cudaStream_t stream);
 
 // Workspace bytes of the bf16 chunk path: a 256-byte header (status word) + slots.
 size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk);

@@ -1,0 +1,130 @@
+// Sequence-split prefill: the helper kernels.  Per block the chunkwise form ("Qwen3.5-9B-npu"
+// model card, section "How it works") is an affine map of the state,
+//     S_{c+1} = M_c S_c + B_c,   M_c = e^{G_C} I - K~^T W,   B_c = K~^T U,
+// (K~ = diag(e^{G_C - G}) K), so a segment of blocks maps its incoming state S through
+// M_s S + L_s, with M_s the product of its blocks' M_c and L_s its final state from a
+// zero start.  A long sequence is cut into segments; the host side (gdn_api.cu) runs
+//   1. every segment from a zero state                        -> L_s
+//   2. every segment with v = 0 from the identity state       -> M_s (B_c = 0 when V = 0)
+//   3. the combine below, in segment order per sequence: S_in(s+1) = M_s S_in(s) + L_s
+//   4. every segment from its S_in(s)                         -> o and the final states
+// with passes 1, 2 and 4 on the ordinary chunked schedules, every segment an independent
+// sequence of their batch.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gdn {
+
+namespace {
+
+// Segment boundaries: sequence n (tokens [bos, eos)) becomes ceil((eos - bos) / seg)
+// segments of seg tokens (the last one shorter); seg_first[n] is the index of its first
+// segment, seg_first[N] the number used; unused entries up to max_segs are empty
+// segments at the end of the token range.  One CTA: thread 0 scans the sequences, then
+// every thread fills boundaries.
+__global__ void __launch_bounds__(256) split_plan_kernel(SplitPlanParams p) {
+  __shared__ int s_used;
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int n = 0; n < p.num_seqs; ++n) {
+      int bos, eos;
+      seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
+      p.seg_first[n] = acc;
+      acc += (eos - bos + p.seg_len - 1) / p.seg_len;
+    }
+    p.seg_first[p.num_seqs] = acc;
+    s_used = acc;
+  }
+  __syncthreads();
+  const int used = s_used;
+  for (int n = threadIdx.x; n < p.num_seqs; n += blockDim.x) {
+    int bos, eos;
+    seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
+    const int first = p.seg_first[n], cnt = p.seg_first[n + 1] - first;
+    for (int j = 0; j < cnt; ++j) p.cu_seg[first + j] = bos + j * p.seg_len;
+  }
+  for (int i = used + threadIdx.x; i <= p.max_segs; i += blockDim.x) p.cu_seg[i] = p.total_tokens;
+}
+
+// state[i][h] = I for every segment i < max_segs and head h (float4 stores)
+__global__ void identity_kernel(float *state, long long count4) {
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < count4;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long flat = 4 * e;
+    const int ij = (int)(flat % (kD * kD)), i = ij / kD, j0 = ij % kD;
+    float4 x;
+    x.x = (i == j0) ? 1.f : 0.f;
+    x.y = (i == j0 + 1) ? 1.f : 0.f;
+    x.z = (i == j0 + 2) ? 1.f : 0.f;
+    x.w = (i == j0 + 3) ? 1.f : 0.f;
+    reinterpret_cast<float4 *>(state)[e] = x;
+  }
+}
+
+constexpr int kCmbCols = 4;  // value columns per combine CTA
+
+// One CTA of 128 threads per (sequence, v-head, 4 value columns): walks the sequence's
+// segments in order with S[:, cols] in shared memory; segment i's incoming state is
+// written to seg_in[i], then S <- M_i S + L_i, thread r forming row r in fp32 on CUDA
+// cores (two partial sums over the keys, so that the step's dependent chain is half as
+// long).  The final S is the sequence's state_out.
+__global__ void __launch_bounds__(kD) split_combine_kernel(SplitCombineParams p) {
+  const int blk = blockIdx.x % (kD / kCmbCols);
+  const int nh = blockIdx.x / (kD / kCmbCols);
+  const int n = nh / p.hv, h = nh - n * p.hv;
+  const int r = threadIdx.x, c0 = blk * kCmbCols;
+  __shared__ __align__(16) float4 sS[kD];  // row k: S[k][c0 .. c0 + 3]
+  const size_t sb = ((size_t)n * p.hv + h) * kD * kD;
+  sS[r] = p.state_in ? *reinterpret_cast<const float4 *>(p.state_in + sb + (size_t)r * kD + c0)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncthreads();
+  const int first = p.seg_first[n], last = p.seg_first[n + 1];
+  for (int i = first; i < last; ++i) {
+    const size_t ib = ((size_t)i * p.hv + h) * kD * kD + (size_t)r * kD;
+    *reinterpret_cast<float4 *>(p.seg_in + ib + c0) = sS[r];
+    const float4 l = *reinterpret_cast<const float4 *>(p.local + ib + c0);
+    float4 a0 = l, a1 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 *Mr = reinterpret_cast<const float4 *>(p.map + ib);  // row r of M_i
+#pragma unroll 4
+    for (int k4 = 0; k4 < kD / 4; ++k4) {
+      const float4 m = Mr[k4];
+      const float4 s0 = sS[4 * k4], s1 = sS[4 * k4 + 1], s2 = sS[4 * k4 + 2], s3 = sS[4 * k4 + 3];
+      a0.x = fmaf(m.x, s0.x, a0.x); a0.y = fmaf(m.x, s0.y, a0.y);
+      a0.z = fmaf(m.x, s0.z, a0.z); a0.w = fmaf(m.x, s0.w, a0.w);
+      a1.x = fmaf(m.y, s1.x, a1.x); a1.y = fmaf(m.y, s1.y, a1.y);
+      a1.z = fmaf(m.y, s1.z, a1.z); a1.w = fmaf(m.y, s1.w, a1.w);
+      a0.x = fmaf(m.z, s2.x, a0.x); a0.y = fmaf(m.z, s2.y, a0.y);
+      a0.z = fmaf(m.z, s2.z, a0.z); a0.w = fmaf(m.z, s2.w, a0.w);
+      a1.x = fmaf(m.w, s3.x, a1.x); a1.y = fmaf(m.w, s3.y, a1.y);
+      a1.z = fmaf(m.w, s3.z, a1.z); a1.w = fmaf(m.w, s3.w, a1.w);
+    }
+    __syncthreads();  // every row of the old S has been read
+    sS[r] = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
+    __syncthreads();
+  }
+  *reinterpret_cast<float4 *>(p.state_out + sb + (size_t)r * kD + c0) = sS[r];
+}
+
+}  // namespace
+
+cudaError_t launch_split_plan(const SplitPlanParams &p, cudaStream_t stream) {
+  split_plan_kernel<<<1, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_identity(float *state, long long states, cudaStream_t stream) {
+  const long long count4 = states * (kD * kD / 4);
+  if (count4 == 0) return cudaSuccess;
+  const long long want = (count4 + 255) / 256;
+  identity_kernel<<<(unsigned)(want < 4096 ? want : 4096), 256, 0, stream>>>(state, count4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_combine(const SplitCombineParams &p, cudaStream_t stream) {
+  const long long units = (long long)p.num_seqs * p.hv * (kD / kCmbCols);
+  if (units == 0) return cudaSuccess;
+  split_combine_kernel<<<(unsigned)units, kD, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

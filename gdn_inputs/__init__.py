@@ -212,6 +212,12 @@ def prefill_t4096_h16() -> Workload:
                     s0_scale=0.1)
 
 
+def long_t65536_h2() -> Workload:
+    """Few heads and one long sequence: H=2, T=65,536, chunk 64, bf16 q/k/v."""
+    return Workload("prefill_B1_H2_T65536_C64", [65536], 2, 2, chunk=64, dtype="bf16",
+                    s0_scale=0.1)
+
+
 def varlen_8seq_hk16_hv32(seed: int = 0) -> Workload:
     """Packed varlen prefill: 8 sequences, lengths U[256, 8192], Hk=16, Hv=32."""
     return Workload("varlen_N8_Hk16_Hv32_C64", varlen_lengths(seed, 8, 256, 8192), 16, 32,

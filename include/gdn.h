@@ -332,6 +332,37 @@ gdn_status gdn_input_prologue(const gdn_shape *shape, const void *q_raw, const v
 gdn_status gdn_gated_rmsnorm(const gdn_shape *shape, const void *o, const void *z,
                              const float *weight, float eps, void *y, void *stream);
 
+/*
+ * Sequence-split prompt pass: the results of gdn_prefill_chunked, for batches with few
+ * (sequence, head) chains and long sequences.  Per block the chunkwise form ("How it
+ * works") maps the state affinely, S -> M S + L with M = e^{G_C} I - (diag(e^{G_C-G}) K)^T W
+ * over the keys, so each sequence is cut into segments of segment_len tokens that run as
+ * independent sequences of one batch, three times over:
+ *   1. from a zero state: each segment's final state L_s;
+ *   2. with v = 0 from the identity state: each segment's map M_s (the product of its
+ *      blocks' maps);
+ *   3. (a combine, in segment order per sequence: S_in(s+1) = M_s S_in(s) + L_s, fp32)
+ *   4. from its incoming state S_in(s): the outputs o.
+ * state_out receives each sequence's final state from step 3.  Each step runs on the
+ * chunked schedules (shape->algo as for gdn_prefill_chunked; GDN_ALGO_RECURRENT is
+ * GDN_ERR_UNSUPPORTED), so the work is about three prompt passes, spread over
+ * segments x heads chains instead of heads.  Pays off when the plain pass leaves most of
+ * the GPU idle (a handful of heads); results within the same bounds as the chunked pass,
+ * not bit-identical to it.
+ * Arguments as for gdn_prefill_chunked, plus segment_len (> 0, a multiple of
+ * shape->chunk); state_out may equal state_in exactly.  workspace: at least
+ * gdn_prefill_split_workspace_size(shape, segment_len) bytes, 256-byte aligned; it holds
+ * the segment boundaries, three sets of per-segment states, a zero v and scratch outputs.
+ * About ten launches, all on `stream`; no synchronisation.
+ */
+gdn_status gdn_prefill_split(const gdn_shape *shape, const void *q, const void *k,
+                             const void *v, const float *g, const float *beta,
+                             const float *state_in, float *state_out,
+                             const int32_t *cu_seqlens, void *o, int32_t segment_len,
+                             void *workspace, size_t workspace_bytes, void *stream);
+/* Workspace bytes of gdn_prefill_split; (size_t)-1 for an invalid shape or segment_len. */
+size_t gdn_prefill_split_workspace_size(const gdn_shape *shape, int32_t segment_len);
+
 /* Workspace bytes `op` (a gdn_op) needs for `shape` (0 when none); (size_t)-1 for an
  * invalid shape or op. */
 size_t gdn_workspace_size(const gdn_shape *shape, int op);

@@ -262,3 +262,35 @@ def test_capture_and_rollback_validation(L):
     assert cr(sh, a4=None) == gdn.GDN_ERR_INVALID_ARG
     assert cr(sh, a0=A + 8) == gdn.GDN_ERR_INVALID_ARG
     assert cr(sh, a5=A + (3 << 20) + 16) == gdn.GDN_ERR_ALIAS
+
+
+def test_split_validation(L):
+    """The sequence-split pass: segment length a positive multiple of the block length,
+    no token loop, a workspace of the size its query returns; every failure before any
+    launch."""
+    sp = L.gdn_prefill_split
+    base = [A, A + (1 << 20), A + (2 << 20), A + (3 << 20), A + (4 << 20), A + (5 << 24),
+            A + (6 << 24), A + (7 << 20), A + (8 << 20)]
+    assert len(base) + 5 == len(sp.argtypes)
+    sh = gdn.make_shape(2, 4096, 1, 2, chunk=64)
+
+    def c(shape, seg=1024, ws=A + (9 << 24), ws_bytes=1 << 40, **kw):
+        args = list(base)
+        for i, v in kw.items():
+            args[int(i[1:])] = v
+        return sp(ctypes.byref(shape), *args, seg, ws, ws_bytes, None)
+    need = gdn.gdn_prefill_split_workspace_size(sh, 1024)
+    # two segments of (4096 / 1024 + 2) sets of states at least
+    assert need > 3 * (4096 // 1024 + 2) * 2 * 128 * 128 * 4
+    for bad_seg in (0, -64, 100):
+        assert c(sh, seg=bad_seg) == gdn.GDN_ERR_INVALID_ARG
+        with pytest.raises(gdn.GdnError):
+            gdn.gdn_prefill_split_workspace_size(sh, bad_seg)
+    rec = gdn.make_shape(2, 4096, 1, 2, chunk=64, algo=gdn.GDN_ALGO_RECURRENT)
+    assert c(rec) == gdn.GDN_ERR_UNSUPPORTED
+    assert c(sh, a7=None) == gdn.GDN_ERR_INVALID_ARG                     # cu_seqlens required
+    assert c(sh, a6=A + (5 << 24) + 4096) == gdn.GDN_ERR_ALIAS           # partly over state_in
+    assert c(sh, ws=None) == gdn.GDN_ERR_WORKSPACE
+    assert c(sh, ws_bytes=need - 1) == gdn.GDN_ERR_WORKSPACE
+    assert c(sh, ws=A + (9 << 24) + 128) == gdn.GDN_ERR_WORKSPACE        # not 256-byte aligned
+    assert c(gdn.make_shape(0, 0, 1, 2, chunk=64)) == gdn.GDN_OK          # nothing to do
