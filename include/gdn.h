@@ -349,9 +349,10 @@ gdn_status gdn_gated_rmsnorm(const gdn_shape *shape, const void *o, const void *
  * segments x heads chains instead of heads.  Pays off when the plain pass leaves most of
  * the GPU idle (a handful of heads); results within the same bounds as the chunked pass,
  * not bit-identical to it.  Sizing: on the two-pass schedule a (segment, head) chain
- * takes 8 CTAs of one SM each, so segments of about T * 8 * num_v_heads / (SM count)
- * tokens (rounded up to shape->chunk) fill the GPU in one wave; e.g. one sequence of
- * 65,536 tokens on 2 heads on 152 SMs: 9 segments of 7,296 tokens.
+ * takes 8 CTAs of one SM each, so P = floor(SM count / (8 * num_v_heads * num_seqs))
+ * segments per sequence fill the GPU in one wave: segment_len = ceil(T / P) rounded up
+ * to shape->chunk; e.g. one sequence of 65,536 tokens on 2 heads on 152 SMs: P = 9,
+ * segments of 7,296 tokens.
  * Arguments as for gdn_prefill_chunked, plus segment_len (> 0, a multiple of
  * shape->chunk); state_out may equal state_in exactly.  workspace: at least
  * gdn_prefill_split_workspace_size(shape, segment_len) bytes, 256-byte aligned; it holds
