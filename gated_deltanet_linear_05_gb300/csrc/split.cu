@@ -61,34 +61,59 @@ __global__ void identity_kernel(float *state, long long count4) {
   }
 }
 
-constexpr int kCmbCols = 4;  // value columns per combine CTA
+constexpr int kCmbCols = 4;     // value columns per combine CTA
+constexpr int kMPitch = kD + 4;  // padded row of a staged map: row r's float4 k lands in
+                                 // bank group (r + k) mod 8, no conflict across 8 lanes
+
+struct CombineSmem {
+  alignas(16) float M[2][kD][kMPitch];  // M_i and M_{i+1} (cp.async double buffer)
+  alignas(16) float4 S[kD];             // row k: S[k][c0 .. c0 + 3]
+};
 
 // One CTA of 128 threads per (sequence, v-head, 4 value columns): walks the sequence's
 // segments in order with S[:, cols] in shared memory; segment i's incoming state is
 // written to seg_in[i], then S <- M_i S + L_i, thread r forming row r in fp32 on CUDA
-// cores (two partial sums over the keys, so that the step's dependent chain is half as
-// long).  The final S is the sequence's state_out.
+// cores (two partial sums over the keys).  M_{i+1} is staged into shared memory by
+// cp.async while step i computes.  The final S is the sequence's state_out.
 __global__ void __launch_bounds__(kD) split_combine_kernel(SplitCombineParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  CombineSmem &sm = *reinterpret_cast<CombineSmem *>(smem_raw);
   const int blk = blockIdx.x % (kD / kCmbCols);
   const int nh = blockIdx.x / (kD / kCmbCols);
   const int n = nh / p.hv, h = nh - n * p.hv;
   const int r = threadIdx.x, c0 = blk * kCmbCols;
-  __shared__ __align__(16) float4 sS[kD];  // row k: S[k][c0 .. c0 + 3]
   const size_t sb = ((size_t)n * p.hv + h) * kD * kD;
-  sS[r] = p.state_in ? *reinterpret_cast<const float4 *>(p.state_in + sb + (size_t)r * kD + c0)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-  __syncthreads();
   const int first = p.seg_first[n], last = p.seg_first[n + 1];
+  auto stage = [&](int i, int buf) {  // M_i into buffer buf, 16-byte pieces along rows
+    const float *src = p.map + ((size_t)i * p.hv + h) * kD * kD;
+    for (int e = r; e < kD * kD / 4; e += kD) {
+      const int row = e >> 5, q4 = e & 31;
+      cp_async16(&sm.M[buf][row][4 * q4], src + (size_t)row * kD + 4 * q4, 16);
+    }
+    cp_async_commit();
+  };
+  if (first < last) stage(first, 0);
+  sm.S[r] = p.state_in ? *reinterpret_cast<const float4 *>(p.state_in + sb + (size_t)r * kD + c0)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
   for (int i = first; i < last; ++i) {
+    const int buf = (i - first) & 1;
+    if (i + 1 < last) {
+      stage(i + 1, buf ^ 1);  // the other buffer's last reader passed the previous barrier
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();  // M_i landed for every thread; S is current
     const size_t ib = ((size_t)i * p.hv + h) * kD * kD + (size_t)r * kD;
-    *reinterpret_cast<float4 *>(p.seg_in + ib + c0) = sS[r];
+    *reinterpret_cast<float4 *>(p.seg_in + ib + c0) = sm.S[r];
     const float4 l = *reinterpret_cast<const float4 *>(p.local + ib + c0);
     float4 a0 = l, a1 = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 *Mr = reinterpret_cast<const float4 *>(p.map + ib);  // row r of M_i
-#pragma unroll 4
+    const float4 *Mr = reinterpret_cast<const float4 *>(&sm.M[buf][r][0]);
+#pragma unroll 8
     for (int k4 = 0; k4 < kD / 4; ++k4) {
       const float4 m = Mr[k4];
-      const float4 s0 = sS[4 * k4], s1 = sS[4 * k4 + 1], s2 = sS[4 * k4 + 2], s3 = sS[4 * k4 + 3];
+      const float4 s0 = sm.S[4 * k4], s1 = sm.S[4 * k4 + 1], s2 = sm.S[4 * k4 + 2],
+                   s3 = sm.S[4 * k4 + 3];
       a0.x = fmaf(m.x, s0.x, a0.x); a0.y = fmaf(m.x, s0.y, a0.y);
       a0.z = fmaf(m.x, s0.z, a0.z); a0.w = fmaf(m.x, s0.w, a0.w);
       a1.x = fmaf(m.y, s1.x, a1.x); a1.y = fmaf(m.y, s1.y, a1.y);
@@ -98,11 +123,11 @@ __global__ void __launch_bounds__(kD) split_combine_kernel(SplitCombineParams p)
       a1.x = fmaf(m.w, s3.x, a1.x); a1.y = fmaf(m.w, s3.y, a1.y);
       a1.z = fmaf(m.w, s3.z, a1.z); a1.w = fmaf(m.w, s3.w, a1.w);
     }
-    __syncthreads();  // every row of the old S has been read
-    sS[r] = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
-    __syncthreads();
+    __syncthreads();  // every row of the old S (and of M_i) has been read
+    sm.S[r] = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
   }
-  *reinterpret_cast<float4 *>(p.state_out + sb + (size_t)r * kD + c0) = sS[r];
+  __syncthreads();
+  *reinterpret_cast<float4 *>(p.state_out + sb + (size_t)r * kD + c0) = sm.S[r];
 }
 
 }  // namespace
@@ -123,7 +148,11 @@ cudaError_t launch_identity(float *state, long long states, cudaStream_t stream)
 cudaError_t launch_split_combine(const SplitCombineParams &p, cudaStream_t stream) {
   const long long units = (long long)p.num_seqs * p.hv * (kD / kCmbCols);
   if (units == 0) return cudaSuccess;
-  split_combine_kernel<<<(unsigned)units, kD, 0, stream>>>(p);
+  const size_t smem = sizeof(CombineSmem);
+  cudaError_t err = cudaFuncSetAttribute(split_combine_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  split_combine_kernel<<<(unsigned)units, kD, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
