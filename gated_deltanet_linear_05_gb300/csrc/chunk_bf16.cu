@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
       ok = mbar_wait(&sm.full[s], (c / kStages) & 1) && ok;
       bar_sync(kBarSReady + par, kPair);
       float R0[2][4], R1[2][4];
-      if (ow < MT) {
+      if (ow < MT && !p.no_out) {
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
             R0[a][e] = (R0[a][e] + R1[a][e]) * EG[16 * ow + 8 * a + 2 * tig + (e & 1)];
       }
       bar_sync(kBarDReady + par, kPair);
-      if (ow < MT) {
+      if (ow < MT && !p.no_out) {
         // O^T += D^T A^T over the causal part (A is zero above the diagonal)
         for (int ks = 0; ks <= ow; ++ks) {
           uint32_t df[4], ba[4];

@@ -84,7 +84,7 @@ size_t chunked_workspace(const gdn_shape *s) {
 }
 
 gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes, void *stream,
-                       float *delta = nullptr, int passes = 0, int u_zero = 0) {
+                       float *delta = nullptr, int passes = 0, int u_zero = 0, int no_out = 0) {
   const gdn_shape *s = c.s;
   if (s->algo == GDN_ALGO_RECURRENT) {  // the token loop
     DecodeParams d{};
@@ -110,6 +110,7 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   p.delta = delta;
   p.passes = passes;
   p.u_zero = u_zero;
+  p.no_out = no_out;
   p.num_seqs = s->num_seqs;
   p.total_tokens = s->total_tokens;
   p.hk = s->num_k_heads;
@@ -249,10 +250,11 @@ gdn_status gdn_prefill_split(const gdn_shape *shape, const void *q, const void *
     if (cudaMemsetAsync(ws + L.v_zero, 0, L.o_scratch - L.v_zero, cs) != cudaSuccess)
       return GDN_ERR_CUDA;
   }
-  // 1. every segment from a zero state: its local final state
-  if ((st = run_chunked(a, inner_ws, inner_bytes, stream, nullptr, run)) != GDN_OK) return st;
+  // 1. every segment from a zero state: its local final state (no outputs needed)
+  if ((st = run_chunked(a, inner_ws, inner_bytes, stream, nullptr, run, 0, shared)) != GDN_OK)
+    return st;
   // 2. every segment with v = 0 from the identity: its map M_s (in place over the identity)
-  if ((st = run_chunked(b, inner_ws, inner_bytes, stream, nullptr, run, shared ? 1 : 0)) != GDN_OK)
+  if ((st = run_chunked(b, inner_ws, inner_bytes, stream, nullptr, run, shared, shared)) != GDN_OK)
     return st;
   // 3. the segments' incoming states in order, and each sequence's final state
   gdn::SplitCombineParams cp{};

@@ -48,6 +48,7 @@ struct ChunkParams {
   // whether pass 2 takes U as zero (the slots of a pass 1 run with these q, k, g, beta)
   int passes;
   int u_zero;
+  int no_out;  // pass 2 writes no output (its output warps keep only their barriers)
 };
 
 // Padded row bytes of 16-bit tiles: 128-element rows and C-element rows.
