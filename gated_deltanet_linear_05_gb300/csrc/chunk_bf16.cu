@@ -485,8 +485,17 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
         if (c >= kStages) ok = mbar_wait(&sm.empty[s], ((c / kStages) - 1) & 1) && ok;
         typename Smem::Stage &st = sm.st[s];
         const char *src = slot0 + (size_t)c * slot_bytes(C);
-        mbar_arrive_expect_tx(&sm.full[s], kStageTx);
-        bulk_g2s(st.H, src, kHeadB, &sm.full[s]);
+        if (p.no_out) {  // the chain's operands only: W^T, K and the decays (not q, A)
+          constexpr uint32_t kWB = (uint32_t)slot_q_off(C), kKB = (uint32_t)(C * kP128);
+          constexpr uint32_t kDB = (uint32_t)(12 * C);
+          mbar_arrive_expect_tx(&sm.full[s], kWB + kKB + kDB + kUB);
+          bulk_g2s(st.H, src, kWB, &sm.full[s]);
+          bulk_g2s(st.H + slot_k_off(C), src + slot_k_off(C), kKB, &sm.full[s]);
+          bulk_g2s(st.H + slot_dec_off(C), src + slot_dec_off(C), kDB, &sm.full[s]);
+        } else {
+          mbar_arrive_expect_tx(&sm.full[s], kStageTx);
+          bulk_g2s(st.H, src, kHeadB, &sm.full[s]);
+        }
         bulk_g2s(st.U, src + slot_u_off(C) + (size_t)blk * kDVB * RC, kUB, &sm.full[s]);
       }
       // the last copies are consumed before the CTA's final barrier
