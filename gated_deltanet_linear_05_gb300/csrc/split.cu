@@ -106,8 +106,9 @@ __global__ void __launch_bounds__(kD) split_combine_kernel(SplitCombineParams p)
     __syncthreads();  // M_i landed for every thread; S is current
     const size_t ib = ((size_t)i * p.hv + h) * kD * kD + (size_t)r * kD;
     *reinterpret_cast<float4 *>(p.seg_in + ib + c0) = sm.S[r];
+    // L_i's row is added last, so that its load overlaps the products
     const float4 l = *reinterpret_cast<const float4 *>(p.local + ib + c0);
-    float4 a0 = l, a1 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
     const float4 *Mr = reinterpret_cast<const float4 *>(&sm.M[buf][r][0]);
 #pragma unroll 8
     for (int k4 = 0; k4 < kD / 4; ++k4) {
@@ -124,7 +125,8 @@ __global__ void __launch_bounds__(kD) split_combine_kernel(SplitCombineParams p)
       a1.z = fmaf(m.w, s3.z, a1.z); a1.w = fmaf(m.w, s3.w, a1.w);
     }
     __syncthreads();  // every row of the old S (and of M_i) has been read
-    sm.S[r] = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
+    sm.S[r] = make_float4(a0.x + a1.x + l.x, a0.y + a1.y + l.y, a0.z + a1.z + l.z,
+                          a0.w + a1.w + l.w);
   }
   __syncthreads();
   *reinterpret_cast<float4 *>(p.state_out + sb + (size_t)r * kD + c0) = sm.S[r];
