@@ -260,11 +260,11 @@ def run_gdn(args):
                    "l2": "flushed (512 MiB write) before every timed step",
                    "parallelism": "dp%d (independent batches per GPU)" % world},
         # traffic: DRAM bytes of the step's two kernels from the committed ncu capture
-        # (prep 94.7 MB + recur 92.2 MB; ncu flushes caches between kernels, so the
+        # (prep 94.1 MB + recur 88.5 MB; ncu flushes caches between kernels, so the
         # workspace round trip counts as DRAM traffic there)
         "roofline": roofline("hbm", gbs, pk["hbm"], "GB/s", traffic=182.6e6),
         "roofline_scope": "one gdn_prefill_chunked call (pass 1 + pass 2); the dominant "
-                          "kernel, pass 2, takes 55.5 of its ~100 us",
+                          "kernel, pass 2, takes 57 of its ~97 us",
         "tensor": {"achieved": round(tfs, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                    "frac": round(tfs / pk["bf16"], 4), "algorithmic_flops": flops},
         "algorithmic_bytes": byts,
