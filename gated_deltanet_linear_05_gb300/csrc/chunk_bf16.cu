@@ -485,17 +485,8 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
         if (c >= kStages) ok = mbar_wait(&sm.empty[s], ((c / kStages) - 1) & 1) && ok;
         typename Smem::Stage &st = sm.st[s];
         const char *src = slot0 + (size_t)c * slot_bytes(C);
-        if (p.no_out) {  // the chain's operands only: W^T, K and the decays (not q, A)
-          constexpr uint32_t kWB = (uint32_t)slot_q_off(C), kKB = (uint32_t)(C * kP128);
-          constexpr uint32_t kDB = (uint32_t)(12 * C);
-          mbar_arrive_expect_tx(&sm.full[s], kWB + kKB + kDB + kUB);
-          bulk_g2s(st.H, src, kWB, &sm.full[s]);
-          bulk_g2s(st.H + slot_k_off(C), src + slot_k_off(C), kKB, &sm.full[s]);
-          bulk_g2s(st.H + slot_dec_off(C), src + slot_dec_off(C), kDB, &sm.full[s]);
-        } else {
-          mbar_arrive_expect_tx(&sm.full[s], kStageTx);
-          bulk_g2s(st.H, src, kHeadB, &sm.full[s]);
-        }
+        mbar_arrive_expect_tx(&sm.full[s], kStageTx);
+        bulk_g2s(st.H, src, kHeadB, &sm.full[s]);
         bulk_g2s(st.U, src + slot_u_off(C) + (size_t)blk * kDVB * RC, kUB, &sm.full[s]);
       }
       // the last copies are consumed before the CTA's final barrier
@@ -543,8 +534,8 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
           for (int hr = 0; hr < 2; ++hr) {
             const float2 u = f16x2_to_float2(*reinterpret_cast<const uint32_t *>(
                 st.U + (gid + 8 * hr) * RC + 2 * (16 * w + 8 * a + 2 * tig)));
-            D0[a][2 * hr] = p.u_zero ? 0.f : u.x;
-            D0[a][2 * hr + 1] = p.u_zero ? 0.f : u.y;
+            D0[a][2 * hr] = u.x;
+            D0[a][2 * hr + 1] = u.y;
             D1[a][2 * hr] = D1[a][2 * hr + 1] = 0.f;
           }
 #pragma unroll
@@ -632,7 +623,7 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
       ok = mbar_wait(&sm.full[s], (c / kStages) & 1) && ok;
       bar_sync(kBarSReady + par, kPair);
       float R0[2][4], R1[2][4];
-      if (ow < MT && !p.no_out) {
+      if (ow < MT) {
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -657,7 +648,7 @@ __global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
             R0[a][e] = (R0[a][e] + R1[a][e]) * EG[16 * ow + 8 * a + 2 * tig + (e & 1)];
       }
       bar_sync(kBarDReady + par, kPair);
-      if (ow < MT && !p.no_out) {
+      if (ow < MT) {
         // O^T += D^T A^T over the causal part (A is zero above the diagonal)
         for (int ks = 0; ks <= ow; ++ks) {
           uint32_t df[4], ba[4];
@@ -719,6 +710,224 @@ cudaError_t launch_recur(const ChunkParams &p, long long heads, cudaStream_t str
   return cudaLaunchKernelEx(&cfg, recur_kernel<C, TO>, p);
 }
 
+// ================================================================== split: state chains
+// The sequence split's runs from zero (-> L_s) and from the identity with U = 0 (-> M_s)
+// need only pass 2's state chain.  One launch covers both: CTAs [0, heads * 8) walk the
+// L chains, the next heads * 8 the M chains (state_in2 / state_out2, U taken as zero).
+// A CTA is the 4 chain warps of recur_kernel plus its producer warp, with a 2-stage ring
+// of the chain's operands only (W^T, K, the decays and this CTA's U columns: 38 KB per
+// block at C = 64) and one snapshot buffer (no output warps read it): ~99 KB of shared
+// memory, so two CTAs share an SM and both kinds of chain run in one wave.
+constexpr int kChThreads = 32 * (kChainWarps + 1);
+constexpr int kChStages = 2;
+
+template <int C>
+struct ChainSmem {
+  static constexpr int RC = row_c(C);
+  struct Stage {
+    alignas(128) char W[slot_q_off(C)];  // W^T, as in the slot
+    alignas(16) char K[C * kP128];       // the block's k rows (fp16)
+    alignas(16) float DEC[3 * C];        // G, e^G, e^(G_C - G)
+    alignas(16) char U[kDVB * RC];       // U^T rows of this CTA's value columns
+  } st[kChStages];
+  alignas(8) uint64_t full[kChStages], empty[kChStages];
+  alignas(16) char Sn[kDVB * kP128];  // S_c^T (fp16) [16 value cols][128 keys]
+  alignas(16) char Dd[kDVB * RC];     // (D diag(e^(G_C - G)))^T (fp16)
+  alignas(16) float S32[kD][kDVB + 4];
+};
+
+template <int C>
+__global__ void __launch_bounds__(kChThreads) split_chain_kernel(ChunkParams p) {
+  constexpr int NB = kD / kDVB, MT = C / 16, RC = row_c(C);
+  constexpr uint32_t kWB = (uint32_t)slot_q_off(C), kKB = (uint32_t)(C * kP128);
+  constexpr uint32_t kDB = (uint32_t)(12 * C), kUB = (uint32_t)(kDVB * RC);
+  using Smem = ChainSmem<C>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const long long half = (long long)p.num_seqs * p.hv * NB;
+  const bool maps = (long long)blockIdx.x >= half;
+  const long long b = maps ? (long long)blockIdx.x - half : (long long)blockIdx.x;
+  const int blk = (int)(b % NB);
+  const int nh = (int)(b / NB);
+  const int n = nh / p.hv;
+  const int h = nh - n * p.hv;
+  const float *s_in = maps ? p.state_in2 : p.state_in;
+  float *s_out = maps ? p.state_out2 : p.state_out;
+
+  int bos, eos;
+  seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
+  const int nchunks = (eos - bos + C - 1) / C;
+  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD + blk * kDVB;
+  const char *slot0 = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, 0)) * slot_bytes(C);
+
+  if (tid == 0) {
+    for (int s = 0; s < kChStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    mbar_fence_init();
+  }
+  for (int e = tid; e < kD * kDVB / 4; e += kChThreads) {
+    const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
+    const float4 val =
+        s_in ? *reinterpret_cast<const float4 *>(s_in + sbase + (size_t)i * kD + 4 * c4)
+             : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4 *>(&sm.S32[i][4 * c4]) = val;
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // pass 1's slots are complete
+
+  if (warp == kChainWarps) {
+    // ---- producer: the chain's operands of each block into the ring
+    if (lane == 0) {
+      bool ok = true;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kChStages;
+        if (c >= kChStages) ok = mbar_wait(&sm.empty[s], ((c / kChStages) - 1) & 1) && ok;
+        typename Smem::Stage &st = sm.st[s];
+        const char *src = slot0 + (size_t)c * slot_bytes(C);
+        mbar_arrive_expect_tx(&sm.full[s], kWB + kKB + kDB + kUB);
+        bulk_g2s(st.W, src, kWB, &sm.full[s]);
+        bulk_g2s(st.K, src + slot_k_off(C), kKB, &sm.full[s]);
+        bulk_g2s(st.DEC, src + slot_dec_off(C), kDB, &sm.full[s]);
+        bulk_g2s(st.U, src + slot_u_off(C) + (size_t)blk * kDVB * RC, kUB, &sm.full[s]);
+      }
+      if (!ok) atomicExch(p.err, 1);
+    }
+  } else {
+    // ---- chain warp w: D for tokens 16w .. 16w+15, the state for keys 32w .. 32w+31
+    const int w = warp;
+    float Sa[4][4];  // S^T[j][i], j = gid (+8), i = 32w + 8nt + 2tig (+1)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        Sa[nt][e] = sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)];
+    auto write_snapshot = [&]() {
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int j = gid + 8 * hr, i = 32 * w + 8 * nt + 2 * tig;
+          *reinterpret_cast<uint32_t *>(sm.Sn + j * kP128 + 2 * i) =
+              pack_f16(Sa[nt][2 * hr], Sa[nt][2 * hr + 1]);
+        }
+    };
+    write_snapshot();
+    bar_sync(kBarChain, kChain);
+
+    bool ok = true;
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kChStages;
+      typename Smem::Stage &st = sm.st[s];
+      const float *EG = st.DEC + C, *ED = st.DEC + 2 * C;
+      ok = mbar_wait(&sm.full[s], (c / kChStages) & 1) && ok;
+
+      if (w < MT) {
+        // D^T = U^T - S^T W^T for tokens 16w .. 16w+15 (U = 0 for the map chains)
+        float D0[2][4], D1[2][4];
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const float2 u = f16x2_to_float2(*reinterpret_cast<const uint32_t *>(
+                st.U + (gid + 8 * hr) * RC + 2 * (16 * w + 8 * a + 2 * tig)));
+            D0[a][2 * hr] = maps ? 0.f : u.x;
+            D0[a][2 * hr + 1] = maps ? 0.f : u.y;
+            D1[a][2 * hr] = D1[a][2 * hr + 1] = 0.f;
+          }
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          uint32_t nf[4], bw[4];
+          lda_p<kP128>(nf, sm.Sn, 0, 16 * ks, lane);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) nf[e] ^= 0x80008000u;  // -S
+          ldb_kn_p<RC>(bw, st.W, 16 * ks, 16 * w, lane);
+          if (ks & 1) {
+            mma_f16(D1[0], nf, bw[0], bw[1]);
+            mma_f16(D1[1], nf, bw[2], bw[3]);
+          } else {
+            mma_f16(D0[0], nf, bw[0], bw[1]);
+            mma_f16(D0[1], nf, bw[2], bw[3]);
+          }
+        }
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int j = gid + 8 * hr, t = 16 * w + 8 * a + 2 * tig;
+            const float d0 = D0[a][2 * hr] + D1[a][2 * hr], d1 = D0[a][2 * hr + 1] + D1[a][2 * hr + 1];
+            *reinterpret_cast<uint32_t *>(sm.Dd + j * RC + 2 * t) = pack_f16(d0 * ED[t], d1 * ED[t + 1]);
+          }
+      }
+      bar_sync(kBarChain, kChain);  // Dd complete; every warp is done reading the snapshot
+
+      // S^T <- e^(G_C) S^T + Dd^T K over keys 32w .. 32w+31
+      {
+        float X[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) X[a][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < MT; ++ks) {
+          uint32_t df[4];
+          lda_p<RC>(df, sm.Dd, 0, 16 * ks, lane);
+#pragma unroll
+          for (int np = 0; np < 2; ++np) {
+            uint32_t bk[4];
+            ldb_kn_p<kP128>(bk, st.K, 16 * ks, 32 * w + 16 * np, lane);
+            mma_f16(X[2 * np], df, bk[0], bk[1]);
+            mma_f16(X[2 * np + 1], df, bk[2], bk[3]);
+          }
+        }
+        const float egc = EG[C - 1];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) Sa[nt][e] = fmaf(egc, Sa[nt][e], X[nt][e]);
+      }
+      write_snapshot();
+      bar_sync(kBarChain, kChain);  // the new snapshot is complete; Dd and the stage are free
+      if (tid == 0) mbar_arrive(&sm.empty[s]);
+    }
+    if (!ok && lane == 0) atomicExch(p.err, 1);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)] = Sa[nt][e];
+  }
+  __syncthreads();
+  for (int e = tid; e < kD * kDVB / 4; e += kChThreads) {
+    const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
+    *reinterpret_cast<float4 *>(s_out + sbase + (size_t)i * kD + 4 * c4) =
+        *reinterpret_cast<const float4 *>(&sm.S32[i][4 * c4]);
+  }
+}
+
+template <int C>
+cudaError_t launch_split_chains(const ChunkParams &p, long long heads, cudaStream_t stream) {
+  const size_t sz = sizeof(ChainSmem<C>);
+  cudaError_t err = cudaFuncSetAttribute(split_chain_kernel<C>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sz);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * heads * (kD / kDVB)));
+  cfg.blockDim = dim3(kChThreads);
+  cfg.dynamicSmemBytes = sz;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, split_chain_kernel<C>, p);
+}
+
 template <int C>
 cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
   int dev = 0, sms = 148;
@@ -732,7 +941,7 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
   long long per_head = (8LL * sms + heads - 1) / heads;
   per_head = max(1LL, min(per_head, max(1LL, max_chunks)));
 
-  if (p.total_tokens > 0 && p.passes != 2) {
+  if (p.total_tokens > 0 && p.passes != 2 && p.passes != 3) {
     const size_t s1 = sizeof(PrepSmem<C>);
     err = cudaFuncSetAttribute(prep_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
     if (err != cudaSuccess) return err;
@@ -741,6 +950,7 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
   }
   if (p.passes == 1) return cudaSuccess;
+  if (p.passes == 3) return launch_split_chains<C>(p, heads, stream);
   return p.o_fp32 ? launch_recur<C, float>(p, heads, stream)
                   : launch_recur<C, __nv_bfloat16>(p, heads, stream);
 }

@@ -84,7 +84,8 @@ size_t chunked_workspace(const gdn_shape *s) {
 }
 
 gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes, void *stream,
-                       float *delta = nullptr, int passes = 0, int u_zero = 0, int no_out = 0) {
+                       float *delta = nullptr, int passes = 0,
+                       const float *state_in2 = nullptr, float *state_out2 = nullptr) {
   const gdn_shape *s = c.s;
   if (s->algo == GDN_ALGO_RECURRENT) {  // the token loop
     DecodeParams d{};
@@ -109,8 +110,8 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   ChunkParams p{};
   p.delta = delta;
   p.passes = passes;
-  p.u_zero = u_zero;
-  p.no_out = no_out;
+  p.state_in2 = state_in2;
+  p.state_out2 = state_out2;
   p.num_seqs = s->num_seqs;
   p.total_tokens = s->total_tokens;
   p.hk = s->num_k_heads;
@@ -237,8 +238,8 @@ gdn_status gdn_prefill_split(const gdn_shape *shape, const void *q, const void *
   if (gdn::launch_identity(ident, (long long)L.max_segs * shape->num_v_heads, cs) != cudaSuccess)
     return GDN_ERR_CUDA;
   // On the bf16 two-pass schedule the three runs share one pass 1 (its slots depend on q,
-  // k, v, g, beta only), and the map run's pass 2 takes U as zero; other schedules run in
-  // full, the map run on a zero v.
+  // k, v, g, beta only), and runs 1 and 2 are one launch of state chains (U taken as zero
+  // for the maps); other schedules run in full, the map run on a zero v.
   const bool shared = shape->qkv_dtype == GDN_BF16 && !single_pass(&L.inner_shape);
   Common a{&L.inner_shape, q, k, v, g, beta, nullptr, local, cu_seg, ws + L.o_scratch};
   Common b{&L.inner_shape, q, k, ws + L.v_zero, g, beta, ident, ident, cu_seg, ws + L.o_scratch};
@@ -250,12 +251,17 @@ gdn_status gdn_prefill_split(const gdn_shape *shape, const void *q, const void *
     if (cudaMemsetAsync(ws + L.v_zero, 0, L.o_scratch - L.v_zero, cs) != cudaSuccess)
       return GDN_ERR_CUDA;
   }
-  // 1. every segment from a zero state: its local final state (no outputs needed)
-  if ((st = run_chunked(a, inner_ws, inner_bytes, stream, nullptr, run, 0, shared)) != GDN_OK)
-    return st;
-  // 2. every segment with v = 0 from the identity: its map M_s (in place over the identity)
-  if ((st = run_chunked(b, inner_ws, inner_bytes, stream, nullptr, run, shared, shared)) != GDN_OK)
-    return st;
+  if (shared) {
+    // 1 and 2 in one launch of state chains: every segment from a zero state (its local
+    // final state L_s) and, with U = 0, from the identity (its map M_s, in place)
+    if ((st = run_chunked(a, inner_ws, inner_bytes, stream, nullptr, 3, ident, ident)) != GDN_OK)
+      return st;
+  } else {
+    // 1. every segment from a zero state: its local final state
+    if ((st = run_chunked(a, inner_ws, inner_bytes, stream)) != GDN_OK) return st;
+    // 2. every segment with v = 0 from the identity: its map M_s (in place over the identity)
+    if ((st = run_chunked(b, inner_ws, inner_bytes, stream)) != GDN_OK) return st;
+  }
   // 3. the segments' incoming states in order, and each sequence's final state
   gdn::SplitCombineParams cp{};
   cp.num_seqs = shape->num_seqs;

@@ -44,11 +44,12 @@ struct ChunkParams {
   int nslots;
   char *slot_ws;      // Hv * nslots slots of slot_bytes(C) bytes, 128-byte aligned
   int *err;           // device status word: nonzero if a kernel wait timed out
-  // Two-pass path only: which passes to run (1: pass 1, 2: pass 2, else both), and
-  // whether pass 2 takes U as zero (the slots of a pass 1 run with these q, k, g, beta)
+  // Two-pass path only: which passes to run (1: pass 1, 2: pass 2, 3: the sequence
+  // split's state chains -- from state_in, and with U = 0 from state_in2 -- on the slots
+  // of a pass 1 run with these q, k, v, g, beta; else both passes)
   int passes;
-  int u_zero;
-  int no_out;  // pass 2 writes no output (its output warps keep only their barriers)
+  const float *state_in2;
+  float *state_out2;
 };
 
 // Padded row bytes of 16-bit tiles: 128-element rows and C-element rows.
