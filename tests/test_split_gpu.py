@@ -102,3 +102,13 @@ def test_long_single_head_sequence():
     x = gi.make_inputs(wl, seed=36)
     o, s = _split(x, wl, 1024)
     _check(o, s, *_ref(x), "bf16", "T=16384")
+
+
+@pytest.mark.slow
+def test_bench_configuration():
+    """The configuration the bench times: one sequence of 65,536 tokens on 2 heads in
+    9 segments of 7,296 tokens (two-pass inner schedule, one chain-only launch)."""
+    wl = gi.long_t65536_h2()
+    x = gi.make_inputs(wl)
+    o, s = _split(x, wl, 7296)
+    _check(o, s, *_ref(x), "bf16", "T=65536, H=2")
