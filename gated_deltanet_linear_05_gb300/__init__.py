@@ -208,15 +208,34 @@ def gdn_prefill_chunked(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=Non
                  cu_seqlens, o, chunk, workspace, stream, algo)
 
 
+def split_segment_len(num_seqs: int, num_v_heads: int, tokens_per_seq: int, chunk: int = 64,
+                      sms: int = 152) -> int:
+    """Segment length that fills the GPU in one wave on the two-pass schedule: each
+    (segment, v-head) chain takes 8 CTAs of one SM, so P = sms // (8 * num_seqs *
+    num_v_heads) segments per sequence (at least 1) and segment_len = ceil(T / P)
+    rounded up to a multiple of chunk."""
+    if num_seqs <= 0 or num_v_heads <= 0 or chunk <= 0:
+        raise ValueError("num_seqs, num_v_heads and chunk must be positive")
+    p = max(1, sms // (8 * num_seqs * num_v_heads))
+    seg = -(-max(1, tokens_per_seq) // p)
+    return -(-seg // chunk) * chunk
+
+
 def gdn_prefill_split(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,
-                      segment_len: int = 1024, chunk: int = 64, workspace=None, stream=None,
+                      segment_len=None, chunk: int = 64, workspace=None, stream=None,
                       algo: int = GDN_ALGO_AUTO):
     """Sequence-split prompt pass: the results of gdn_prefill_chunked, each sequence cut
     into segments of segment_len tokens (a multiple of chunk) that run side by side.
+    segment_len None: split_segment_len for the device's SM count and the longest
+    sequence the shapes allow (total tokens / sequences, rounded up).
     Returns (o, state_out)."""
     torch = _torch()
     if o is None:
         o = torch.empty_like(v)
+    if segment_len is None:
+        n = cu_seqlens.numel() - 1
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        segment_len = split_segment_len(n, v.shape[1], -(-q.shape[0] // max(1, n)), chunk, sms)
     _check_tensors(q, k, v, g, beta, state_in, state_out, cu_seqlens, o, workspace)
     shape = _shape_of(q, v, o, state_out, cu_seqlens, chunk, algo)
     need = gdn_prefill_split_workspace_size(shape, segment_len)

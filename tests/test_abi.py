@@ -294,3 +294,19 @@ def test_split_validation(L):
     assert c(sh, ws_bytes=need - 1) == gdn.GDN_ERR_WORKSPACE
     assert c(sh, ws=A + (9 << 24) + 128) == gdn.GDN_ERR_WORKSPACE        # not 256-byte aligned
     assert c(gdn.make_shape(0, 0, 1, 2, chunk=64)) == gdn.GDN_OK          # nothing to do
+
+
+def test_split_segment_rule():
+    """The binding's segment-length rule (one wave of two-pass chains)."""
+    f = gdn.split_segment_len
+    assert f(1, 2, 65536) == 7296          # 9 segments of 114 blocks on 152 SMs
+    assert f(1, 1, 16384) == 896           # 19 segments
+    assert f(1, 16, 4096) == 4096          # 16 heads fill the GPU already: one segment
+    assert f(2, 2, 1000, chunk=16) == 256  # 4 segments, rounded up to the block length
+    assert f(1, 2, 65536) % 64 == 0
+    for n, hv, t in [(1, 2, 65536), (1, 1, 16384), (3, 1, 5000)]:
+        seg = f(n, hv, t)
+        segs = -(-t // seg)
+        assert segs * n * hv * 8 <= 152 or segs == 1
+    with pytest.raises(ValueError):
+        f(0, 2, 100)
