@@ -86,6 +86,22 @@ def test_in_place_and_zero_state():
     _check(o, s, *_ref(x, state_in=False), "bf16", "zero state")
 
 
+def test_default_segment_length():
+    """segment_len None: the binding's one-wave rule for the device (3000 tokens on 2 heads:
+    9 segments of 384 tokens on 152 SMs)."""
+    import torch
+    import gated_deltanet_linear_05_gb300 as gdn
+    wl = gi.Workload("split7", [3000], 1, 2, chunk=64, dtype="bf16", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=37)
+    d = device_inputs(x, "bf16")
+    s_out = torch.full_like(d["state0"], float("nan"))
+    o = torch.full(d["v"].shape, float("nan"), device="cuda", dtype=torch.float32)
+    gdn.gdn_prefill_split(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state0"], s_out,
+                          d["cu_seqlens"], o)
+    torch.cuda.synchronize()
+    _check(to_np(o), to_np(s_out), *_ref(x), "bf16", "default segments")
+
+
 def test_segment_longer_than_the_sequences():
     """One segment per sequence: the map of step 2 is applied to the incoming state, and
     the outputs come from the plain chunked pass of step 4."""
