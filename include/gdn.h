@@ -345,8 +345,9 @@ gdn_status gdn_gated_rmsnorm(const gdn_shape *shape, const void *o, const void *
  *   4. from its incoming state S_in(s): the outputs o.
  * state_out receives each sequence's final state from step 3.  Each step runs on the
  * chunked schedules (shape->algo as for gdn_prefill_chunked; GDN_ALGO_RECURRENT is
- * GDN_ERR_UNSUPPORTED), so the work is about three prompt passes, spread over
- * segments x heads chains instead of heads.  Pays off when the plain pass leaves most of
+ * GDN_ERR_UNSUPPORTED), so the work is about three state chains per segment (with one
+ * shared pass 1 on the bf16 two-pass schedule), spread over segments x heads chains
+ * instead of heads.  Pays off when the plain pass leaves most of
  * the GPU idle (a handful of heads); results within the same bounds as the chunked pass,
  * not bit-identical to it.  Sizing: on the two-pass schedule a (segment, head) chain
  * takes 8 CTAs of one SM each, so P = floor(SM count / (8 * num_v_heads * num_seqs))
@@ -357,7 +358,9 @@ gdn_status gdn_gated_rmsnorm(const gdn_shape *shape, const void *o, const void *
  * shape->chunk); state_out may equal state_in exactly.  workspace: at least
  * gdn_prefill_split_workspace_size(shape, segment_len) bytes, 256-byte aligned; it holds
  * the segment boundaries, three sets of per-segment states, a zero v and scratch outputs.
- * About ten launches, all on `stream`; no synchronisation.
+ * Six launches on the bf16 two-pass schedule (segment plan, identity states, pass 1,
+ * the state chains of steps 1 and 2 together, the combine, pass 2), a few more on the
+ * other schedules; all on `stream`, no synchronisation.
  */
 gdn_status gdn_prefill_split(const gdn_shape *shape, const void *q, const void *k,
                              const void *v, const float *g, const float *beta,
