@@ -13,25 +13,24 @@
 //     of I + N by forward substitution, and W and U by blocked forward substitution
 //     over the 16-token blocks, X_i = T_ii (R_i - sum_{j<i} N_ij X_j) -- the same
 //     triangular solve as the block inverse of the page, applied to the right-hand
-//     sides instead of forming (I + N)^-1.  Each block's W^T, fp16 q and k rows, A,
-//     decays and U^T go to its own workspace slot in the padded shared-memory layout
-//     pass 2 reads.
-//   pass 2 (recur_kernel, one CTA per (sequence, v-head, 16 value columns)): walks the
+//     sides instead of forming (I + N)^-1.  Each block's -W, K~^T = (diag(e^(G_C - G)) K)^T,
+//     A, U and decays go to its own workspace slot, in the orientation pass 2 loads
+//     straight into its tensor-core fragments.
+//   pass 2 (chain_kernel, one CTA per (sequence, v-head, 16 value columns)): walks the
 //     blocks of the sequence in order with the state block S[:, cols] in fp32 registers
-//     (read from state_in once, written to state_out once).  A producer warp streams
-//     each block's slot part into a 2-stage shared-memory ring with two bulk (TMA)
-//     copies signalled on mbarriers.  Eight compute warps each own 8 tokens of the
-//     block for
-//       D^T = U^T - S^T W^T   and   R^T = S^T Q^T   (sharing the S^T fragments),
-//     exchange D once through shared memory, then each carries 16 keys of the state,
-//       S^T <- exp(G_T) S^T + (D^T diag(exp(G_T - G))) K,
-//     and finishes its tokens' outputs O^T = diag(e^G) R^T + D^T A^T.
+//     (read from state_in once, written to state_out once): D = U - W S and
+//     S <- e^(G_C) S + K~^T D per block, exporting each block's S_c and D_c (fp16).
+//   pass 3 (out_kernel, one CTA per (v-head, block), all in parallel): the block outputs
+//     O = diag(e^G) Q S_c + A D_c.
 // Tensor-core products (mma.sync) take fp16 operands with fp32 accumulation: bf16 q, k
-// and v enter exactly (converted to fp16), the state, D, T, W and A are rounded to fp16
-// (11 significant bits) for the products only; the state itself, the sums and every
+// and v enter exactly (converted to fp16), the state, D, T, W, A and K~ are rounded to
+// fp16 (11 significant bits) for the products only; the state itself, the sums and every
 // decay are fp32.  Decay factors between two tokens are always the exp of a difference
 // of cumsums.  A partly filled block is padded with g = 0, beta = 0 and zero q/k/v rows
 // (token_valid), which leaves the state exactly as after the sequence's last token.
+#include <cuda.h>
+#include <string.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -53,6 +52,41 @@ __device__ __forceinline__ void acc_to_f16(const float (&x)[4], const float (&y)
   a[3] = pack_f16(y[2] * t0, y[3] * t1);
 }
 
+// Contractions over the keys and over the tokens in pass 2 take the k index in a
+// permuted order: in every span of 32 (for C = 16: 16) indices, lane (gid, tig) supplies
+// the consecutive indices span + 8tig .. +7 (4tig .. +3), elements {4e, 4e+1} as the k
+// pair (2tig, 2tig+1) and {4e+2, 4e+3} as (2tig+8, 2tig+9) of the span's k-step e.  A and
+// B of every product use the same order, so the products are unchanged and each lane
+// reads one contiguous run per row.
+template <int C>
+struct TokSpan {
+  static constexpr int SPAN = C < 32 ? C : 32;  // tokens per span
+  static constexpr int NSP = C / SPAN;          // spans per block
+  static constexpr int KW = SPAN / 8;           // 32-bit words per lane and row run
+  static constexpr int KS = SPAN / 16;          // k-steps per span
+};
+
+// Fragment order of the slot's -W, K~^T and U: the chain kernel loads each group of 32
+// lane runs (512 bytes, or 256 for C = 16) with one coalesced warp instruction.  Groups,
+// lane = 4 gid + tig:
+//   WN (chain warp w < C/16, key span s < 4, row half rh): lane's run = -W row
+//      16w + gid + 8rh, keys 32s + 8tig .. +7                                   (16 B)
+//   KT (chain warp w < 4, key tile nt < 4, token span s): K~^T row 32w + 8nt + gid, the
+//      lane's token run of span s                                              (4 KW B)
+//   U  (value-column block b < 8, chain warp w < C/16): the words U[16w + gid + 8rh]
+//      [16b + 8nt + 2tig, +1] for (nt, rh) = (0,0), (0,1), (1,0), (1,1)       (16 B)
+__device__ __forceinline__ int wn_off(int w, int s, int rh, int lane) {
+  return (((w * 4 + s) * 2 + rh) * 32 + lane) * 16;
+}
+template <int C>
+__device__ __forceinline__ int kt_off(int w, int nt, int s, int lane) {
+  using TS = TokSpan<C>;
+  return (((w * 4 + nt) * TS::NSP + s) * 32 + lane) * (4 * TS::KW);
+}
+template <int C>
+__device__ __forceinline__ int u_off(int b, int w, int lane) {
+  return ((b * (C / 16) + w) * 32 + lane) * 16;
+}
 // ================================================================== pass 1
 
 template <int C>
@@ -85,10 +119,6 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
   const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
   const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
   const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
-  if (blockIdx.x == 0 && tid == 0) *p.err = 0;
-  // pass 2 may be scheduled now (programmatic dependent launch): its CTAs set up on SMs
-  // that pass 1 has left and wait for pass 1's completion before reading any slot
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   int bos, eos;
   seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
@@ -99,8 +129,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
     const int tok0 = bos + c * C;
     const int L = min(C, eos - tok0);
     char *slot = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, c)) * slot_bytes(C);
-    char *w_out = slot, *a_out = slot + slot_a_off(C), *u_out = slot + slot_u_off(C);
-    char *q_out = slot + slot_q_off(C), *k_out = slot + slot_k_off(C);
+    char *wn_out = slot, *kt_out = slot + slot_kt_off(C), *a_out = slot + slot_a_off(C);
+    char *u_out = slot + slot_u_off(C);
     float *dec_out = reinterpret_cast<float *>(slot + slot_dec_off(C));
     __syncthreads();  // the previous block is done with shared memory
 
@@ -281,24 +311,23 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
       }
     }
     // the A tile's upper 16x16 blocks (never computed) are zero: MT (MT - 1) / 2 tiles of
-    // 16 rows x two 16-byte halves
-    for (int e = tid; e < 16 * MT * (MT - 1); e += NT) {
-      const int tile = e >> 5, row = (e >> 1) & 15, hh = e & 1;
+    // 16 rows x 8 column pairs
+    for (int e = tid; e < 64 * MT * (MT - 1); e += NT) {
+      const int tile = e >> 7, row = (e >> 3) & 15, pr = e & 7;
       int mt = 0, np = 1, cnt = tile;  // tile -> (mt, np > mt), row-major over the upper part
       while (cnt >= MT - 1 - mt) {
         cnt -= MT - 1 - mt;
         ++mt;
       }
       np = mt + 1 + cnt;
-      *reinterpret_cast<uint4 *>(a_out + (16 * mt + row) * RC + 2 * (16 * np + 8 * hh)) =
-          make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint32_t *>(a_out + (16 * mt + row) * RC + 2 * (16 * np + 2 * pr)) = 0u;
     }
     __syncthreads();
 
     cp_async_wait<0>();  // v has landed (visible to all after the next barrier)
     // ---- T_ii = (I + N_ii)^-1 for the 16x16 diagonal blocks in fp32: one column per
-    //      thread, forward substitution.  Meanwhile the other threads ship the fp16 q, k
-    //      rows and the decays to the slot.
+    //      thread, forward substitution.  Meanwhile the other threads write the slot's
+    //      K~^T = (diag(e^(G_C - G)) K)^T (fp16, in fragment order) and the decays.
     if (tid < C) {
       const int blk = tid >> 4, cc = tid & 15;
       float x[16];
@@ -308,17 +337,29 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
         *reinterpret_cast<__half *>(sm.T16[blk] + r * 48 + 2 * cc) = __float2half_rn(x[r]);
     } else {
       const int t2 = tid - C, n2 = NT - C;
-      for (int e = t2; e < 2 * C * 16; e += n2) {  // 16 granules of 8 elements per row
-        const int which = e / (C * 16), r = (e >> 4) & (C - 1), gq = e & 15;
-        const uint4 x = *reinterpret_cast<const uint4 *>((which ? sm.Q : sm.K) + r * kP128 + 16 * gq);
-        *reinterpret_cast<uint4 *>((which ? q_out : k_out) + r * kP128 + 16 * gq) =
-            make_uint4(bf16x2_to_f16x2(x.x), bf16x2_to_f16x2(x.y), bf16x2_to_f16x2(x.z),
-                       bf16x2_to_f16x2(x.w));
+      using TS = TokSpan<C>;
+      for (int e = t2; e < 4 * 4 * TS::NSP * 32; e += n2) {  // one lane run of K~^T each
+        const int lane_ = e & 31, sp = (e >> 5) % TS::NSP, wn = (e >> 5) / TS::NSP;
+        const int key = 8 * wn + (lane_ >> 2);  // 32w + 8nt + gid, wn = 4w + nt
+        const int t0 = TS::SPAN * sp + (TS::SPAN / 4) * (lane_ & 3);
+        uint32_t w[TS::KW];
+#pragma unroll
+        for (int u = 0; u < TS::KW; ++u) {
+          const int t = t0 + 2 * u;
+          const float k0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm.K + t * kP128 + 2 * key));
+          const float k1 =
+              __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm.K + (t + 1) * kP128 + 2 * key));
+          w[u] = pack_f16(k0 * sm.ED[t], k1 * sm.ED[t + 1]);
+        }
+        char *dst = kt_out + e * (4 * TS::KW);
+        if constexpr (TS::KW == 4)
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        else
+          *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
       }
       for (int t = t2; t < C; t += n2) {
         dec_out[t] = sm.G[t];
         dec_out[C + t] = sm.EG[t];
-        dec_out[2 * C + t] = sm.ED[t];
       }
     }
     __syncthreads();
@@ -327,11 +368,14 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
     //      substitution over the 16-token blocks, X_i = T_ii (R_i - sum_{j<i} N_ij X_j),
     //      transposed so that each warp solves its own 32 columns without exchange:
     //      X_i^T = (R_i^T - sum_j X_j^T N_ij^T) T_ii^T.  Warps 0-3: W (32 keys each),
-    //      warps 4-7: U (32 value columns each); both stored by column (W^T, U^T).
+    //      warps 4-7: U (32 value columns each).  Each solved tile goes back to token rows
+    //      by a transposing stmatrix: -W into the q tile (no longer needed), U in place
+    //      over the rows of v it was solved from (only this warp reads those columns).
     {
       const int kind = warp >> 2, c0 = 32 * (warp & 3);
       const char *X = kind ? sm.V : sm.K;
-      char *xo = kind ? u_out : w_out;
+      char *xo = kind ? sm.V : sm.Q;
+      const float sgn = kind ? 1.f : -1.f;
       uint32_t Xf[MT][2][4];  // fp16 A fragments of the solved blocks X_j^T
 #pragma unroll
       for (int i = 0; i < MT; ++i) {
@@ -386,31 +430,62 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
             for (int e = 0; e < 4; ++e) out[mt][nt][e] = 0.f;
             mma_f16(out[mt][nt], y[mt], bt[2 * nt], bt[2 * nt + 1]);
           }
+        __syncwarp();  // every lane's reads of R_i are done before the in-place stores
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-              const int col = c0 + 16 * mt + gid + 8 * hr, t = 16 * i + 8 * nt + 2 * tig;
-              *reinterpret_cast<uint32_t *>(xo + col * RC + 2 * t) =
-                  pack_f16(out[mt][nt][2 * hr], out[mt][nt][2 * hr + 1]);
-            }
+          // 8x8 matrices (columns c0 + 16mt + 8hr.., tokens 16i + 8nt..), m = 2nt + hr,
+          // stored transposed to rows 16i + 8nt + r, columns c0 + 16mt + 8hr
+          const int m = lane >> 3, r = lane & 7;
+          stsm_x4_t(xo + (16 * i + 8 * (m >> 1) + r) * kP128 + 2 * (c0 + 16 * mt + 8 * (m & 1)),
+                    pack_f16(sgn * out[mt][0][0], sgn * out[mt][0][1]),
+                    pack_f16(sgn * out[mt][0][2], sgn * out[mt][0][3]),
+                    pack_f16(sgn * out[mt][1][0], sgn * out[mt][1][1]),
+                    pack_f16(sgn * out[mt][1][2], sgn * out[mt][1][3]));
           if (i + 1 < MT) acc_to_f16(out[mt][0], out[mt][1], 1.f, 1.f, 1.f, 1.f, Xf[i][mt]);
         }
       }
+    }
+    __syncthreads();
+    // ---- -W and U to the slot in fragment order (16-byte lane runs, coalesced stores)
+    for (int e = tid; e < 2 * C * 16; e += NT) {
+      const int which = e / (C * 16), f = e % (C * 16), ln = f & 31, g = ln >> 2, tg = ln & 3;
+      uint4 x;
+      if (!which) {  // WN group (w, s, rh) = (f >> 8, (f >> 6) & 3, (f >> 5) & 1)
+        const int w = f >> 8, sp = (f >> 6) & 3, rh = (f >> 5) & 1;
+        x = *reinterpret_cast<const uint4 *>(sm.Q + (16 * w + g + 8 * rh) * kP128 + 2 * (32 * sp + 8 * tg));
+      } else {       // U group (b, w) = ((f >> 5) / MT, (f >> 5) % MT)
+        const int w = (f >> 5) % MT, b = (f >> 5) / MT;
+        const char *r0 = sm.V + (16 * w + g) * kP128 + 2 * (16 * b + 2 * tg);
+        x.x = *reinterpret_cast<const uint32_t *>(r0);                  // nt 0, rh 0
+        x.y = *reinterpret_cast<const uint32_t *>(r0 + 8 * kP128);      // nt 0, rh 1
+        x.z = *reinterpret_cast<const uint32_t *>(r0 + 16);             // nt 1, rh 0
+        x.w = *reinterpret_cast<const uint32_t *>(r0 + 8 * kP128 + 16); // nt 1, rh 1
+      }
+      *reinterpret_cast<uint4 *>((which ? u_out : wn_out) + 16 * f) = x;
     }
   }
 }
 
 // ================================================================== pass 2
-
+// One CTA per (sequence, v-head, 16 value columns) walks the sequence's blocks in order.
+//   producer warp: per block, bulk (TMA) copies of the slot's chain operands and, for the
+//     outputs, a tensor-map TMA of the block's q rows and a bulk copy of A, into a
+//     3-stage shared-memory ring signalled on mbarriers.
+//   chain warps 0-3: the state block S[:, cols] in fp32 registers for the whole sequence
+//     (read from state_in once, written to state_out once), warp w holding keys
+//     32w .. 32w+31.  Per block, for tokens 16w .. 16w+15 (w < C/16),
+//       D = U - W S          (fragment-ordered -W and U, S from a shared fp16 snapshot),
+//     D goes to shared memory (transposed), then each warp updates its keys,
+//       S <- e^(G_C) S + K~^T D,
+//     and writes its part of the next snapshot.
+//   output warps 4-7: for tokens 16ow .. 16ow+15, O = diag(e^G) Q S + A D from the same
+//     snapshot and the exchanged D.
+// Hand-offs between chain and output warps are named barriers; the ring's are mbarriers
+// with bounded waits (a wait that gives up sets the workspace status word).
+constexpr int kDVB = 16;  // value columns per CTA
 constexpr int kChainWarps = 4, kOutWarps = 4;
-constexpr int kRecThreads = 32 * (kChainWarps + kOutWarps + 1);  // + 1 producer warp
 constexpr int kChain = 32 * kChainWarps;
 constexpr int kPair = 32 * (kChainWarps + kOutWarps);
-constexpr int kStages = 3;
-constexpr int kDVB = 16;  // value columns per CTA
 
 // Named barriers of pass 2 (0 is __syncthreads)
 constexpr int kBarChain = 1;   // the chain warps among themselves
@@ -418,341 +493,277 @@ constexpr int kBarSReady = 2;  // +parity: snapshot S_c published (chain arrives
 constexpr int kBarDone = 4;    // +parity: output warps done with block c (output arrives, chain waits)
 constexpr int kBarDReady = 6;  // +parity: D_c published (chain arrives, output waits)
 
-template <int C, typename TO>
+// Byte offset of byte b of row r in a shared tile of RB-byte rows whose 16-byte granules
+// are permuted per row (granule g stored at g ^ f(r), f(r) = 4 (r & 1) + ((r >> 1) & 3)):
+// the fragment loads (eight lanes read four granules of two rows), ldmatrix (eight rows at
+// one granule) and the stmatrix stores all touch eight distinct bank groups.
+__device__ __forceinline__ int swz_row(int r, int RB, int b) {
+  const int f = ((r & 1) << 2) | ((r >> 1) & 3);
+  return r * RB + (((b >> 4) ^ f) << 4) + (b & 15);
+}
+
+// The chain's operands of one block, as copied from the slot (fragment order).
+template <int C>
+struct ChainStage {
+  alignas(128) char WN[C * 256];        // -W
+  alignas(128) char KT[C * 256];        // K~^T
+  alignas(128) char U[(C / 16) * 512];  // U of this CTA's 16 value columns
+  alignas(16) float DEC[2 * C];         // G, e^G
+};
+// The outputs' operands of one block.
+template <int C>
+struct alignas(1024) OutStage {
+  char Q[2][C * 128];    // q rows, keys 0-63 | 64-127 (bf16, TMA 128-byte swizzle)
+  alignas(128) char A[C * row_c(C)];
+};
+
+template <int C, int MODE>
 struct RecSmem {
-  static constexpr int RC = row_c(C);
-  struct Stage {
-    alignas(128) char H[slot_head_bytes(C)];  // W^T | Q | K | A | DEC, as in the slot
-    alignas(16) char U[kDVB * RC];            // U^T rows of this CTA's value columns
-  } st[kStages];
-  alignas(8) uint64_t full[kStages], empty[kStages];
-  alignas(16) char Sn[2][kDVB * kP128];  // S_c^T (fp16) [16 value cols][128 keys], by parity
-  alignas(16) char Db[2][kDVB * RC];     // D_c^T (fp16) [16 value cols][C tokens], by parity
-  alignas(16) char Dd[kDVB * RC];        // (D diag(e^(G_C - G)))^T (fp16)
-  alignas(16) TO O[kOutWarps][16][kDVB];
+  static constexpr int NST = MODE == 0 ? 3 : 2;  // ring depth
+  ChainStage<C> cs[NST];
+  alignas(128) char Sn[2][kDVB * 256];  // S^T (fp16) [16 value cols][128 keys], by parity
+  alignas(128) char Dt[2][kDVB * 128];  // D^T (fp16) [16 value cols][C tokens], by parity
   alignas(16) float S32[kD][kDVB + 4];  // fp32 staging of the state block
+  alignas(8) uint64_t full[NST], empty[NST];
 };
+template <int C, int MODE>
+constexpr size_t rec_smem_bytes() {
+  const size_t base = (sizeof(RecSmem<C, MODE>) + 1023) / 1024 * 1024;
+  return 1024 + base + (MODE == 0 ? 3 * sizeof(OutStage<C>) : 0);  // + alignment slack
+}
 
-template <int C, typename TO>
-__global__ void __launch_bounds__(kRecThreads) recur_kernel(ChunkParams p) {
-  constexpr int NB = kD / kDVB, MT = C / 16, RC = row_c(C);
-  constexpr uint32_t kHeadB = (uint32_t)slot_head_bytes(C);
-  constexpr uint32_t kUB = (uint32_t)(kDVB * RC);
-  constexpr uint32_t kStageTx = kHeadB + kUB;
-  using Smem = RecSmem<C, TO>;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int blk = blockIdx.x % NB;
-  const int nh = blockIdx.x / NB;
-  const int n = nh / p.hv;
-  const int h = nh - n * p.hv;
-  TO *o = static_cast<TO *>(p.o);
-
-  int bos, eos;
-  seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
-  const int nchunks = (eos - bos + C - 1) / C;
-  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD + blk * kDVB;
-  const char *slot0 = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, 0)) * slot_bytes(C);
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1 + kOutWarps);  // the chain warps once, each output warp
-    }
-    mbar_fence_init();
-  }
-  // state block S[:, blk*16 .. +16) -> fp32 staging (coalesced 64-byte rows)
-  for (int e = tid; e < kD * kDVB / 4; e += kRecThreads) {
-    const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
-    const float4 val =
-        p.state_in ? *reinterpret_cast<const float4 *>(p.state_in + sbase + (size_t)i * kD + 4 * c4)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4 *>(&sm.S32[i][4 * c4]) = val;
-  }
-  __syncthreads();
-  // pass 1 complete and its slot writes visible (returns at once without a pending
-  // prerequisite grid)
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
-
-  if (warp == kChainWarps + kOutWarps) {
-    // ---- producer: stream each block's slot part into the ring
-    if (lane == 0) {
-      bool ok = true;
-      for (int c = 0; c < nchunks; ++c) {
-        const int s = c % kStages;
-        if (c >= kStages) ok = mbar_wait(&sm.empty[s], ((c / kStages) - 1) & 1) && ok;
-        typename Smem::Stage &st = sm.st[s];
-        const char *src = slot0 + (size_t)c * slot_bytes(C);
-        mbar_arrive_expect_tx(&sm.full[s], kStageTx);
-        bulk_g2s(st.H, src, kHeadB, &sm.full[s]);
-        bulk_g2s(st.U, src + slot_u_off(C) + (size_t)blk * kDVB * RC, kUB, &sm.full[s]);
-      }
-      // the last copies are consumed before the CTA's final barrier
-      if (!ok) atomicExch(p.err, 1);
-    }
-  } else if (warp < kChainWarps) {
-    // ---- chain warp w: D for tokens 16w .. 16w+15, the state for keys 32w .. 32w+31
-    const int w = warp;
-    float Sa[4][4];  // S^T[j][i], j = gid (+8), i = 32w + 8nt + 2tig (+1)
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        Sa[nt][e] = sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)];
-    auto write_snapshot = [&](char *Sn) {
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int j = gid + 8 * hr, i = 32 * w + 8 * nt + 2 * tig;
-          *reinterpret_cast<uint32_t *>(Sn + j * kP128 + 2 * i) =
-              pack_f16(Sa[nt][2 * hr], Sa[nt][2 * hr + 1]);
-        }
-    };
-    write_snapshot(sm.Sn[0]);
-    bar_sync(kBarChain, kChain);
-    bar_arrive(kBarSReady + 0, kPair);
-
-    bool ok = true;
-#pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c % kStages, par = c & 1;
-      typename Smem::Stage &st = sm.st[s];
-      const char *Wt = st.H, *Ks = st.H + slot_k_off(C);
-      const float *DG = reinterpret_cast<const float *>(st.H + slot_dec_off(C));
-      const float *EG = DG + C, *ED = DG + 2 * C;
-      ok = mbar_wait(&sm.full[s], (c / kStages) & 1) && ok;
-
-      if (w < MT) {
-        // D^T = U^T - S^T W^T for tokens 16w .. 16w+15, keys split in halves
-        float D0[2][4], D1[2][4];
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const float2 u = f16x2_to_float2(*reinterpret_cast<const uint32_t *>(
-                st.U + (gid + 8 * hr) * RC + 2 * (16 * w + 8 * a + 2 * tig)));
-            D0[a][2 * hr] = u.x;
-            D0[a][2 * hr + 1] = u.y;
-            D1[a][2 * hr] = D1[a][2 * hr + 1] = 0.f;
-          }
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          uint32_t nf[4], bw[4];
-          lda_p<kP128>(nf, sm.Sn[par], 0, 16 * ks, lane);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) nf[e] ^= 0x80008000u;  // -S
-          ldb_kn_p<RC>(bw, Wt, 16 * ks, 16 * w, lane);
-          if (ks & 1) {
-            mma_f16(D1[0], nf, bw[0], bw[1]);
-            mma_f16(D1[1], nf, bw[2], bw[3]);
-          } else {
-            mma_f16(D0[0], nf, bw[0], bw[1]);
-            mma_f16(D0[1], nf, bw[2], bw[3]);
-          }
-        }
-        // D (for the outputs) and its carry-scaled copy (for the state), fp16
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int j = gid + 8 * hr, t = 16 * w + 8 * a + 2 * tig;
-            const float d0 = D0[a][2 * hr] + D1[a][2 * hr], d1 = D0[a][2 * hr + 1] + D1[a][2 * hr + 1];
-            *reinterpret_cast<uint32_t *>(sm.Db[par] + j * RC + 2 * t) = pack_f16(d0, d1);
-            *reinterpret_cast<uint32_t *>(sm.Dd + j * RC + 2 * t) = pack_f16(d0 * ED[t], d1 * ED[t + 1]);
-          }
-      }
-      bar_sync(kBarChain, kChain);
-      bar_arrive(kBarDReady + par, kPair);
-
-      // S^T <- e^(G_C) S^T + Dd^T K over keys 32w .. 32w+31
-      {
-        float X[4][4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) X[a][e] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < MT; ++ks) {
-          uint32_t df[4];
-          lda_p<RC>(df, sm.Dd, 0, 16 * ks, lane);
-#pragma unroll
-          for (int np = 0; np < 2; ++np) {
-            uint32_t b[4];
-            ldb_kn_p<kP128>(b, Ks, 16 * ks, 32 * w + 16 * np, lane);
-            mma_f16(X[2 * np], df, b[0], b[1]);
-            mma_f16(X[2 * np + 1], df, b[2], b[3]);
-          }
-        }
-        const float egc = EG[C - 1];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) Sa[nt][e] = fmaf(egc, Sa[nt][e], X[nt][e]);
-      }
-      // S_{c+1} into the other snapshot buffer once the output warps are done with block
-      // c - 1 (which read it as S_{c-1})
-      if (c >= 1) bar_sync(kBarDone + (par ^ 1), kPair);
-      write_snapshot(sm.Sn[par ^ 1]);
-      bar_sync(kBarChain, kChain);
-      if (tid == 0) mbar_arrive(&sm.empty[s]);
-      bar_arrive(kBarSReady + (par ^ 1), kPair);
-    }
-    if (nchunks >= 1) bar_sync(kBarDone + ((nchunks - 1) & 1), kPair);
-    if (!ok && lane == 0) atomicExch(p.err, 1);
-    // final state block -> fp32 staging
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)] = Sa[nt][e];
+__device__ __forceinline__ void put4(uint32_t (&d)[4], uint4 x) {
+  d[0] = x.x;
+  d[1] = x.y;
+  d[2] = x.z;
+  d[3] = x.w;
+}
+template <int KW>
+__device__ __forceinline__ void lds_words(uint32_t (&d)[KW], const char *p) {
+  if constexpr (KW == 4) {
+    put4(d, *reinterpret_cast<const uint4 *>(p));
   } else {
-    // ---- output warp: O^T = diag(e^G) S^T Q^T + D^T A^T for tokens 16ow .. 16ow+15
-    const int ow = warp - kChainWarps;
-    bool ok = true;
-#pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c % kStages, par = c & 1;
-      typename Smem::Stage &st = sm.st[s];
-      const char *Qs = st.H + slot_q_off(C), *A = st.H + slot_a_off(C);
-      const float *EG = reinterpret_cast<const float *>(st.H + slot_dec_off(C)) + C;
-      const int tok0 = bos + c * C;
-      const int L = min(C, eos - tok0);
-      ok = mbar_wait(&sm.full[s], (c / kStages) & 1) && ok;
-      bar_sync(kBarSReady + par, kPair);
-      float R0[2][4], R1[2][4];
-      if (ow < MT) {
+    const uint2 x = *reinterpret_cast<const uint2 *>(p);
+    d[0] = x.x;
+    d[1] = x.y;
+  }
+}
+// Lane (gid, tig)'s token run of span `span` in row r of the swizzled D^T tile.
+template <int KW>
+__device__ __forceinline__ void lds_run(uint32_t (&d)[KW], const char *tile, int r, int span, int tig) {
+  lds_words<KW>(d, tile + swz_row(r, 128, 2 * (KW == 4 ? 32 * span + 8 * tig : 16 * span + 4 * tig)));
+}
+
+// 3-D tensor-map TMA load (box of the map) into shared memory, completion on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4}], [%5];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Chain warp w's snapshot part: S^T rows (value columns) 0-15, keys 32w .. 32w+31, fp16.
+__device__ __forceinline__ void write_snapshot(const float (&Sa)[4][4], char *Sn, int w, int lane) {
+  const int m = lane >> 3, r = lane & 7;
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
+  for (int hf = 0; hf < 2; ++hf)  // matrices m = 2 (nt - 2hf) + rh: rows 8rh.., keys 32w + 8nt..
+    stsm_x4(Sn + swz_row(8 * (m & 1) + r, 256, 2 * (32 * w + 8 * (2 * hf + (m >> 1)))),
+            pack_f16(Sa[2 * hf][0], Sa[2 * hf][1]), pack_f16(Sa[2 * hf][2], Sa[2 * hf][3]),
+            pack_f16(Sa[2 * hf + 1][0], Sa[2 * hf + 1][1]), pack_f16(Sa[2 * hf + 1][2], Sa[2 * hf + 1][3]));
+}
+
+// One block of a chain warp: D for its tokens, the exchange, its keys' state update and
+// snapshot.  MODE 0: output warps share the snapshots and D through named barriers.
+template <int C, int MODE>
+__device__ __forceinline__ void chain_block(int c, const ChainStage<C> &st, float (&Sa)[4][4],
+                                            RecSmem<C, MODE> &sm, int w, int lane, bool dwork,
+                                            bool with_u) {
+  using TS = TokSpan<C>;
+  const int gid = lane >> 2, tig = lane & 3, par = c & 1;
+  if (dwork) {
+    // four independent accumulations per n-tile (key spans s), two products deep each
+    float d[4][2][4];  // [key span][n-tile: value columns 8nt..][fragment]
 #pragma unroll
-          for (int e = 0; e < 4; ++e) R0[a][e] = R1[a][e] = 0.f;
+    for (int g = 0; g < 4; ++g)
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          uint32_t sf[4], bq[4];
-          lda_p<kP128>(sf, sm.Sn[par], 0, 16 * ks, lane);
-          ldb_nk_p<kP128>(bq, Qs, 16 * ow, 16 * ks, lane);
-          if (ks & 1) {
-            mma_f16(R1[0], sf, bq[0], bq[1]);
-            mma_f16(R1[1], sf, bq[2], bq[3]);
-          } else {
-            mma_f16(R0[0], sf, bq[0], bq[1]);
-            mma_f16(R0[1], sf, bq[2], bq[3]);
-          }
-        }
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
+        for (int i = 0; i < 4; ++i) d[g][nt][i] = 0.f;
+    const char *Sn = sm.Sn[par];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            R0[a][e] = (R0[a][e] + R1[a][e]) * EG[16 * ow + 8 * a + 2 * tig + (e & 1)];
+    for (int s = 0; s < 4; ++s) {
+      uint32_t b0[4], b1[4], w0[4], w1[4];
+      put4(b0, *reinterpret_cast<const uint4 *>(Sn + swz_row(gid, 256, 64 * s + 16 * tig)));
+      put4(b1, *reinterpret_cast<const uint4 *>(Sn + swz_row(gid + 8, 256, 64 * s + 16 * tig)));
+      put4(w0, *reinterpret_cast<const uint4 *>(st.WN + wn_off(w, s, 0, lane)));
+      put4(w1, *reinterpret_cast<const uint4 *>(st.WN + wn_off(w, s, 1, lane)));
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t a[4] = {w0[2 * e], w1[2 * e], w0[2 * e + 1], w1[2 * e + 1]};
+        mma_f16(d[s][0], a, b0[2 * e], b0[2 * e + 1]);
+        mma_f16(d[s][1], a, b1[2 * e], b1[2 * e + 1]);
       }
-      bar_sync(kBarDReady + par, kPair);
-      if (ow < MT) {
-        // O^T += D^T A^T over the causal part (A is zero above the diagonal)
-        for (int ks = 0; ks <= ow; ++ks) {
-          uint32_t df[4], ba[4];
-          lda_p<RC>(df, sm.Db[par], 0, 16 * ks, lane);
-          ldb_nk_p<RC>(ba, A, 16 * ow, 16 * ks, lane);
-          mma_f16(R0[0], df, ba[0], ba[1]);
-          mma_f16(R0[1], df, ba[2], ba[3]);
-        }
-        // stage O^T [t][j] and store this warp's rows that lie in the sequence
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            Elem<TO>::store(&sm.O[ow][8 * a + 2 * tig + (e & 1)][gid + 8 * (e >> 1)], R0[a][e]);
-        __syncwarp();
-        constexpr int EPG = 16 / sizeof(TO);  // elements per 16-byte granule
-        constexpr int GPR = kDVB / EPG;       // granules per output row
-        for (int e = lane; e < 16 * GPR; e += 32) {
-          const int r = e / GPR, gi = e % GPR, t = 16 * ow + r;
-          if (t < L)
-            *reinterpret_cast<uint4 *>(o + ((size_t)(tok0 + t) * p.hv + h) * kD + blk * kDVB +
-                                       gi * EPG) =
-                *reinterpret_cast<const uint4 *>(&sm.O[ow][r][gi * EPG]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[s]);
-      bar_arrive(kBarDone + par, kPair);
     }
-    if (nchunks >= 0) bar_sync(kBarSReady + (nchunks & 1), kPair);
-    if (!ok && lane == 0) atomicExch(p.err, 1);
+    uint32_t u[4] = {0u, 0u, 0u, 0u};  // (nt, rh) = (0,0), (0,1), (1,0), (1,1)
+    if (with_u) put4(u, *reinterpret_cast<const uint4 *>(st.U + (32 * w + lane) * 16));
+    float D[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh) {
+        const float2 uu = f16x2_to_float2(u[2 * nt + rh]);
+        D[nt][2 * rh] = uu.x + ((d[0][nt][2 * rh] + d[1][nt][2 * rh]) + (d[2][nt][2 * rh] + d[3][nt][2 * rh]));
+        D[nt][2 * rh + 1] = uu.y + ((d[0][nt][2 * rh + 1] + d[1][nt][2 * rh + 1]) +
+                                    (d[2][nt][2 * rh + 1] + d[3][nt][2 * rh + 1]));
+      }
+    // D^T: matrices m = 2nt + rh (tokens 16w + 8rh.., columns 8nt..) stored transposed
+    const int m = lane >> 3, r = lane & 7;
+    stsm_x4_t(sm.Dt[par] + swz_row(8 * (m >> 1) + r, 128, 32 * w + 16 * (m & 1)),
+              pack_f16(D[0][0], D[0][1]), pack_f16(D[0][2], D[0][3]), pack_f16(D[1][0], D[1][1]),
+              pack_f16(D[1][2], D[1][3]));
   }
-  __syncthreads();
-  for (int e = tid; e < kD * kDVB / 4; e += kRecThreads) {
-    const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
-    *reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)i * kD + 4 * c4) =
-        *reinterpret_cast<const float4 *>(&sm.S32[i][4 * c4]);
+  bar_sync(kBarChain, kChain);
+  if (MODE == 0) bar_arrive(kBarDReady + par, kPair);
+
+  // S^T <- e^(G_C) S^T + D^T K~ over keys 32w .. 32w+31: one fresh accumulation per
+  // token span, summed with the scaled state at the end
+  float X[TS::NSP][4][4];
+#pragma unroll
+  for (int s = 0; s < TS::NSP; ++s)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) X[s][nt][i] = 0.f;
+#pragma unroll
+  for (int s = 0; s < TS::NSP; ++s) {
+    uint32_t a0[TS::KW], a1[TS::KW], kt[4][TS::KW];
+    lds_run<TS::KW>(a0, sm.Dt[par], gid, s, tig);
+    lds_run<TS::KW>(a1, sm.Dt[par], gid + 8, s, tig);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) lds_words<TS::KW>(kt[nt], st.KT + kt_off<C>(w, nt, s, lane));
+#pragma unroll
+    for (int e = 0; e < TS::KS; ++e) {
+      const uint32_t a[4] = {a0[2 * e], a1[2 * e], a0[2 * e + 1], a1[2 * e + 1]};
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) mma_f16(X[s][nt], a, kt[nt][2 * e], kt[nt][2 * e + 1]);
+    }
   }
+  const float gam = st.DEC[2 * C - 1];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float x = X[0][nt][i];
+#pragma unroll
+      for (int s = 1; s < TS::NSP; ++s) x += X[s][nt][i];
+      Sa[nt][i] = fmaf(gam, Sa[nt][i], x);
+    }
+  // S_{c+1} into the other snapshot buffer once the output warps are done with block c - 1
+  if (MODE == 0 && c >= 1) bar_sync(kBarDone + (par ^ 1), kPair);
+  write_snapshot(Sa, sm.Sn[par ^ 1], w, lane);
+  bar_sync(kBarChain, kChain);
+  if (MODE == 0) bar_arrive(kBarSReady + (par ^ 1), kPair);
 }
 
 template <int C, typename TO>
-cudaError_t launch_recur(const ChunkParams &p, long long heads, cudaStream_t stream) {
-  const size_t s2 = sizeof(RecSmem<C, TO>);
-  cudaError_t err = cudaFuncSetAttribute(recur_kernel<C, TO>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
-  if (err != cudaSuccess) return err;
-  // launched as a programmatic dependent of pass 1, so that its launch and set-up overlap
-  // the tail of pass 1
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(heads * (kD / kDVB)));
-  cfg.blockDim = dim3(kRecThreads);
-  cfg.dynamicSmemBytes = s2;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, recur_kernel<C, TO>, p);
+__device__ __forceinline__ void out_block(int c, const ChainStage<C> &cst, const OutStage<C> &ost,
+                                          RecSmem<C, 0> &sm, int ow, int lane, TO *o, int tok0,
+                                          int L, int hv, int h, int blk) {
+  constexpr int RC = row_c(C);
+  const int gid = lane >> 2, tig = lane & 3, par = c & 1;
+  const bool work = 16 * ow < C;
+  bar_sync(kBarSReady + par, kPair);
+  float R[2][4];
+  if (work) {
+    float r2[2][2][4];  // [k-step parity][n-tile][fragment]
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r2[e][nt][i] = 0.f;
+    const char *Sn = sm.Sn[par];
+#pragma unroll
+    for (int ks = 0; ks < kD / 16; ++ks) {
+      uint32_t a[4], b[4];
+      lda_tile<128>(a, ost.Q[ks >> 2], 16 * ow, 16 * (ks & 3), lane);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = bf16x2_to_f16x2(a[i]);
+      ldsm_x4(b, Sn + swz_row((lane & 7) + (lane >> 4) * 8, 256, 2 * (16 * ks + ((lane >> 3) & 1) * 8)));
+      mma_f16(r2[ks & 1][0], a, b[0], b[1]);
+      mma_f16(r2[ks & 1][1], a, b[2], b[3]);
+    }
+    const float e0 = cst.DEC[C + 16 * ow + gid], e1 = cst.DEC[C + 16 * ow + gid + 8];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) R[nt][i] = (r2[0][nt][i] + r2[1][nt][i]) * (i < 2 ? e0 : e1);
+  }
+  bar_sync(kBarDReady + par, kPair);
+  if (work) {
+    // O += A D over the causal part (A is zero above the diagonal)
+    for (int ks = 0; ks <= ow; ++ks) {
+      uint32_t a[4], b[4];
+      lda_p<RC>(a, ost.A, 16 * ow, 16 * ks, lane);
+      ldsm_x4(b, sm.Dt[par] + swz_row((lane & 7) + (lane >> 4) * 8, 128, 2 * (16 * ks + ((lane >> 3) & 1) * 8)));
+      mma_f16(R[0], a, b[0], b[1]);
+      mma_f16(R[1], a, b[2], b[3]);
+    }
+#pragma unroll
+    for (int rh = 0; rh < 2; ++rh) {
+      const int t = 16 * ow + gid + 8 * rh;
+      if (t < L) {
+        TO *dst = o + ((size_t)(tok0 + t) * hv + h) * kD + kDVB * blk + 2 * tig;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          if constexpr (sizeof(TO) == 4) {
+            *reinterpret_cast<float2 *>(dst + 8 * nt) = make_float2(R[nt][2 * rh], R[nt][2 * rh + 1]);
+          } else {
+            *reinterpret_cast<__nv_bfloat162 *>(dst + 8 * nt) =
+                __floats2bfloat162_rn(R[nt][2 * rh], R[nt][2 * rh + 1]);
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  bar_arrive(kBarDone + par, kPair);
 }
 
-// ================================================================== split: state chains
-// The sequence split's runs from zero (-> L_s) and from the identity with U = 0 (-> M_s)
-// need only pass 2's state chain.  One launch covers both: CTAs [0, heads * 8) walk the
-// L chains, the next heads * 8 the M chains (state_in2 / state_out2, U taken as zero).
-// A CTA is the 4 chain warps of recur_kernel plus its producer warp, with a 2-stage ring
-// of the chain's operands only (W^T, K, the decays and this CTA's U columns: 38 KB per
-// block at C = 64) and one snapshot buffer (no output warps read it): ~99 KB of shared
-// memory, so two CTAs share an SM and both kinds of chain run in one wave.
-constexpr int kChThreads = 32 * (kChainWarps + 1);
-constexpr int kChStages = 2;
-
-template <int C>
-struct ChainSmem {
-  static constexpr int RC = row_c(C);
-  struct Stage {
-    alignas(128) char W[slot_q_off(C)];  // W^T, as in the slot
-    alignas(16) char K[C * kP128];       // the block's k rows (fp16)
-    alignas(16) float DEC[3 * C];        // G, e^G, e^(G_C - G)
-    alignas(16) char U[kDVB * RC];       // U^T rows of this CTA's value columns
-  } st[kChStages];
-  alignas(8) uint64_t full[kChStages], empty[kChStages];
-  alignas(16) char Sn[kDVB * kP128];  // S_c^T (fp16) [16 value cols][128 keys]
-  alignas(16) char Dd[kDVB * RC];     // (D diag(e^(G_C - G)))^T (fp16)
-  alignas(16) float S32[kD][kDVB + 4];
-};
-
-template <int C>
-__global__ void __launch_bounds__(kChThreads) split_chain_kernel(ChunkParams p) {
+// MODE 0: pass 2 (state chain and outputs): 4 chain + 4 output warps + 1 producer warp.
+// MODE 1: the sequence split's state chains: CTAs [0, heads * 8) run from state_in, the
+// next heads * 8 from state_in2 with U taken as zero (-> state_out2); 4 chain warps + the
+// producer, no outputs.
+template <int C, typename TO, int MODE>
+__global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 ? 1 : 2)
+    recur_kernel(ChunkParams p, const __grid_constant__ CUtensorMap qmap) {
   constexpr int NB = kD / kDVB, MT = C / 16, RC = row_c(C);
-  constexpr uint32_t kWB = (uint32_t)slot_q_off(C), kKB = (uint32_t)(C * kP128);
-  constexpr uint32_t kDB = (uint32_t)(12 * C), kUB = (uint32_t)(kDVB * RC);
-  using Smem = ChainSmem<C>;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  constexpr int NT = MODE == 0 ? kPair + 32 : kChain + 32;
+  constexpr int NST = RecSmem<C, MODE>::NST, PW = NT / 32 - 1;  // ring depth, producer warp
+  constexpr size_t SB = slot_bytes(C);
+  constexpr uint32_t kChainTx = (uint32_t)(2 * C * 256 + MT * 512 + 8 * C);
+  constexpr uint32_t kOutTx = (uint32_t)(2 * C * 128 + C * RC);
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *base = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  RecSmem<C, MODE> &sm = *reinterpret_cast<RecSmem<C, MODE> *>(base);
+  OutStage<C> *os = reinterpret_cast<OutStage<C> *>(base + (sizeof(RecSmem<C, MODE>) + 1023) / 1024 * 1024);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const long long half = (long long)p.num_seqs * p.hv * NB;
-  const bool maps = (long long)blockIdx.x >= half;
-  const long long b = maps ? (long long)blockIdx.x - half : (long long)blockIdx.x;
+  long long b = blockIdx.x;
+  bool maps = false;
+  if (MODE == 1) {
+    const long long half = (long long)p.num_seqs * p.hv * NB;
+    maps = b >= half;
+    if (maps) b -= half;
+  }
   const int blk = (int)(b % NB);
   const int nh = (int)(b / NB);
   const int n = nh / p.hv;
   const int h = nh - n * p.hv;
+  const int kh = h / (p.hv / p.hk);
   const float *s_in = maps ? p.state_in2 : p.state_in;
   float *s_out = maps ? p.state_out2 : p.state_out;
 
@@ -760,172 +771,144 @@ __global__ void __launch_bounds__(kChThreads) split_chain_kernel(ChunkParams p) 
   seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
   const int nchunks = (eos - bos + C - 1) / C;
   const size_t sbase = ((size_t)n * p.hv + h) * kD * kD + blk * kDVB;
-  const char *slot0 = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, 0)) * slot_bytes(C);
+  const char *slot0 = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, 0)) * SB;
 
   if (tid == 0) {
-    for (int s = 0; s < kChStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], MODE == 0 ? 1 + kOutWarps : 1);  // the chain group, each output warp
     }
     mbar_fence_init();
   }
-  for (int e = tid; e < kD * kDVB / 4; e += kChThreads) {
+  // state block S[:, blk*16 .. +16) -> fp32 staging (coalesced 64-byte rows)
+  for (int e = tid; e < kD * kDVB / 4; e += NT) {
     const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
-    const float4 val =
-        s_in ? *reinterpret_cast<const float4 *>(s_in + sbase + (size_t)i * kD + 4 * c4)
-             : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 val = s_in ? *reinterpret_cast<const float4 *>(s_in + sbase + (size_t)i * kD + 4 * c4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
     *reinterpret_cast<float4 *>(&sm.S32[i][4 * c4]) = val;
   }
   __syncthreads();
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // pass 1's slots are complete
 
-  if (warp == kChainWarps) {
-    // ---- producer: the chain's operands of each block into the ring
+  if (warp == PW) {
+    // ---- producer: each block's operands into the ring
     if (lane == 0) {
       bool ok = true;
       for (int c = 0; c < nchunks; ++c) {
-        const int s = c % kChStages;
-        if (c >= kChStages) ok = mbar_wait(&sm.empty[s], ((c / kChStages) - 1) & 1) && ok;
-        typename Smem::Stage &st = sm.st[s];
-        const char *src = slot0 + (size_t)c * slot_bytes(C);
-        mbar_arrive_expect_tx(&sm.full[s], kWB + kKB + kDB + kUB);
-        bulk_g2s(st.W, src, kWB, &sm.full[s]);
-        bulk_g2s(st.K, src + slot_k_off(C), kKB, &sm.full[s]);
-        bulk_g2s(st.DEC, src + slot_dec_off(C), kDB, &sm.full[s]);
-        bulk_g2s(st.U, src + slot_u_off(C) + (size_t)blk * kDVB * RC, kUB, &sm.full[s]);
+        const int s = c % NST;
+        if (c >= NST) ok = mbar_wait(&sm.empty[s], ((c / NST) - 1) & 1) && ok;
+        const char *src = slot0 + (size_t)c * SB;
+        ChainStage<C> &cs = sm.cs[s];
+        mbar_arrive_expect_tx(&sm.full[s], kChainTx + (MODE == 0 ? kOutTx : 0));
+        bulk_g2s(cs.WN, src, C * 256, &sm.full[s]);
+        bulk_g2s(cs.KT, src + slot_kt_off(C), C * 256, &sm.full[s]);
+        bulk_g2s(cs.U, src + slot_u_off(C) + u_off<C>(blk, 0, 0), MT * 512, &sm.full[s]);
+        bulk_g2s(cs.DEC, src + slot_dec_off(C), 8 * C, &sm.full[s]);
+        if (MODE == 0) {
+          tma_load_3d(os[s].Q[0], &qmap, 0, kh, bos + c * C, &sm.full[s]);
+          tma_load_3d(os[s].Q[1], &qmap, 64, kh, bos + c * C, &sm.full[s]);
+          bulk_g2s(os[s].A, src + slot_a_off(C), C * RC, &sm.full[s]);
+        }
       }
+      // every copy is consumed (full waited on) before the CTA's final barrier
       if (!ok) atomicExch(p.err, 1);
     }
-  } else {
-    // ---- chain warp w: D for tokens 16w .. 16w+15, the state for keys 32w .. 32w+31
+  } else if (warp < kChainWarps) {
     const int w = warp;
+    const bool dwork = w < MT;
     float Sa[4][4];  // S^T[j][i], j = gid (+8), i = 32w + 8nt + 2tig (+1)
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        Sa[nt][e] = sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)];
-    auto write_snapshot = [&]() {
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int j = gid + 8 * hr, i = 32 * w + 8 * nt + 2 * tig;
-          *reinterpret_cast<uint32_t *>(sm.Sn + j * kP128 + 2 * i) =
-              pack_f16(Sa[nt][2 * hr], Sa[nt][2 * hr + 1]);
-        }
-    };
-    write_snapshot();
+      for (int e = 0; e < 4; ++e) Sa[nt][e] = sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)];
+    write_snapshot(Sa, sm.Sn[0], w, lane);
     bar_sync(kBarChain, kChain);
-
+    if (MODE == 0) bar_arrive(kBarSReady + 0, kPair);
     bool ok = true;
 #pragma unroll 1
     for (int c = 0; c < nchunks; ++c) {
-      const int s = c % kChStages;
-      typename Smem::Stage &st = sm.st[s];
-      const float *EG = st.DEC + C, *ED = st.DEC + 2 * C;
-      ok = mbar_wait(&sm.full[s], (c / kChStages) & 1) && ok;
-
-      if (w < MT) {
-        // D^T = U^T - S^T W^T for tokens 16w .. 16w+15 (U = 0 for the map chains)
-        float D0[2][4], D1[2][4];
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const float2 u = f16x2_to_float2(*reinterpret_cast<const uint32_t *>(
-                st.U + (gid + 8 * hr) * RC + 2 * (16 * w + 8 * a + 2 * tig)));
-            D0[a][2 * hr] = maps ? 0.f : u.x;
-            D0[a][2 * hr + 1] = maps ? 0.f : u.y;
-            D1[a][2 * hr] = D1[a][2 * hr + 1] = 0.f;
-          }
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          uint32_t nf[4], bw[4];
-          lda_p<kP128>(nf, sm.Sn, 0, 16 * ks, lane);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) nf[e] ^= 0x80008000u;  // -S
-          ldb_kn_p<RC>(bw, st.W, 16 * ks, 16 * w, lane);
-          if (ks & 1) {
-            mma_f16(D1[0], nf, bw[0], bw[1]);
-            mma_f16(D1[1], nf, bw[2], bw[3]);
-          } else {
-            mma_f16(D0[0], nf, bw[0], bw[1]);
-            mma_f16(D0[1], nf, bw[2], bw[3]);
-          }
-        }
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int j = gid + 8 * hr, t = 16 * w + 8 * a + 2 * tig;
-            const float d0 = D0[a][2 * hr] + D1[a][2 * hr], d1 = D0[a][2 * hr + 1] + D1[a][2 * hr + 1];
-            *reinterpret_cast<uint32_t *>(sm.Dd + j * RC + 2 * t) = pack_f16(d0 * ED[t], d1 * ED[t + 1]);
-          }
-      }
-      bar_sync(kBarChain, kChain);  // Dd complete; every warp is done reading the snapshot
-
-      // S^T <- e^(G_C) S^T + Dd^T K over keys 32w .. 32w+31
-      {
-        float X[4][4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) X[a][e] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < MT; ++ks) {
-          uint32_t df[4];
-          lda_p<RC>(df, sm.Dd, 0, 16 * ks, lane);
-#pragma unroll
-          for (int np = 0; np < 2; ++np) {
-            uint32_t bk[4];
-            ldb_kn_p<kP128>(bk, st.K, 16 * ks, 32 * w + 16 * np, lane);
-            mma_f16(X[2 * np], df, bk[0], bk[1]);
-            mma_f16(X[2 * np + 1], df, bk[2], bk[3]);
-          }
-        }
-        const float egc = EG[C - 1];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) Sa[nt][e] = fmaf(egc, Sa[nt][e], X[nt][e]);
-      }
-      write_snapshot();
-      bar_sync(kBarChain, kChain);  // the new snapshot is complete; Dd and the stage are free
-      if (tid == 0) mbar_arrive(&sm.empty[s]);
+      const int s = c % NST;
+      ok = mbar_wait(&sm.full[s], (c / NST) & 1) && ok;
+      chain_block<C, MODE>(c, sm.cs[s], Sa, sm, w, lane, dwork, !maps);
+      if (tid == 0) mbar_arrive(&sm.empty[s]);  // all chain warps are past the barrier
     }
+    if (MODE == 0 && nchunks >= 1) bar_sync(kBarDone + ((nchunks - 1) & 1), kPair);
     if (!ok && lane == 0) atomicExch(p.err, 1);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)] = Sa[nt][e];
+      for (int e = 0; e < 4; ++e) sm.S32[32 * w + 8 * nt + 2 * tig + (e & 1)][gid + 8 * (e >> 1)] = Sa[nt][e];
+  } else if (MODE == 0) {
+    const int ow = warp - kChainWarps;
+    TO *o = static_cast<TO *>(p.o);
+    bool ok = true;
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % NST;
+      ok = mbar_wait(&sm.full[s], (c / NST) & 1) && ok;
+      const int tok0 = bos + c * C;
+      out_block<C, TO>(c, sm.cs[s], os[s], *reinterpret_cast<RecSmem<C, 0> *>(&sm), ow, lane, o, tok0,
+                       min(C, eos - tok0), p.hv, h, blk);
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+    }
+    bar_sync(kBarSReady + (nchunks & 1), kPair);
+    if (!ok && lane == 0) atomicExch(p.err, 1);
   }
   __syncthreads();
-  for (int e = tid; e < kD * kDVB / 4; e += kChThreads) {
+  for (int e = tid; e < kD * kDVB / 4; e += NT) {
     const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
     *reinterpret_cast<float4 *>(s_out + sbase + (size_t)i * kD + 4 * c4) =
         *reinterpret_cast<const float4 *>(&sm.S32[i][4 * c4]);
   }
 }
 
-template <int C>
-cudaError_t launch_split_chains(const ChunkParams &p, long long heads, cudaStream_t stream) {
-  const size_t sz = sizeof(ChainSmem<C>);
-  cudaError_t err = cudaFuncSetAttribute(split_chain_kernel<C>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sz);
+// cuTensorMapEncodeTiled from the driver, looked up once (no link against libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// Tensor map of q [T, Hk, 128] bf16 for boxes of 64 keys x 1 head x C tokens, 128-byte
+// swizzle (rows past T read as zero).
+cudaError_t q_tensor_map(CUtensorMap *map, const void *q, int total_tokens, int hk, int C) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)hk, (cuuint64_t)total_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)hk * kD * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int C, typename TO, int MODE>
+cudaError_t launch_recur(const ChunkParams &p, long long heads, cudaStream_t stream) {
+  constexpr size_t smem = rec_smem_bytes<C, MODE>();
+  cudaError_t err = cudaFuncSetAttribute(recur_kernel<C, TO, MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(2 * heads * (kD / kDVB)));
-  cfg.blockDim = dim3(kChThreads);
-  cfg.dynamicSmemBytes = sz;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_chain_kernel<C>, p);
+  CUtensorMap qmap;
+  memset(&qmap, 0, sizeof(qmap));
+  if (MODE == 0 && p.total_tokens > 0) {  // (no block, no q load, without tokens)
+    err = q_tensor_map(&qmap, p.q, p.total_tokens, p.hk, C);
+    if (err != cudaSuccess) return err;
+  }
+  const unsigned grid = (unsigned)((MODE == 1 ? 2 : 1) * heads * (kD / kDVB));
+  recur_kernel<C, TO, MODE><<<grid, MODE == 0 ? kPair + 32 : kChain + 32, smem, stream>>>(p, qmap);
+  return cudaGetLastError();
 }
 
 template <int C>
@@ -950,22 +933,16 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
   }
   if (p.passes == 1) return cudaSuccess;
-  if (p.passes == 3) return launch_split_chains<C>(p, heads, stream);
-  return p.o_fp32 ? launch_recur<C, float>(p, heads, stream)
-                  : launch_recur<C, __nv_bfloat16>(p, heads, stream);
+  if (p.passes == 3) return launch_recur<C, float, 1>(p, heads, stream);
+  return p.o_fp32 ? launch_recur<C, float, 0>(p, heads, stream)
+                  : launch_recur<C, __nv_bfloat16, 0>(p, heads, stream);
 }
 
 }  // namespace
 
 size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk) {
   const size_t slots = (size_t)hv * ((size_t)total_tokens / chunk + num_seqs);
-  size_t sb = 0;
-  switch (chunk) {
-    case 16: sb = slot_bytes(16); break;
-    case 32: sb = slot_bytes(32); break;
-    default: sb = slot_bytes(64); break;
-  }
-  return 256 + slots * sb;
+  return 256 + slots * slot_bytes(chunk);
 }
 
 cudaError_t launch_chunk_bf16(const ChunkParams &p, cudaStream_t stream) {

@@ -289,6 +289,24 @@ __device__ __forceinline__ void ldb1_kn_p(uint32_t (&b)[2], const char *base, in
                : "r"(smem_u32(pad_at<STRIDE>(base, k0 + (lane & 7) + ((lane >> 3) & 1) * 8, n0))));
 }
 
+// Four 8x8 16-bit matrices from the mma fragment layout (lane (gid, tig) holds row gid,
+// columns 2tig, 2tig + 1 of matrix i in r_i) to shared memory; lane l gives the address
+// of row l % 8 of matrix l / 8.  The .trans form stores each matrix transposed.
+__device__ __forceinline__ void stsm_x4(void *smem, uint32_t r0, uint32_t r1, uint32_t r2,
+                                        uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(
+                   smem_u32(smem)),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+__device__ __forceinline__ void stsm_x4_t(void *smem, uint32_t r0, uint32_t r1, uint32_t r2,
+                                          uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(
+                   smem_u32(smem)),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
 __device__ __forceinline__ void bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");

@@ -31,19 +31,20 @@ struct ChunkParams {
   const int32_t *cu_seqlens;
   void *o;
   float *delta;  // per-token deltas [T, Hv, 128] fp32, or NULL (single-pass and fp32 kernels)
-  // Workspace of the two-pass bf16 path (chunk_bf16.cu): one slot per (v-head,
-  // block); block c of sequence n uses slot bos_n / C + n + c, which is unique and below
-  // nslots = total_tokens / C + num_seqs.  A slot holds the block's operands for pass 2
-  // in the padded shared-memory layout that pass reads (rows past the sequence end zero):
-  //   W^T fp16 [128][C], rows of 2C+16 B   W = (I+N)^-1 diag(beta e^G) K, by key
-  //   Q   fp16 [C][128], rows of 272 B     the block's q rows (k-head of this v-head)
-  //   K   fp16 [C][128], rows of 272 B     the block's k rows
-  //   A   fp16 [C][C],   rows of 2C+16 B   decay-masked causal Q K^T
-  //   DEC fp32 [3][C]                      G (in-block cumsum), e^G, e^(G_C - G)
-  //   U^T fp16 [128][C], rows of 2C+16 B   U = (I+N)^-1 diag(beta) V, by value column
+  // Workspace of the two-pass bf16 path (chunk_bf16.cu): one slot per (v-head, block);
+  // block c of sequence n uses slot bos_n / C + n + c, which is unique and below
+  // nslots = total_tokens / C + num_seqs.  A slot holds the block's state-free operands,
+  // each region one bulk copy for pass 2 (chunk_bf16.cu; rows past the sequence end are
+  // zero).  WN, KT and U are in the fragment order pass 2's chain warps read (each warp's
+  // 32 lane runs contiguous):
+  //   WN  fp16, C x 128       -W, W = (I+N)^-1 diag(beta e^G) K (rows: tokens)
+  //   KT  fp16, 128 x C       (diag(e^(G_C - G)) K)^T (rows: keys)
+  //   A   fp16 [C][2C + 16 B] decay-masked causal Q K^T, padded rows
+  //   U   fp16, C x 128       U = (I+N)^-1 diag(beta) V (rows: tokens), per 16-column block
+  //   DEC fp32 [2][C]         G (in-block cumsum), e^G
   int nslots;
   char *slot_ws;      // Hv * nslots slots of slot_bytes(C) bytes, 128-byte aligned
-  int *err;           // device status word: nonzero if a kernel wait timed out
+  int *err;           // device status word (workspace header)
   // Two-pass path only: which passes to run (1: pass 1, 2: pass 2, 3: the sequence
   // split's state chains -- from state_in, and with U = 0 from state_in2 -- on the slots
   // of a pass 1 run with these q, k, v, g, beta; else both passes)
@@ -52,19 +53,17 @@ struct ChunkParams {
   float *state_out2;
 };
 
-// Padded row bytes of 16-bit tiles: 128-element rows and C-element rows.
+// Padded row bytes of 16-bit tiles staged in shared memory: 128-element rows and
+// C-element rows (16 mod 128, so that eight rows read at one column hit eight bank groups).
 constexpr int kP128 = 272;
 __host__ __device__ constexpr int row_c(int C) { return 2 * C + 16; }
 // Slot layout offsets (bytes) for block length C.
-__host__ __device__ constexpr size_t slot_q_off(int C) { return (size_t)128 * row_c(C); }
-__host__ __device__ constexpr size_t slot_k_off(int C) { return slot_q_off(C) + (size_t)C * kP128; }
-__host__ __device__ constexpr size_t slot_a_off(int C) { return slot_k_off(C) + (size_t)C * kP128; }
-__host__ __device__ constexpr size_t slot_dec_off(int C) { return slot_a_off(C) + (size_t)C * row_c(C); }
-// W^T | Q | K | A | DEC, contiguous: what every pass-2 CTA of the head copies
-__host__ __device__ constexpr size_t slot_head_bytes(int C) { return slot_dec_off(C) + (size_t)12 * C; }
-__host__ __device__ constexpr size_t slot_u_off(int C) { return slot_head_bytes(C); }
+__host__ __device__ constexpr size_t slot_kt_off(int C) { return (size_t)C * 256; }
+__host__ __device__ constexpr size_t slot_a_off(int C) { return slot_kt_off(C) + (size_t)C * 256; }
+__host__ __device__ constexpr size_t slot_u_off(int C) { return slot_a_off(C) + (size_t)C * row_c(C); }
+__host__ __device__ constexpr size_t slot_dec_off(int C) { return slot_u_off(C) + (size_t)C * 256; }
 __host__ __device__ constexpr size_t slot_bytes(int C) {
-  return (slot_u_off(C) + (size_t)128 * row_c(C) + 127) / 128 * 128;
+  return (slot_dec_off(C) + (size_t)8 * C + 127) / 128 * 128;
 }
 
 // The block's input prologue (block_io.cu): causal conv + SiLU over [q | k | v] raw
