@@ -33,7 +33,8 @@ EXPORTS = ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_block",
            "gdn_workspace_size", "gdn_status_string", "gdn_prefill_chunked_noalloc",
            "gdn_input_prologue", "gdn_gated_rmsnorm", "gdn_verify_block_capture",
            "gdn_state_rollback", "gdn_conv_state_rollback", "gdn_prefill_split",
-           "gdn_prefill_split_workspace_size")
+           "gdn_prefill_split_workspace_size", "gdn_device_status", "gdn_selftest_wait_timeout")
+GDN_STATUS_WAIT_TIMEOUT = 1
 
 
 class GdnUnavailable(RuntimeError):
@@ -98,6 +99,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill_split.restype = ctypes.c_int
         L.gdn_prefill_split_workspace_size.argtypes = [ctypes.POINTER(GdnShape), I32]
         L.gdn_prefill_split_workspace_size.restype = ctypes.c_size_t
+        L.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
+        L.gdn_device_status.restype = ctypes.c_int
+        L.gdn_selftest_wait_timeout.argtypes = [I32, P]
+        L.gdn_selftest_wait_timeout.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -111,6 +116,23 @@ def make_shape(num_seqs: int, total_tokens: int, num_k_heads: int, num_v_heads: 
                o_fp32: int = 0, algo: int = GDN_ALGO_AUTO) -> GdnShape:
     return GdnShape(num_seqs, total_tokens, num_k_heads, num_v_heads, dk, dv, chunk, dtype, o_fp32,
                     algo)
+
+
+def gdn_device_status(stream=None) -> int:
+    """Read and clear the library's status word on the current device (GDN_STATUS_* bits);
+    synchronizes the stream first."""
+    v = ctypes.c_uint32(0)
+    st = lib().gdn_device_status(ctypes.byref(v), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_device_status")
+    return v.value
+
+
+def gdn_selftest_wait_timeout(polls: int = 1024, stream=None) -> None:
+    """Launch the status path's self-test: one bounded wait that nothing completes."""
+    st = lib().gdn_selftest_wait_timeout(int(polls), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_selftest_wait_timeout")
 
 
 def gdn_workspace_size(shape: GdnShape, op: int) -> int:
@@ -226,16 +248,20 @@ def gdn_prefill_split(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,
                       algo: int = GDN_ALGO_AUTO):
     """Sequence-split prompt pass: the results of gdn_prefill_chunked, each sequence cut
     into segments of segment_len tokens (a multiple of chunk) that run side by side.
-    segment_len None: split_segment_len for the device's SM count and the longest
-    sequence the shapes allow (total tokens / sequences, rounded up).
+    segment_len None: split_segment_len for the device's SM count and the mean sequence
+    length (total tokens / sequences, rounded up), so with ragged sequences the longest
+    ones get more than one wave's worth of segments; with no sequences, one block.
     Returns (o, state_out)."""
     torch = _torch()
     if o is None:
         o = torch.empty_like(v)
     if segment_len is None:
         n = cu_seqlens.numel() - 1
-        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
-        segment_len = split_segment_len(n, v.shape[1], -(-q.shape[0] // max(1, n)), chunk, sms)
+        if n <= 0:
+            segment_len = chunk  # nothing to split: the call only validates and returns
+        else:
+            sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+            segment_len = split_segment_len(n, v.shape[1], -(-q.shape[0] // n), chunk, sms)
     _check_tensors(q, k, v, g, beta, state_in, state_out, cu_seqlens, o, workspace)
     shape = _shape_of(q, v, o, state_out, cu_seqlens, chunk, algo)
     need = gdn_prefill_split_workspace_size(shape, segment_len)

@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
 //   output warps 4-7: for tokens 16ow .. 16ow+15, O = diag(e^G) Q S + A D from the same
 //     snapshot and the exchanged D.
 // Hand-offs between chain and output warps are named barriers; the ring's are mbarriers
-// with bounded waits (a wait that gives up sets the workspace status word).
+// with bounded waits (a wait that gives up reports GDN_STATUS_WAIT_TIMEOUT).
 constexpr int kDVB = 16;  // value columns per CTA
 constexpr int kChainWarps = 4, kOutWarps = 4;
 constexpr int kChain = 32 * kChainWarps;
@@ -810,7 +810,7 @@ __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 
         }
       }
       // every copy is consumed (full waited on) before the CTA's final barrier
-      if (!ok) atomicExch(p.err, 1);
+      if (!ok) report_status(p.err, GDN_STATUS_WAIT_TIMEOUT);
     }
   } else if (warp < kChainWarps) {
     const int w = warp;
@@ -832,7 +832,7 @@ __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 
       if (tid == 0) mbar_arrive(&sm.empty[s]);  // all chain warps are past the barrier
     }
     if (MODE == 0 && nchunks >= 1) bar_sync(kBarDone + ((nchunks - 1) & 1), kPair);
-    if (!ok && lane == 0) atomicExch(p.err, 1);
+    if (!ok && lane == 0) report_status(p.err, GDN_STATUS_WAIT_TIMEOUT);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -851,7 +851,7 @@ __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 
       if (lane == 0) mbar_arrive(&sm.empty[s]);
     }
     bar_sync(kBarSReady + (nchunks & 1), kPair);
-    if (!ok && lane == 0) atomicExch(p.err, 1);
+    if (!ok && lane == 0) report_status(p.err, GDN_STATUS_WAIT_TIMEOUT);
   }
   __syncthreads();
   for (int e = tid; e < kD * kDVB / 4; e += NT) {

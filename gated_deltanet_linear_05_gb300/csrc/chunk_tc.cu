@@ -22,8 +22,9 @@
 //              inverses of I + N by forward substitution, and W, U by blocked forward
 //              substitution on mma.sync (as in the two-pass path).
 //   warp 12 lane 0: issues every tcgen05 MMA and its commits.
-// Hand-offs are mbarriers (bounded waits; a timeout sets the workspace-free error flag
-// path: results are then unspecified, the kernel still returns).
+// Hand-offs are mbarriers (bounded waits; a wait that gives up reports
+// GDN_STATUS_WAIT_TIMEOUT to the device status word: results are then unspecified, the
+// kernel still returns).
 // Precision: the Gram MMA takes the exact bf16 q, k; every other product takes fp16
 // operands (q, k, v exact; S, D, W, A rounded to 11 bits for the product) with fp32
 // accumulation, as in the mma.sync paths.
@@ -617,7 +618,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(ChunkParams p) {
     }
   }
 
-  if (!ok && p.err) atomicExch(p.err, 1);
+  if (!ok) report_status(p.err, GDN_STATUS_WAIT_TIMEOUT);
   tc::fence_before();
   __syncthreads();
   if (warp == 0) {

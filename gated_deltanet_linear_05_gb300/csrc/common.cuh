@@ -98,6 +98,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
   }
   return done != 0;
 }
+// mbar_wait with a caller-given number of polls.
+__device__ __forceinline__ bool mbar_wait_polls(uint64_t *bar, uint32_t parity, int polls) {
+  uint32_t done = 0;
+  for (int it = 0; it < polls && !done; ++it) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  }
+  return done != 0;
+}
+// Set status bits in the library's device status word (see gdn_device_status).
+__device__ __forceinline__ void report_status(unsigned int *word, unsigned int bits) {
+  if (word) atomicOr(word, bits);
+}
 // Like mbar_wait, but each try suspends the thread until the phase completes or about
 // 50 us pass, so that waiting warps do not take issue slots from working ones.  Gives up
 // after 2^15 tries (over a second) and returns false.

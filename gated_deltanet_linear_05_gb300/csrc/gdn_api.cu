@@ -2,10 +2,45 @@
 // Declarations and the argument contract: include/gdn.h.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace {
+
+// The library's device status word: kernels OR GDN_STATUS_* bits into it when a bounded
+// wait gives up; gdn_device_status reads and clears it.  In host code the name is only a
+// stand-in for the symbol: its device address is looked up per device.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mutex;
+unsigned int *g_status_addr[kMaxDevices] = {};
+
+// Device address of the status word on the current device (looked up on first use), or
+// NULL if the lookup fails (kernels then report nowhere).
+unsigned int *status_word() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mutex);
+  if (!g_status_addr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+    g_status_addr[dev] = static_cast<unsigned int *>(ptr);
+  }
+  return g_status_addr[dev];
+}
+
+// One thread waits `polls` times on a shared-memory barrier that nothing completes and
+// reports the timeout: the status path without a lost signal anywhere else.  No copy or
+// tensor-core operation targets the barrier, so giving up leaves nothing in flight.
+__global__ void selftest_wait_kernel(int polls, unsigned int *word) {
+  __shared__ __align__(8) uint64_t bar;
+  gdn::mbar_init(&bar, 1);
+  gdn::mbar_fence_init();
+  if (!gdn::mbar_wait_polls(&bar, 0, polls)) gdn::report_status(word, GDN_STATUS_WAIT_TIMEOUT);
+}
 
 using gdn::ChunkParams;
 using gdn::DecodeParams;
@@ -108,6 +143,7 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
     return cuda_status(gdn::launch_decode(d, static_cast<cudaStream_t>(stream)));
   }
   ChunkParams p{};
+  p.err = status_word();
   p.delta = delta;
   p.passes = passes;
   p.state_in2 = state_in2;
@@ -143,7 +179,6 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
     return GDN_ERR_WORKSPACE;
   char *ws = static_cast<char *>(workspace);
   p.nslots = s->total_tokens / s->chunk + s->num_seqs;
-  p.err = reinterpret_cast<int *>(ws);
   p.slot_ws = ws + 256;
   return cuda_status(gdn::launch_chunk_bf16(p, st));
 }
@@ -287,6 +322,26 @@ size_t gdn_workspace_size(const gdn_shape *s, int op) {
   const bool chunked = (op == GDN_OP_PREFILL || op == GDN_OP_VERIFY);
   if (check_shape(s, chunked) != GDN_OK) return (size_t)-1;
   return chunked ? chunked_workspace(s) : 0;
+}
+
+gdn_status gdn_device_status(uint32_t *status, void *stream) {
+  if (!status) return GDN_ERR_INVALID_ARG;
+  unsigned int *word = status_word();
+  if (!word) return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return GDN_ERR_CUDA;
+  *status = v;
+  return GDN_OK;
+}
+
+gdn_status gdn_selftest_wait_timeout(int32_t polls, void *stream) {
+  if (polls < 1 || polls > (1 << 22)) return GDN_ERR_INVALID_ARG;
+  unsigned int *word = status_word();
+  if (!word) return GDN_ERR_CUDA;
+  selftest_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(polls, word);
+  return cuda_status(cudaGetLastError());
 }
 
 const char *gdn_status_string(gdn_status status) {

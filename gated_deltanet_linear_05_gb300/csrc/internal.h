@@ -44,7 +44,7 @@ struct ChunkParams {
   //   DEC fp32 [2][C]         G (in-block cumsum), e^G
   int nslots;
   char *slot_ws;      // Hv * nslots slots of slot_bytes(C) bytes, 128-byte aligned
-  int *err;           // device status word (workspace header)
+  unsigned int *err;  // the library's device status word (GDN_STATUS_* bits), or NULL
   // Two-pass path only: which passes to run (1: pass 1, 2: pass 2, 3: the sequence
   // split's state chains -- from state_in, and with U = 0 from state_in2 -- on the slots
   // of a pass 1 run with these q, k, v, g, beta; else both passes)
@@ -131,7 +131,7 @@ cudaError_t launch_split_plan(const SplitPlanParams &p, cudaStream_t stream);
 cudaError_t launch_identity(float *state, long long states, cudaStream_t stream);
 cudaError_t launch_split_combine(const SplitCombineParams &p, cudaStream_t stream);
 
-// Workspace bytes of the bf16 chunk path: a 256-byte header (status word) + slots.
+// Workspace bytes of the bf16 chunk path: a 256-byte reserved header + slots.
 size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk);
 
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);

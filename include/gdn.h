@@ -46,16 +46,21 @@
  *
  * Ownership and execution: the caller owns every buffer.  Calls enqueue work on
  * `stream` (a cudaStream_t; NULL = the legacy default stream) and return without
- * synchronising.  The library allocates no memory and keeps no state between calls;
- * scratch memory, where an entry point needs it, is the caller's `workspace`
- * (query its size with gdn_workspace_size).
+ * synchronising.  The library allocates no memory; scratch memory, where an entry point
+ * needs it, is the caller's `workspace` (query its size with gdn_workspace_size).  The
+ * only state it keeps is one 32-bit status word per device (gdn_device_status), whose
+ * address the first chunked call on a device looks up (make that call before any stream
+ * capture).
  *
  * Errors: arguments are validated on the host before anything is launched; a bad
  * argument returns its status and enqueues nothing.  A failed launch returns
- * GDN_ERR_CUDA.  cu_seqlens lives on the device and is not read by the host: a
- * malformed cu_seqlens (decreasing, or past total_tokens) cannot make a kernel read
- * or write outside the buffers sized by `shape` (every range is clamped to
- * [0, total_tokens]), but the results are then unspecified.  Faults raised later on
+ * GDN_ERR_CUDA.  The kernels' waits on shared-memory barriers are bounded: a wait that
+ * gives up (a lost signal) ends the kernel normally with unspecified results and sets
+ * GDN_STATUS_WAIT_TIMEOUT in the device status word, which gdn_device_status reports.
+ * cu_seqlens lives on the device and is not read by the host: a malformed cu_seqlens
+ * (decreasing, or past total_tokens) cannot make a kernel read or write outside the
+ * buffers sized by `shape` (every range is clamped to [0, total_tokens]), but the results
+ * are then unspecified.  Faults raised later on
  * the device surface at the caller's next synchronisation, as usual in CUDA.
  */
 #ifndef GDN_H_
@@ -243,13 +248,17 @@ gdn_status gdn_conv_state_rollback(const gdn_shape *shape, const void *q_raw, co
  * real-time path where an allocation could block or fail.  Such a caller still
  * owns q, k, v, g, beta, the states, cu_seqlens and o, exactly as for
  * gdn_prefill_chunked; only the scratch (the `workspace` there) comes from a fixed
- * array of GDN_NOALLOC_SCRATCH_BYTES compiled into the library.  The array lives on
- * every GPU where this entry point has run until the process exits.
+ * array of GDN_NOALLOC_SCRATCH_BYTES compiled into the library.  When the array is
+ * reserved on a GPU depends on CUDA's module loading: with lazy loading (the default)
+ * when the first call on that GPU looks up its address; with eager loading
+ * (CUDA_MODULE_LOADING=EAGER) on every GPU whose context loads the library.  It stays
+ * reserved until the process exits.
  *
  * Same arguments and results as gdn_prefill_chunked, without workspace.  The request
  * must fit: gdn_workspace_size(shape, GDN_OP_PREFILL) <= GDN_NOALLOC_SCRATCH_BYTES,
  * else GDN_ERR_WORKSPACE is returned and nothing is launched (f32 q/k/v need no
- * scratch and always fit).  The first call on a device looks up the array's device
+ * scratch and always fit).  This size check comes after the shape checks but before the
+ * pointer checks: a too-large request with bad pointers reports GDN_ERR_WORKSPACE.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  All calls share the one array: two calls whose work
  * overlaps on the GPU (different streams, or different host threads) race on it and
@@ -369,6 +378,25 @@ gdn_status gdn_prefill_split(const gdn_shape *shape, const void *q, const void *
                              void *workspace, size_t workspace_bytes, void *stream);
 /* Workspace bytes of gdn_prefill_split; (size_t)-1 for an invalid shape or segment_len. */
 size_t gdn_prefill_split_workspace_size(const gdn_shape *shape, int32_t segment_len);
+
+/* Bits of the device status word. */
+#define GDN_STATUS_WAIT_TIMEOUT 1u /* a kernel gave up a bounded wait on a barrier */
+
+/*
+ * Reads and clears the library's status word on the current device: the OR of the
+ * GDN_STATUS_* bits that its kernels reported since the last read (0: every bounded wait
+ * completed).  A GDN_STATUS_WAIT_TIMEOUT means that some call's results are unspecified;
+ * the kernel returned normally and the context stays usable.  Synchronizes `stream`
+ * before reading (do not call during stream capture).  status: host pointer.
+ */
+gdn_status gdn_device_status(uint32_t *status, void *stream);
+
+/*
+ * Self-test of that path: one kernel waits `polls` times (1 .. 2^22) on a shared-memory
+ * barrier that nothing completes, gives up, reports GDN_STATUS_WAIT_TIMEOUT and returns.
+ * No copy or tensor-core operation is left in flight.  One launch on `stream`.
+ */
+gdn_status gdn_selftest_wait_timeout(int32_t polls, void *stream);
 
 /* Workspace bytes `op` (a gdn_op) needs for `shape` (0 when none); (size_t)-1 for an
  * invalid shape or op. */

@@ -310,3 +310,10 @@ def test_split_segment_rule():
         assert segs * n * hv * 8 <= 152 or segs == 1
     with pytest.raises(ValueError):
         f(0, 2, 100)
+
+
+def test_status_entry_points_validate_before_any_cuda_call(L):
+    """A null status pointer and a poll count outside 1 .. 2^22 are rejected on the host."""
+    assert L.gdn_device_status(None, None) == gdn.GDN_ERR_INVALID_ARG
+    for polls in (0, -1, (1 << 22) + 1):
+        assert L.gdn_selftest_wait_timeout(polls, None) == gdn.GDN_ERR_INVALID_ARG
