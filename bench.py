@@ -32,7 +32,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GDN prefill tokens/s (%TC roofline); decode state GB/s (%HBM peak)"
 D = 128
-EXTRA_ROWS = ("decode", "verify", "varlen", "prologue", "gated_rmsnorm", "accept", "split")
+EXTRA_ROWS = ("decode", "decode_block", "verify", "varlen", "prologue", "gated_rmsnorm", "accept",
+              "split")
 
 
 def parse():
@@ -236,6 +237,7 @@ def run_gdn(args):
 
     if not args.no_extra:
         rows = {"decode": lambda: bench_decode(torch, gdn, gi, device, pk, args),
+                "decode_block": lambda: bench_decode_block(torch, gdn, gi, device, pk, args),
                 "verify": lambda: bench_verify(torch, gdn, gi, device, pk, args, flush),
                 "varlen": lambda: bench_varlen(torch, gdn, gi, device, pk, args, flush),
                 "prologue": lambda: bench_prologue(torch, gdn, gi, device, pk, args, flush),
@@ -337,6 +339,81 @@ def bench_decode(torch, gdn, gi, device, pk, args):
             "launch": "100 steps replayed from one CUDA graph",
             "us_per_step_eager_launches": round(ms_eager * 1e3, 3),
             "us_per_step_l2_resident": round(times["resident"] * 1e3, 3), "gpu_launches": steps}
+
+
+def decode_block_bytes(n, hk, hv, s=2, conv_width=4):
+    """The block's decode step: the state read and written, the raw q/k/v projections, a and
+    b, z read and y written, the conv FIFO read and written, the conv and norm weights."""
+    C = (2 * hk + hv) * D
+    return (n * hv * 2 * D * D * 4 + n * C * s + n * hv * 8 + 2 * n * hv * D * s +
+            2 * n * (conv_width - 1) * C * s + C * conv_width * 4 + D * 4)
+
+
+def bench_decode_block(torch, gdn, gi, device, pk, args):
+    """The block's whole decode step (input prologue, state step, gated RMSNorm), 32
+    sequences x 16 heads, one token each: one fused launch (gdn_decode_block_step) against
+    the three separate launches; 8 state sets rotated (268 MB > 2x L2), conv FIFO in place,
+    100 steps captured in one CUDA graph per form."""
+    wl = gi.decode_b32_h16()
+    R, steps = 8, 100
+    d = block_dev_inputs(gi.make_block_inputs(wl), torch, device)
+    S = [dev_inputs(gi.make_inputs(wl, seed=r, step=0), torch, device)["state0"] for r in range(R)]
+    cs = d["conv_state0"]
+    N, Hk, Hv = wl.num_seqs, wl.num_k_heads, wl.num_v_heads
+    q = torch.empty((N, Hk, D), dtype=torch.bfloat16, device=device)
+    k = torch.empty_like(q)
+    v = torch.empty((N, Hv, D), dtype=torch.bfloat16, device=device)
+    g = torch.empty((N, Hv), device=device)
+    beta = torch.empty_like(g)
+    o = torch.empty((N, Hv, D), device=device)
+    y = torch.empty_like(d["z"])
+
+    def fused(i):
+        st = S[i % R]
+        gdn.gdn_decode_block_step(d["q_raw"], d["k_raw"], d["v_raw"], d["a"], d["b"], d["conv_w"],
+                                  d["A_log"], d["dt_bias"], cs, cs, st, st, d["z"], d["norm_w"],
+                                  1e-6, 1e-6, y)
+
+    def three(i):
+        st = S[i % R]
+        gdn.gdn_input_prologue(d["q_raw"], d["k_raw"], d["v_raw"], d["a"], d["b"], d["conv_w"],
+                               d["A_log"], d["dt_bias"], cs, cs, None, 1e-6, q, k, v, g, beta)
+        gdn.gdn_decode_step(q, k, v, g, beta, st, st, None, o)
+        gdn.gdn_gated_rmsnorm(o, d["z"], d["norm_w"], 1e-6, y)
+
+    def run(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    times = {}
+    for name, fn in (("fused", fused), ("three_launches", three)):
+        for i in range(2 * R):
+            fn(i)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn(0)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(gr, stream=stream):
+                for i in range(steps):
+                    fn(i)
+        gr.replay()
+        torch.cuda.synchronize()
+        times[name] = min(run(gr.replay) for _ in range(3)) / steps
+    byts = decode_block_bytes(N, Hk, Hv)
+    ms = times["fused"]
+    return {"workload": wl.name + "_block_x100steps", "us_per_step": round(ms * 1e3, 3),
+            "us_per_step_three_launches": round(times["three_launches"] * 1e3, 3),
+            "speedup_over_three_launches": round(times["three_launches"] / ms, 3),
+            "roofline": roofline("hbm", byts / (ms * 1e-3) / 1e9, pk["hbm"], "GB/s"),
+            "bytes_per_step": byts, "l2": "8 state sets rotated (268 MB)",
+            "launch": "100 steps replayed from one CUDA graph per form", "gpu_launches": steps}
 
 
 SCHEDULES = (("two_pass", 1), ("single_pass", 2), ("tensor_memory", 3),  # C = 64 only

@@ -33,7 +33,8 @@ EXPORTS = ("gdn_prefill_chunked", "gdn_decode_step", "gdn_verify_block",
            "gdn_workspace_size", "gdn_status_string", "gdn_prefill_chunked_noalloc",
            "gdn_input_prologue", "gdn_gated_rmsnorm", "gdn_verify_block_capture",
            "gdn_state_rollback", "gdn_conv_state_rollback", "gdn_prefill_split",
-           "gdn_prefill_split_workspace_size", "gdn_device_status", "gdn_selftest_wait_timeout")
+           "gdn_prefill_split_workspace_size", "gdn_device_status", "gdn_selftest_wait_timeout",
+           "gdn_decode_block_step")
 GDN_STATUS_WAIT_TIMEOUT = 1
 
 
@@ -99,6 +100,9 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill_split.restype = ctypes.c_int
         L.gdn_prefill_split_workspace_size.argtypes = [ctypes.POINTER(GdnShape), I32]
         L.gdn_prefill_split_workspace_size.restype = ctypes.c_size_t
+        L.gdn_decode_block_step.argtypes = ([ctypes.POINTER(GdnShape)] + [P] * 10 + [F] +
+                                            [P] * 4 + [F, P, P, P])
+        L.gdn_decode_block_step.restype = ctypes.c_int
         L.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
         L.gdn_device_status.restype = ctypes.c_int
         L.gdn_selftest_wait_timeout.argtypes = [I32, P]
@@ -348,6 +352,31 @@ def gdn_gated_rmsnorm(o, z, weight, eps: float = 1e-6, y=None, stream=None):
     if st != GDN_OK:
         raise GdnError(st, "gdn_gated_rmsnorm")
     return y
+
+
+def gdn_decode_block_step(q_raw, k_raw, v_raw, a, b, conv_w, A_log, dt_bias, conv_state_in,
+                          conv_state_out, state_in, state_out, z, norm_w, eps_qk: float = 1e-6,
+                          eps_norm: float = 1e-6, y=None, o=None, stream=None):
+    """The block's one-token decode step in one launch: input prologue, state step and
+    gated RMSNorm.  q_raw, k_raw [N, Hk, 128], v_raw and z [N, Hv, 128] (bf16 or fp32),
+    a, b [N, Hv], conv_w [C, 4], A_log, dt_bias [Hv], norm_w [128] fp32, conv states
+    [N, 3, C] in q_raw's dtype (in may be None, out may be None or the same tensor),
+    states [N, Hv, 128, 128] fp32 (in may be None or equal out).  Returns (y, state_out);
+    o (fp32 [N, Hv, 128], optional) receives the layer output before the norm."""
+    _check_tensors(q_raw, k_raw, v_raw, a, b, conv_w, A_log, dt_bias, conv_state_in,
+                   conv_state_out, state_in, state_out, z, norm_w, y, o)
+    N, hk, dk = q_raw.shape
+    hv, dv = v_raw.shape[1], v_raw.shape[2]
+    shape = make_shape(N, N, hk, hv, dk, dv, 64, _dtype_code(q_raw), 0)
+    y = _torch().empty_like(z) if y is None else y
+    st = lib().gdn_decode_block_step(
+        ctypes.byref(shape), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(a), _ptr(b),
+        _ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(conv_state_in), _ptr(conv_state_out),
+        float(eps_qk), _ptr(state_in), _ptr(state_out), _ptr(z), _ptr(norm_w), float(eps_norm),
+        _ptr(y), _ptr(o), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_decode_block_step")
+    return y, state_out
 
 
 def gdn_verify_block_capture(q, k, v, g, beta, state_in, state_out, cu_seqlens, o=None,

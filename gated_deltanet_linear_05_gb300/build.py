@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgdn.so")
 SOURCES = ["gdn_api.cu", "decode.cu", "chunk_f32.cu", "chunk_bf16.cu", "chunk_fused.cu", "chunk_tc.cu",
-           "gdn_noalloc.cu", "block_io.cu", "rollback.cu", "split.cu"]
+           "gdn_noalloc.cu", "block_io.cu", "rollback.cu", "split.cu", "decode_block.cu"]
 HEADERS = ["common.cuh", "internal.h", "tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -489,6 +489,63 @@ gdn_status gdn_input_prologue(const gdn_shape *shape, const void *q_raw, const v
   return cuda_status(gdn::launch_prologue(p, static_cast<cudaStream_t>(stream)));
 }
 
+gdn_status gdn_decode_block_step(const gdn_shape *shape, const void *q_raw, const void *k_raw,
+                                 const void *v_raw, const float *a, const float *b,
+                                 const float *conv_w, const float *A_log, const float *dt_bias,
+                                 const void *conv_state_in, void *conv_state_out, float eps_qk,
+                                 const float *state_in, float *state_out, const void *z,
+                                 const float *norm_w, float eps_norm, void *y, float *o,
+                                 void *stream) {
+  gdn_status st = check_shape(shape, false);
+  if (st != GDN_OK) return st;
+  const gdn_shape *s = shape;
+  const int ratio = s->num_v_heads / s->num_k_heads;
+  if (ratio != 1 && ratio != 2) return GDN_ERR_UNSUPPORTED;  // a cluster of 4 or 8 CTAs
+  if (s->total_tokens != s->num_seqs) return GDN_ERR_INVALID_ARG;  // one token per sequence
+  if (!(eps_qk >= 0.f) || !(eps_norm >= 0.f)) return GDN_ERR_INVALID_ARG;
+  if (s->num_seqs == 0) return GDN_OK;
+  const void *need16[] = {q_raw, k_raw, v_raw, conv_w, state_out, z, norm_w, y};
+  for (const void *ptr : need16)
+    if (!ptr || !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+  const void *need4[] = {a, b, A_log, dt_bias};
+  for (const void *ptr : need4)
+    if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 3u)) return GDN_ERR_INVALID_ARG;
+  if ((state_in && !aligned16(state_in)) || (o && !aligned16(o)) ||
+      (conv_state_in && !aligned16(conv_state_in)) || (conv_state_out && !aligned16(conv_state_out)))
+    return GDN_ERR_INVALID_ARG;
+  if (state_in && partial_overlap(state_in, state_out, state_bytes(s))) return GDN_ERR_ALIAS;
+  const size_t es = s->qkv_dtype == GDN_BF16 ? 2 : 4;
+  const size_t C = (size_t)(2 * s->num_k_heads + s->num_v_heads) * s->dk;
+  if (conv_state_in && conv_state_out &&
+      partial_overlap(conv_state_in, conv_state_out, (size_t)s->num_seqs * (GDN_CONV_WIDTH - 1) * C * es))
+    return GDN_ERR_ALIAS;
+  if (partial_overlap(y, z, (size_t)s->num_seqs * s->num_v_heads * s->dv * es)) return GDN_ERR_ALIAS;
+  gdn::DecodeBlockParams p{};
+  p.num_seqs = s->num_seqs;
+  p.hk = s->num_k_heads;
+  p.hv = s->num_v_heads;
+  p.dtype = s->qkv_dtype;
+  p.eps_qk = eps_qk;
+  p.eps_norm = eps_norm;
+  p.q_raw = q_raw;
+  p.k_raw = k_raw;
+  p.v_raw = v_raw;
+  p.a = a;
+  p.b = b;
+  p.conv_w = conv_w;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.conv_state_in = conv_state_in;
+  p.conv_state_out = conv_state_out;
+  p.state_in = state_in;
+  p.state_out = state_out;
+  p.z = z;
+  p.norm_w = norm_w;
+  p.y = y;
+  p.o = o;
+  return cuda_status(gdn::launch_decode_block(p, static_cast<cudaStream_t>(stream)));
+}
+
 gdn_status gdn_gated_rmsnorm(const gdn_shape *shape, const void *o, const void *z,
                              const float *weight, float eps, void *y, void *stream) {
   gdn_status st = check_shape(shape, false);

@@ -108,6 +108,25 @@ struct NormParams {
   void *y;
 };
 
+// The block's fused one-token decode step (decode_block.cu): prologue + state step +
+// gated RMSNorm; one token per sequence, Hv / Hk in {1, 2}.
+struct DecodeBlockParams {
+  int num_seqs, hk, hv;
+  gdn_dtype dtype;  // of the raw projections, the conv state, z and y
+  float eps_qk, eps_norm;
+  const void *q_raw, *k_raw, *v_raw;
+  const float *a, *b, *conv_w, *A_log, *dt_bias;
+  const void *conv_state_in;
+  void *conv_state_out;
+  const float *state_in;
+  float *state_out;
+  const void *z;
+  const float *norm_w;
+  void *y;
+  float *o;  // the layer output before the norm (fp32), or NULL
+};
+cudaError_t launch_decode_block(const DecodeBlockParams &p, cudaStream_t stream);
+
 cudaError_t launch_prologue(const PrologueParams &p, cudaStream_t stream);
 cudaError_t launch_gated_rmsnorm(const NormParams &p, cudaStream_t stream);
 

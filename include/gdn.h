@@ -324,6 +324,39 @@ gdn_status gdn_input_prologue(const gdn_shape *shape, const void *q_raw, const v
                               float *g, float *beta, void *stream);
 
 /*
+ * The GDN block's whole one-token decode step in one launch: gdn_input_prologue (conv
+ * FIFO + SiLU, q/k L2 norm, gates; "Qwen3.5-4B — Hexagon NPU (QHexRT) — v81" model card,
+ * introduction; "Qwen3.5-0.8B on Dragon Q6A NPU via QNN EP", main changes), the
+ * delta-rule step of gdn_decode_step ("Qwen3.5-9B-npu" model card, "How it works", the
+ * 1-token matrix form) and gdn_gated_rmsnorm (the same card: the output feeds only the
+ * scale-invariant norm), with q, k, v, g and beta kept on chip.  It computes what those
+ * three calls compute (q, k and v rounded to qkv_dtype as the prologue stores them; the
+ * norm taken on the fp32 layer output), up to the order of floating-point sums.
+ * One token per sequence (total_tokens == num_seqs), num_v_heads / num_k_heads 1 or 2
+ * (else GDN_ERR_UNSUPPORTED: a k-head's v-heads form one thread-block cluster).
+ *     q_raw, k_raw  [N, Hk, dk]   qkv_dtype     v_raw, z  [N, Hv, dv]   qkv_dtype
+ *     a, b          [N, Hv]       float32       conv_w    [C, W] float32 (C = 2 Hk dk + Hv dv)
+ *     A_log, dt_bias [Hv]         float32       norm_w    [dv]          float32
+ *     conv_state_in/out [N, W-1, C] qkv_dtype; in may be NULL (zeros), out may be NULL
+ *                   (not written); they may be the same buffer (in place)
+ *     state_in/out  [N, Hv, dk, dv] float32; in may be NULL (zero), may equal out
+ *     y             [N, Hv, dv]   qkv_dtype: the block's output after the gated norm
+ *                   (may be z exactly; other overlap is GDN_ERR_ALIAS)
+ *     o             [N, Hv, dv]   float32, the layer output before the norm, or NULL
+ *     eps_qk, eps_norm >= 0 (as for gdn_input_prologue and gdn_gated_rmsnorm)
+ * Device pointers: the vectors 16-byte aligned, a, b, A_log, dt_bias 4-byte aligned.
+ * dk = dv = 128.  One launch; no workspace.  Launched, like gdn_decode_step, as a
+ * programmatic dependent of the work before it on `stream`.
+ */
+gdn_status gdn_decode_block_step(const gdn_shape *shape, const void *q_raw, const void *k_raw,
+                                 const void *v_raw, const float *a, const float *b,
+                                 const float *conv_w, const float *A_log, const float *dt_bias,
+                                 const void *conv_state_in, void *conv_state_out, float eps_qk,
+                                 const float *state_in, float *state_out, const void *z,
+                                 const float *norm_w, float eps_norm, void *y, float *o,
+                                 void *stream);
+
+/*
  * The GDN block's output epilogue: the gated RMSNorm of each (token, v-head) row of the
  * layer output ("Qwen3.5-4B — Hexagon NPU (QHexRT) — v81" model card, introduction;
  * "Qwen3.5-9B-npu" model card, "How it works": the output feeds only this

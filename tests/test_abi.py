@@ -317,3 +317,21 @@ def test_status_entry_points_validate_before_any_cuda_call(L):
     assert L.gdn_device_status(None, None) == gdn.GDN_ERR_INVALID_ARG
     for polls in (0, -1, (1 << 22) + 1):
         assert L.gdn_selftest_wait_timeout(polls, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_decode_block_step_validation(L):
+    """The fused decode step: grouped heads beyond a cluster of 8 are not built, one token
+    per sequence, non-negative eps; all rejected before any launch."""
+    P = ctypes.c_void_p
+    fake = [P(0x1000 * (i + 1)) for i in range(10)]
+
+    def call(shape, eps_qk=1e-6, eps_norm=1e-6):
+        return L.gdn_decode_block_step(ctypes.byref(shape), *fake, ctypes.c_float(eps_qk),
+                                       P(0x20000), P(0x20000), P(0x30000), P(0x40000),
+                                       ctypes.c_float(eps_norm), P(0x50000), None, None)
+
+    assert call(gdn.make_shape(2, 2, 1, 4)) == gdn.GDN_ERR_UNSUPPORTED        # Hv / Hk = 4
+    assert call(gdn.make_shape(2, 3, 2, 4)) == gdn.GDN_ERR_INVALID_ARG        # T != N
+    assert call(gdn.make_shape(2, 2, 2, 4), eps_qk=-1.0) == gdn.GDN_ERR_INVALID_ARG
+    assert call(gdn.make_shape(2, 2, 2, 4), eps_norm=float("nan")) == gdn.GDN_ERR_INVALID_ARG
+    assert call(gdn.make_shape(0, 0, 2, 4)) == gdn.GDN_OK                     # empty batch
