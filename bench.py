@@ -210,6 +210,8 @@ def run_gdn(args):
     times = timed_steps(torch, step, args.steps, args.warmup, flush)
     torch.cuda.synchronize()
     ms = barrier_max(statistics.mean(times))
+    # the same step back to back, L2 not flushed (whatever the previous step left in L2)
+    warm_ms = barrier_max(statistics.mean(timed_steps(torch, step, max(3, min(args.steps, 50)), 2)))
     flops, byts = prefill_work(wl.lengths, Hk, Hv, C)
     tok_s = world * wl.total_tokens / (ms * 1e-3)
     gbs = byts / (ms * 1e-3) / 1e9
@@ -262,14 +264,15 @@ def run_gdn(args):
                    "l2": "flushed (512 MiB write) before every timed step",
                    "parallelism": "dp%d (independent batches per GPU)" % world},
         # traffic: DRAM bytes of the step's two kernels from the committed ncu capture
-        # (prep 94.1 MB + recur 88.5 MB; ncu flushes caches between kernels, so the
+        # (pass 1 58.6 MB + pass 2 80.3 MB; ncu flushes caches between kernels, so the
         # workspace round trip counts as DRAM traffic there)
-        "roofline": roofline("hbm", gbs, pk["hbm"], "GB/s", traffic=182.6e6),
+        "roofline": roofline("hbm", gbs, pk["hbm"], "GB/s", traffic=138.9e6),
         "roofline_scope": "one gdn_prefill_chunked call (pass 1 + pass 2); the dominant "
-                          "kernel, pass 2, takes 57 of its ~97 us",
+                          "kernel, pass 2, takes ~62 of its ~99 us",
         "tensor": {"achieved": round(tfs, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                    "frac": round(tfs / pk["bf16"], 4), "algorithmic_flops": flops},
         "algorithmic_bytes": byts,
+        "ms_per_step_warm_l2": round(warm_ms, 5),
         "peaks_source": pk["source"],
         "e2e": {"value": round(world * wl.total_tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
@@ -647,9 +650,22 @@ def cpu_baseline(seconds):
         if el >= seconds or reps >= 100:
             break
     tokens = reps * wl.total_tokens * len(pairs) / wl.num_v_heads
+    # one thread: one head of the same workload, repeated for about a tenth of the time
+    t1, reps1 = time.perf_counter(), 0
+    while True:
+        oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state0"], x["cu_seqlens"],
+                         pairs=pairs[:1], threads=1)
+        reps1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= max(0.1, seconds / 10) or reps1 >= 100:
+            break
+    tokens1 = reps1 * wl.total_tokens / wl.num_v_heads
     return {"value": round(tokens / el, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": "%d of the %d heads of %s (full T), %d repetitions, %.1f s, float64 per-token "
-                      "recurrence" % (len(pairs), wl.num_v_heads, wl.name, reps, el)}
+                      "recurrence" % (len(pairs), wl.num_v_heads, wl.name, reps, el),
+            "value_1thread": round(tokens1 / el1, 1),
+            "sample_1thread": "1 head of %s (full T) on 1 thread, %d repetitions, %.2f s"
+                              % (wl.name, reps1, el1)}
 
 
 def run_reference(args):
