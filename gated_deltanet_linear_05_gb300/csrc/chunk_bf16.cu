@@ -342,20 +342,33 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
         const int lane_ = e & 31, sp = (e >> 5) % TS::NSP, wn = (e >> 5) / TS::NSP;
         const int key = 8 * wn + (lane_ >> 2);  // 32w + 8nt + gid, wn = 4w + nt
         const int t0 = TS::SPAN * sp + (TS::SPAN / 4) * (lane_ & 3);
+        // the token pairs are taken in an order rotated by the lane's token group, so that
+        // the four groups of a warp read rows in four different bank groups (their runs
+        // start 8 rows apart: with 272-byte rows, the same bank group)
+        const int rot = (lane_ & 3) & (TS::KW - 1);
         uint32_t w[TS::KW];
 #pragma unroll
         for (int u = 0; u < TS::KW; ++u) {
-          const int t = t0 + 2 * u;
+          const int t = t0 + 2 * ((u + rot) & (TS::KW - 1));
           const float k0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm.K + t * kP128 + 2 * key));
           const float k1 =
               __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm.K + (t + 1) * kP128 + 2 * key));
           w[u] = pack_f16(k0 * sm.ED[t], k1 * sm.ED[t + 1]);
         }
+        uint32_t wo[TS::KW];  // back in token order: pair j was computed at step (j - rot)
+#pragma unroll
+        for (int j = 0; j < TS::KW; ++j) {
+          uint32_t x = w[0];
+#pragma unroll
+          for (int u = 1; u < TS::KW; ++u)
+            if (((u + rot) & (TS::KW - 1)) == j) x = w[u];
+          wo[j] = x;
+        }
         char *dst = kt_out + e * (4 * TS::KW);
         if constexpr (TS::KW == 4)
-          *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(wo[0], wo[1], wo[2], wo[3]);
         else
-          *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+          *reinterpret_cast<uint2 *>(dst) = make_uint2(wo[0], wo[1]);
       }
       for (int t = t2; t < C; t += n2) {
         dec_out[t] = sm.G[t];
