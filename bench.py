@@ -346,7 +346,8 @@ def bench_decode(torch, gdn, gi, device, pk, args):
 
 def decode_block_bytes(n, hk, hv, s=2, conv_width=4):
     """The block's decode step: the state read and written, the raw q/k/v projections, a and
-    b, z read and y written, the conv FIFO read and written, the conv and norm weights."""
+    b, z read and y written, the conv FIFO read and written, the conv and norm weights (the
+    fused kernel's 0.5 MB of scratch, o and its partial sums, stays in L2 and is not counted)."""
     C = (2 * hk + hv) * D
     return (n * hv * 2 * D * D * 4 + n * C * s + n * hv * 8 + 2 * n * hv * D * s +
             2 * n * (conv_width - 1) * C * s + C * conv_width * 4 + D * 4)
@@ -370,12 +371,14 @@ def bench_decode_block(torch, gdn, gi, device, pk, args):
     beta = torch.empty_like(g)
     o = torch.empty((N, Hv, D), device=device)
     y = torch.empty_like(d["z"])
+    ws = torch.zeros(gdn.gdn_workspace_size(gdn.make_shape(N, N, Hk, Hv), gdn.GDN_OP_DECODE_BLOCK)
+                     + 256, dtype=torch.uint8, device=device)
 
     def fused(i):
         st = S[i % R]
         gdn.gdn_decode_block_step(d["q_raw"], d["k_raw"], d["v_raw"], d["a"], d["b"], d["conv_w"],
                                   d["A_log"], d["dt_bias"], cs, cs, st, st, d["z"], d["norm_w"],
-                                  1e-6, 1e-6, y)
+                                  1e-6, 1e-6, y, workspace=ws)
 
     def three(i):
         st = S[i % R]

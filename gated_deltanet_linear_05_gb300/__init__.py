@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(HERE, "libgdn.so")
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIAS, GDN_ERR_WORKSPACE, \
     GDN_ERR_CUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
-GDN_OP_PREFILL, GDN_OP_DECODE, GDN_OP_VERIFY = 0, 1, 2
+GDN_OP_PREFILL, GDN_OP_DECODE, GDN_OP_VERIFY, GDN_OP_DECODE_BLOCK = 0, 1, 2, 3
 GDN_ALGO_AUTO, GDN_ALGO_TWO_PASS, GDN_ALGO_SINGLE_PASS, GDN_ALGO_TENSOR_MEMORY = 0, 1, 2, 3
 GDN_ALGO_RECURRENT = 4
 GDN_SINGLE_PASS_MIN_HEADS = 128
@@ -101,7 +101,7 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill_split_workspace_size.argtypes = [ctypes.POINTER(GdnShape), I32]
         L.gdn_prefill_split_workspace_size.restype = ctypes.c_size_t
         L.gdn_decode_block_step.argtypes = ([ctypes.POINTER(GdnShape)] + [P] * 10 + [F] +
-                                            [P] * 4 + [F, P, P, P])
+                                            [P] * 4 + [F, P, P, P, S, P])
         L.gdn_decode_block_step.restype = ctypes.c_int
         L.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
         L.gdn_device_status.restype = ctypes.c_int
@@ -356,24 +356,33 @@ def gdn_gated_rmsnorm(o, z, weight, eps: float = 1e-6, y=None, stream=None):
 
 def gdn_decode_block_step(q_raw, k_raw, v_raw, a, b, conv_w, A_log, dt_bias, conv_state_in,
                           conv_state_out, state_in, state_out, z, norm_w, eps_qk: float = 1e-6,
-                          eps_norm: float = 1e-6, y=None, o=None, stream=None):
+                          eps_norm: float = 1e-6, y=None, o=None, workspace=None, stream=None):
     """The block's one-token decode step in one launch: input prologue, state step and
     gated RMSNorm.  q_raw, k_raw [N, Hk, 128], v_raw and z [N, Hv, 128] (bf16 or fp32),
     a, b [N, Hv], conv_w [C, 4], A_log, dt_bias [Hv], norm_w [128] fp32, conv states
     [N, 3, C] in q_raw's dtype (in may be None, out may be None or the same tensor),
     states [N, Hv, 128, 128] fp32 (in may be None or equal out).  Returns (y, state_out);
-    o (fp32 [N, Hv, 128], optional) receives the layer output before the norm."""
+    o (fp32 [N, Hv, 128], optional) receives the layer output before the norm.
+    workspace: a uint8 CUDA tensor of gdn_workspace_size(shape, GDN_OP_DECODE_BLOCK) + 256
+    bytes, zeroed once and reused across steps (None: a fresh zeroed one per call)."""
     _check_tensors(q_raw, k_raw, v_raw, a, b, conv_w, A_log, dt_bias, conv_state_in,
                    conv_state_out, state_in, state_out, z, norm_w, y, o)
     N, hk, dk = q_raw.shape
     hv, dv = v_raw.shape[1], v_raw.shape[2]
     shape = make_shape(N, N, hk, hv, dk, dv, 64, _dtype_code(q_raw), 0)
     y = _torch().empty_like(z) if y is None else y
+    if workspace is None:
+        workspace = _torch().zeros(gdn_workspace_size(shape, GDN_OP_DECODE_BLOCK) + 256,
+                                   dtype=_torch().uint8, device=z.device)
+    _check_tensors(workspace)
+    base = workspace.data_ptr()
+    ws_ptr = (base + 255) & ~255
+    ws_bytes = workspace.numel() - (ws_ptr - base)
     st = lib().gdn_decode_block_step(
         ctypes.byref(shape), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(a), _ptr(b),
         _ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(conv_state_in), _ptr(conv_state_out),
         float(eps_qk), _ptr(state_in), _ptr(state_out), _ptr(z), _ptr(norm_w), float(eps_norm),
-        _ptr(y), _ptr(o), _stream(stream))
+        _ptr(y), _ptr(o), ws_ptr, ws_bytes, _stream(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_decode_block_step")
     return y, state_out

@@ -10,17 +10,21 @@
 //
 // One CTA of 64 threads owns a quarter of one (sequence, v-head) state, S[:, 32c .. +32],
 // laid out as in the one-token decode kernel (rows 0-63 in registers, rows 64-127 staged
-// in shared memory by cp.async), so the whole batch's state streams in one wave.  Each
-// CTA forms the conv + SiLU + L2 norm of its token's 128 q and 128 k channels (the
-// k-head's, shared by its v-heads; two adjacent channels per thread) and the conv + SiLU
-// of its 32 v channels, rounded to
+// in shared memory by cp.async; 72 registers, 14 CTAs per SM), so a batch of up to
+// 2128 / 4 sequence-heads streams its state in one wave.  Each CTA forms the conv + SiLU
+// + L2 norm of its token's 128 q and 128 k channels (the k-head's, shared by its v-heads;
+// two adjacent channels per thread) and the conv + SiLU of its 32 v channels, rounded to
 // the storage dtype as the standalone prologue stores them, so the fused step computes
-// what the three separate launches compute.  The CTAs of one k-head's v-heads (4 per
-// v-head) form a thread-block cluster:
-//   - the norm's sum of o^2 over the 128 values of a row is the sum of the four quarters'
-//     partial sums, exchanged through distributed shared memory;
-//   - the cluster barrier that publishes them also orders every CTA's reads of the q/k
-//     FIFO entries before their update, so the FIFO may be updated in place.
+// what the three separate launches compute.  The CTAs of a row (a v-head's four quarters)
+// and of a k-head (its v-heads' quarters) meet through a small workspace, without waiting
+// for one another:
+//   - each quarter writes its 32 values of o and its sum of o^2, then counts in on the
+//     v-head's counter; the last of the four applies the gated norm to the whole row;
+//   - each CTA counts in on the k-head's counter after it has read the k-head's q/k FIFO
+//     entries; the last one advances them, so the FIFO may be updated in place.
+// The last CTA of a counter resets it to zero for the next call.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -31,22 +35,25 @@ namespace {
 constexpr int kDBThreads = 64;
 constexpr int kDBCols = 32;  // value columns per CTA
 
+// two consecutive elements kept as loaded (one register for bf16): the FIFO entries that
+// move one place down are stored back bit for bit
 template <typename T>
-__device__ __forceinline__ float ld_elem(const void *p, size_t i) {
-  return Elem<T>::load(static_cast<const T *>(p) + i);
+using RawPair = typename std::conditional<sizeof(T) == 2, __nv_bfloat162, float2>::type;
+template <typename T>
+__device__ __forceinline__ RawPair<T> ld_raw(const void *p, size_t i) {
+  return *reinterpret_cast<const RawPair<T> *>(static_cast<const T *>(p) + i);
 }
-// two consecutive elements (an even element index: one 32-bit or 64-bit access)
 template <typename T>
-__device__ __forceinline__ void ld_pair(const void *p, size_t i, float (&x)[2]) {
-  if constexpr (sizeof(T) == 2) {
-    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(static_cast<const T *>(p) + i);
-    x[0] = __low2float(v);
-    x[1] = __high2float(v);
-  } else {
-    const float2 v = *reinterpret_cast<const float2 *>(static_cast<const T *>(p) + i);
-    x[0] = v.x;
-    x[1] = v.y;
-  }
+__device__ __forceinline__ float raw_lo(RawPair<T> v) {
+  if constexpr (sizeof(T) == 2) return __low2float(v); else return v.x;
+}
+template <typename T>
+__device__ __forceinline__ float raw_hi(RawPair<T> v) {
+  if constexpr (sizeof(T) == 2) return __high2float(v); else return v.y;
+}
+template <typename T>
+__device__ __forceinline__ void st_raw(T *p, RawPair<T> v) {
+  *reinterpret_cast<RawPair<T> *>(p) = v;
 }
 template <typename T>
 __device__ __forceinline__ void st_pair(T *p, const float (&x)[2]) {
@@ -66,24 +73,8 @@ __device__ __forceinline__ float to_storage(float x) {
 __device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.f + decay_exp(-u)); }
 __device__ __forceinline__ float softplus_f(float u) { return fmaxf(u, 0.f) + log1pf(expf(-fabsf(u))); }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-  return r;
-}
-// store a float into the same variable of the shared memory of cluster CTA `rank`
-__device__ __forceinline__ void st_cluster(float *local, uint32_t rank, float x) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(remote), "f"(x) : "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
 template <typename T>
-__global__ void __launch_bounds__(kDBThreads, 12) decode_block_kernel(DecodeBlockParams p) {
+__global__ void __launch_bounds__(kDBThreads, 14) decode_block_kernel(DecodeBlockParams p) {
   const int quarter = blockIdx.x & 3;
   const int nh = blockIdx.x >> 2;
   const int n = nh / p.hv;
@@ -97,14 +88,12 @@ __global__ void __launch_bounds__(kDBThreads, 12) decode_block_kernel(DecodeBloc
   const size_t C = (size_t)(2 * p.hk + p.hv) * kD;  // conv channels [q | k | v]
   const size_t qc0 = (size_t)kh * kD, kc0 = (size_t)(p.hk + kh) * kD;
   const size_t vc0 = (size_t)(2 * p.hk + h) * kD + quarter * kDBCols;
-  // the k-head's q/k FIFO entries are advanced by one CTA of the cluster
-  const bool qk_writer = (h % ratio) == 0 && quarter == 0;
 
   __shared__ __align__(16) float4 s_S[64][kDBCols / 4];  // rows 64-127 of the slice
   __shared__ float s_q[kD], s_k[kD], s_v[kDBCols];
   __shared__ float s_red[2][2][kDBCols];
   __shared__ float s_ss[2][2];       // [warp][q, k] partial sums of squares
-  __shared__ float s_norm[4];        // each quarter's sum of o^2 (written by the quarters)
+  __shared__ int s_last[2];          // this CTA is the last of its v-head / of its k-head
   __shared__ float s_gate[2];        // d = e^g, beta
 
   // the previous step (a programmatic primary) has completed and its writes are visible
@@ -139,40 +128,45 @@ __global__ void __launch_bounds__(kDBThreads, 12) decode_block_kernel(DecodeBloc
   //      the q and k channel pairs 2tid, 2tid + 1 and, for tid < 16, the v channel pair
   //      2tid, 2tid + 1 of this quarter (pairs: one 32-bit load per FIFO entry)
   const size_t fin = (size_t)n * 3 * C;  // this sequence's FIFO, oldest entry first
-  auto conv2 = [&](const void *raw, size_t ri, size_t ch, float (&f)[3][2], float (&x)[2],
+  auto conv2 = [&](const void *raw, size_t ri, size_t ch, RawPair<T> (&f)[3], RawPair<T> &x,
                    float (&y)[2]) {
     const float4 w0 = *reinterpret_cast<const float4 *>(p.conv_w + 4 * ch);
     const float4 w1 = *reinterpret_cast<const float4 *>(p.conv_w + 4 * ch + 4);
-    ld_pair<T>(raw, ri, x);
+    x = ld_raw<T>(raw, ri);
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      if (p.conv_state_in)
-        ld_pair<T>(p.conv_state_in, fin + i * C + ch, f[i]);
-      else
-        f[i][0] = f[i][1] = 0.f;
-    }
-    float a0 = w0.w * x[0], a1 = w1.w * x[1];
-    a0 = fmaf(w0.z, f[2][0], a0);
-    a1 = fmaf(w1.z, f[2][1], a1);
-    a0 = fmaf(w0.y, f[1][0], a0);
-    a1 = fmaf(w1.y, f[1][1], a1);
-    a0 = fmaf(w0.x, f[0][0], a0);
-    a1 = fmaf(w1.x, f[0][1], a1);
+    for (int i = 0; i < 3; ++i)
+      f[i] = p.conv_state_in ? ld_raw<T>(p.conv_state_in, fin + i * C + ch) : RawPair<T>{};
+    float a0 = w0.w * raw_lo<T>(x), a1 = w1.w * raw_hi<T>(x);
+    a0 = fmaf(w0.z, raw_lo<T>(f[2]), a0);
+    a1 = fmaf(w1.z, raw_hi<T>(f[2]), a1);
+    a0 = fmaf(w0.y, raw_lo<T>(f[1]), a0);
+    a1 = fmaf(w1.y, raw_hi<T>(f[1]), a1);
+    a0 = fmaf(w0.x, raw_lo<T>(f[0]), a0);
+    a1 = fmaf(w1.x, raw_hi<T>(f[0]), a1);
     y[0] = silu_f(a0);
     y[1] = silu_f(a1);
   };
+  T *fo = static_cast<T *>(p.conv_state_out) + fin;
+  // the FIFO entries of channels ch, ch + 1 move one place down; the token enters last
+  auto adv = [&](size_t ch, const RawPair<T> (&f)[3], RawPair<T> x) {
+    st_raw<T>(fo + ch, f[1]);
+    st_raw<T>(fo + C + ch, f[2]);
+    st_raw<T>(fo + 2 * C + ch, x);
+  };
   const size_t qri = ((size_t)n * p.hk + kh) * kD + 2 * tid;
   const size_t vri = ((size_t)n * p.hv + h) * kD + quarter * kDBCols + 2 * tid;
-  float fq[3][2], fk[3][2], xq[2], xk[2], yq[2], yk[2];  // FIFO entries kept for the update
+  RawPair<T> fq[3], fk[3], xq, xk;  // the k-head's FIFO entries, kept for the update
+  float yq[2], yk[2];
   conv2(p.q_raw, qri, qc0 + 2 * tid, fq, xq, yq);
   conv2(p.k_raw, qri, kc0 + 2 * tid, fk, xk, yk);
   float ssq = fmaf(yq[1], yq[1], yq[0] * yq[0]), ssk = fmaf(yk[1], yk[1], yk[0] * yk[0]);
-  float fv[3][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}}, xv[2] = {0.f, 0.f};
   if (tid < kDBCols / 2) {
+    RawPair<T> fv[3], xv;
     float yv[2];
     conv2(p.v_raw, vri, vc0 + 2 * tid, fv, xv, yv);
     s_v[2 * tid] = to_storage<T>(yv[0]);
     s_v[2 * tid + 1] = to_storage<T>(yv[1]);
+    if (p.conv_state_out) adv(vc0 + 2 * tid, fv, xv);  // read by this CTA only, just now
   }
   ssq = warp_sum(ssq);
   ssk = warp_sum(ssk);
@@ -180,6 +174,10 @@ __global__ void __launch_bounds__(kDBThreads, 12) decode_block_kernel(DecodeBloc
     s_ss[warp][0] = ssq;
     s_ss[warp][1] = ssk;
   }
+  // the gated norm's z and weight for this thread's two columns, loaded now (only the row's
+  // last quarter uses them, at the very end)
+  const RawPair<T> zr = ld_raw<T>(p.z, ((size_t)n * p.hv + h) * kD + 2 * tid);
+  const float2 nw = __ldg(reinterpret_cast<const float2 *>(p.norm_w + 2 * tid));
   if (tid == 0) {
     const size_t gi = (size_t)n * p.hv + h;
     const float g = -expf(__ldg(p.A_log + h)) * softplus_f(p.a[gi] + __ldg(p.dt_bias + h));
@@ -239,41 +237,49 @@ __global__ void __launch_bounds__(kDBThreads, 12) decode_block_kernel(DecodeBloc
     o[e] = d * ww + qk * delta[e];
     oss = fmaf(o[e], o[e], oss);
   }
-  // this quarter's sum of o^2 (warp 0, lanes 0-7 hold the 32 columns) to the v-head's
-  // four quarters (cluster ranks 4r .. 4r + 3)
+  // ---- this quarter's o and sum of o^2 to the workspace (warp 0, lanes 0-7 hold the 32
+  //      columns); then count in
   oss += __shfl_xor_sync(0xffffffffu, oss, 1);
   oss += __shfl_xor_sync(0xffffffffu, oss, 2);
   oss += __shfl_xor_sync(0xffffffffu, oss, 4);
-  if (warp == 0 && lane < 4) st_cluster(&s_norm[quarter], (cluster_rank() & ~3u) + lane, oss);
-  // every CTA of the cluster has read its FIFO entries and published its sum
-  cluster_sync_all();
-
-  // ---- gated RMSNorm of the row, stored in the storage dtype
+  const size_t rowh = (size_t)n * p.hv + h;
   if (warp == 0 && rsub == 0) {
-    const float sc = 1.f / sqrtf((s_norm[0] + s_norm[1] + s_norm[2] + s_norm[3]) * (1.f / kD) + p.eps_norm);
-    const size_t row = ((size_t)n * p.hv + h) * kD + col0;
-    T *y = static_cast<T *>(p.y);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float zz = ld_elem<T>(p.z, row + e);
-      Elem<T>::store(y + row + e, o[e] * sc * __ldg(p.norm_w + col0 + e) * silu_f(zz));
-      if (p.o) p.o[row + e] = o[e];
-    }
+    const float4 ov = make_float4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<float4 *>(p.ws_o + rowh * kD + col0) = ov;
+    if (p.o) *reinterpret_cast<float4 *>(p.o + rowh * kD + col0) = ov;
+    if (lane == 0) p.ws_part[rowh * 4 + quarter] = oss;
   }
-  // ---- the advanced FIFO: the entries shift by one and the current input enters last
-  //      (past the barrier, every CTA that reads the k-head's q/k entries has read them)
-  if (p.conv_state_out) {
-    T *fo = static_cast<T *>(p.conv_state_out) + fin;
-    auto adv = [&](size_t ch, const float (&f)[3][2], const float (&x)[2]) {
-      st_pair<T>(fo + ch, f[1]);
-      st_pair<T>(fo + C + ch, f[2]);
-      st_pair<T>(fo + 2 * C + ch, x);
-    };
-    if (qk_writer) {
-      adv(qc0 + 2 * tid, fq, xq);
-      adv(kc0 + 2 * tid, fk, xk);
-    }
-    if (tid < kDBCols / 2) adv(vc0 + 2 * tid, fv, xv);
+  // o, the sum and every FIFO read of the CTA are done (the barrier) and visible on the GPU
+  // (the fence, cumulative over what the barrier ordered) before the counts below
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    unsigned int *cv = p.ws_cnt + rowh, *ck = p.ws_cnt + (size_t)p.num_seqs * p.hv + (size_t)n * p.hk + kh;
+    const unsigned int gv = atomicAdd(cv, 1u), gk = atomicAdd(ck, 1u);
+    s_last[0] = gv == 3u;
+    s_last[1] = gk == 4u * (unsigned int)ratio - 1u;
+    if (gv == 3u) *cv = 0u;  // every quarter has counted in: ready for the next call
+    if (gk == 4u * (unsigned int)ratio - 1u) *ck = 0u;
+  }
+  __syncthreads();
+  // ---- the last CTA of the k-head advances its q/k FIFO entries (every CTA that reads them
+  //      has read them before counting in)
+  if (s_last[1] && p.conv_state_out) {
+    adv(qc0 + 2 * tid, fq, xq);
+    adv(kc0 + 2 * tid, fk, xk);
+  }
+  // ---- the last quarter of the v-head: the gated RMSNorm of the whole row, two values per
+  //      thread, stored in the storage dtype
+  if (s_last[0]) {
+    __threadfence();
+    const float tot = __ldcg(p.ws_part + rowh * 4) + __ldcg(p.ws_part + rowh * 4 + 1) +
+                      __ldcg(p.ws_part + rowh * 4 + 2) + __ldcg(p.ws_part + rowh * 4 + 3);
+    const float sc = 1.f / sqrtf(tot * (1.f / kD) + p.eps_norm);
+    const float2 ov = __ldcg(reinterpret_cast<const float2 *>(p.ws_o + rowh * kD + 2 * tid));
+    float yy[2];
+    yy[0] = ov.x * sc * nw.x * silu_f(raw_lo<T>(zr));
+    yy[1] = ov.y * sc * nw.y * silu_f(raw_hi<T>(zr));
+    st_pair<T>(static_cast<T *>(p.y) + rowh * kD + 2 * tid, yy);
   }
   // ---- S' = d S + k delta^T, written straight from the update
 #pragma unroll
@@ -297,15 +303,11 @@ cudaError_t launch_t(const DecodeBlockParams &p, cudaStream_t stream) {
   cfg.blockDim = dim3(kDBThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;  // one k-head's v-heads x 4 quarters
-  attr[0].val.clusterDim.x = 4 * (p.hv / p.hk);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_block_kernel<T>, p);
 }
 

@@ -318,9 +318,14 @@ gdn_status gdn_prefill_split(const gdn_shape *shape, const void *q, const void *
 extern "C" {
 
 size_t gdn_workspace_size(const gdn_shape *s, int op) {
-  if (op != GDN_OP_PREFILL && op != GDN_OP_DECODE && op != GDN_OP_VERIFY) return (size_t)-1;
+  if (op != GDN_OP_PREFILL && op != GDN_OP_DECODE && op != GDN_OP_VERIFY && op != GDN_OP_DECODE_BLOCK)
+    return (size_t)-1;
   const bool chunked = (op == GDN_OP_PREFILL || op == GDN_OP_VERIFY);
   if (check_shape(s, chunked) != GDN_OK) return (size_t)-1;
+  if (op == GDN_OP_DECODE_BLOCK) {
+    size_t a, b, c;
+    return gdn::decode_block_ws_parts(s->num_seqs, s->num_k_heads, s->num_v_heads, &a, &b, &c);
+  }
   return chunked ? chunked_workspace(s) : 0;
 }
 
@@ -495,12 +500,10 @@ gdn_status gdn_decode_block_step(const gdn_shape *shape, const void *q_raw, cons
                                  const void *conv_state_in, void *conv_state_out, float eps_qk,
                                  const float *state_in, float *state_out, const void *z,
                                  const float *norm_w, float eps_norm, void *y, float *o,
-                                 void *stream) {
+                                 void *workspace, size_t workspace_bytes, void *stream) {
   gdn_status st = check_shape(shape, false);
   if (st != GDN_OK) return st;
   const gdn_shape *s = shape;
-  const int ratio = s->num_v_heads / s->num_k_heads;
-  if (ratio != 1 && ratio != 2) return GDN_ERR_UNSUPPORTED;  // a cluster of 4 or 8 CTAs
   if (s->total_tokens != s->num_seqs) return GDN_ERR_INVALID_ARG;  // one token per sequence
   if (!(eps_qk >= 0.f) || !(eps_norm >= 0.f)) return GDN_ERR_INVALID_ARG;
   if (s->num_seqs == 0) return GDN_OK;
@@ -520,7 +523,16 @@ gdn_status gdn_decode_block_step(const gdn_shape *shape, const void *q_raw, cons
       partial_overlap(conv_state_in, conv_state_out, (size_t)s->num_seqs * (GDN_CONV_WIDTH - 1) * C * es))
     return GDN_ERR_ALIAS;
   if (partial_overlap(y, z, (size_t)s->num_seqs * s->num_v_heads * s->dv * es)) return GDN_ERR_ALIAS;
+  size_t off_cnt, off_part, off_o;
+  const size_t need = gdn::decode_block_ws_parts(s->num_seqs, s->num_k_heads, s->num_v_heads, &off_cnt,
+                                                 &off_part, &off_o);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return GDN_ERR_WORKSPACE;
+  char *ws = static_cast<char *>(workspace);
   gdn::DecodeBlockParams p{};
+  p.ws_cnt = reinterpret_cast<unsigned int *>(ws + off_cnt);
+  p.ws_part = reinterpret_cast<float *>(ws + off_part);
+  p.ws_o = reinterpret_cast<float *>(ws + off_o);
   p.num_seqs = s->num_seqs;
   p.hk = s->num_k_heads;
   p.hv = s->num_v_heads;

@@ -109,7 +109,8 @@ struct NormParams {
 };
 
 // The block's fused one-token decode step (decode_block.cu): prologue + state step +
-// gated RMSNorm; one token per sequence, Hv / Hk in {1, 2}.
+// gated RMSNorm; one token per sequence.  Workspace: counters [N Hv + N Hk] (zero between
+// calls), each quarter's sum of o^2 [N Hv 4], o [N Hv 128] fp32.
 struct DecodeBlockParams {
   int num_seqs, hk, hv;
   gdn_dtype dtype;  // of the raw projections, the conv state, z and y
@@ -124,7 +125,17 @@ struct DecodeBlockParams {
   const float *norm_w;
   void *y;
   float *o;  // the layer output before the norm (fp32), or NULL
+  unsigned int *ws_cnt;
+  float *ws_part, *ws_o;
 };
+// Workspace bytes of the fused decode step: counters, partial sums, o (each 256-aligned).
+inline size_t decode_block_ws_parts(int n, int hk, int hv, size_t *cnt, size_t *part, size_t *o) {
+  auto a = [](size_t x) { return (x + 255) / 256 * 256; };
+  *cnt = 0;
+  *part = a(sizeof(unsigned int) * ((size_t)n * hv + (size_t)n * hk));
+  *o = *part + a(sizeof(float) * (size_t)n * hv * 4);
+  return *o + a(sizeof(float) * (size_t)n * hv * 128);
+}
 cudaError_t launch_decode_block(const DecodeBlockParams &p, cudaStream_t stream);
 
 cudaError_t launch_prologue(const PrologueParams &p, cudaStream_t stream);

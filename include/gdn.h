@@ -84,7 +84,12 @@ typedef enum {
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
-typedef enum { GDN_OP_PREFILL = 0, GDN_OP_DECODE = 1, GDN_OP_VERIFY = 2 } gdn_op;
+typedef enum {
+  GDN_OP_PREFILL = 0,
+  GDN_OP_DECODE = 1,
+  GDN_OP_VERIFY = 2,
+  GDN_OP_DECODE_BLOCK = 3  /* gdn_decode_block_step */
+} gdn_op;
 
 /* Kernel schedule of the bf16 chunked pass (prefill and verify); f32 q/k/v have one.
  *   TWO_PASS     a parallel pass over all blocks of all heads builds the state-free
@@ -332,8 +337,7 @@ gdn_status gdn_input_prologue(const gdn_shape *shape, const void *q_raw, const v
  * scale-invariant norm), with q, k, v, g and beta kept on chip.  It computes what those
  * three calls compute (q, k and v rounded to qkv_dtype as the prologue stores them; the
  * norm taken on the fp32 layer output), up to the order of floating-point sums.
- * One token per sequence (total_tokens == num_seqs), num_v_heads / num_k_heads 1 or 2
- * (else GDN_ERR_UNSUPPORTED: a k-head's v-heads form one thread-block cluster).
+ * One token per sequence (total_tokens == num_seqs).
  *     q_raw, k_raw  [N, Hk, dk]   qkv_dtype     v_raw, z  [N, Hv, dv]   qkv_dtype
  *     a, b          [N, Hv]       float32       conv_w    [C, W] float32 (C = 2 Hk dk + Hv dv)
  *     A_log, dt_bias [Hv]         float32       norm_w    [dv]          float32
@@ -344,9 +348,15 @@ gdn_status gdn_input_prologue(const gdn_shape *shape, const void *q_raw, const v
  *                   (may be z exactly; other overlap is GDN_ERR_ALIAS)
  *     o             [N, Hv, dv]   float32, the layer output before the norm, or NULL
  *     eps_qk, eps_norm >= 0 (as for gdn_input_prologue and gdn_gated_rmsnorm)
+ *     workspace     gdn_workspace_size(shape, GDN_OP_DECODE_BLOCK) bytes, 256-byte aligned
+ *                   (else GDN_ERR_WORKSPACE): per-call scratch through which the CTAs of
+ *                   a row and of a k-head meet without waiting for one another.  It must
+ *                   be zero before the first call that uses it (one cudaMemsetAsync);
+ *                   every call leaves it ready for the next.  Calls sharing a workspace
+ *                   must not overlap on the GPU.
  * Device pointers: the vectors 16-byte aligned, a, b, A_log, dt_bias 4-byte aligned.
- * dk = dv = 128.  One launch; no workspace.  Launched, like gdn_decode_step, as a
- * programmatic dependent of the work before it on `stream`.
+ * dk = dv = 128.  One launch.  Launched, like gdn_decode_step, as a programmatic
+ * dependent of the work before it on `stream`.
  */
 gdn_status gdn_decode_block_step(const gdn_shape *shape, const void *q_raw, const void *k_raw,
                                  const void *v_raw, const float *a, const float *b,
@@ -354,7 +364,7 @@ gdn_status gdn_decode_block_step(const gdn_shape *shape, const void *q_raw, cons
                                  const void *conv_state_in, void *conv_state_out, float eps_qk,
                                  const float *state_in, float *state_out, const void *z,
                                  const float *norm_w, float eps_norm, void *y, float *o,
-                                 void *stream);
+                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * The GDN block's output epilogue: the gated RMSNorm of each (token, v-head) row of the

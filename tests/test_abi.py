@@ -320,17 +320,26 @@ def test_status_entry_points_validate_before_any_cuda_call(L):
 
 
 def test_decode_block_step_validation(L):
-    """The fused decode step: grouped heads beyond a cluster of 8 are not built, one token
-    per sequence, non-negative eps; all rejected before any launch."""
+    """The fused decode step: one token per sequence, non-negative eps, a workspace of
+    gdn_workspace_size(GDN_OP_DECODE_BLOCK) bytes on a 256-byte boundary; all rejected
+    before any launch."""
     P = ctypes.c_void_p
     fake = [P(0x1000 * (i + 1)) for i in range(10)]
+    fake[9] = fake[8]  # the FIFO updated in place
 
-    def call(shape, eps_qk=1e-6, eps_norm=1e-6):
+    def call(shape, eps_qk=1e-6, eps_norm=1e-6, ws=0x100000, ws_bytes=1 << 20):
         return L.gdn_decode_block_step(ctypes.byref(shape), *fake, ctypes.c_float(eps_qk),
                                        P(0x20000), P(0x20000), P(0x30000), P(0x40000),
-                                       ctypes.c_float(eps_norm), P(0x50000), None, None)
+                                       ctypes.c_float(eps_norm), P(0x50000), None, P(ws),
+                                       ctypes.c_size_t(ws_bytes), None)
 
-    assert call(gdn.make_shape(2, 2, 1, 4)) == gdn.GDN_ERR_UNSUPPORTED        # Hv / Hk = 4
+    sh = gdn.make_shape(2, 2, 1, 4)                                            # Hv / Hk = 4
+    need = L.gdn_workspace_size(ctypes.byref(sh), gdn.GDN_OP_DECODE_BLOCK)
+    # counters (2 x 4 + 2 x 1 words), quarter sums (2 x 4 x 4), o (2 x 4 x 128), 256-aligned
+    assert need == 256 + 256 + 2 * 4 * 128 * 4
+    assert call(sh, ws_bytes=need - 1) == gdn.GDN_ERR_WORKSPACE
+    assert call(sh, ws=0x100080, ws_bytes=need) == gdn.GDN_ERR_WORKSPACE      # not 256-aligned
+    assert call(sh, ws=0) == gdn.GDN_ERR_WORKSPACE
     assert call(gdn.make_shape(2, 3, 2, 4)) == gdn.GDN_ERR_INVALID_ARG        # T != N
     assert call(gdn.make_shape(2, 2, 2, 4), eps_qk=-1.0) == gdn.GDN_ERR_INVALID_ARG
     assert call(gdn.make_shape(2, 2, 2, 4), eps_norm=float("nan")) == gdn.GDN_ERR_INVALID_ARG

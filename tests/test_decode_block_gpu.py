@@ -55,10 +55,12 @@ def _check_y(y, y_ref, dt):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
-@pytest.mark.parametrize("hk,hv", [(4, 4), (2, 4)])
+@pytest.mark.parametrize("hk,hv", [(4, 4), (2, 4), (1, 4), (2, 16)])
 def test_fused_decode_steps_in_place_against_the_oracle_chain(dt, hk, hv):
-    """Three consecutive steps, FIFO and state updated in place, fresh token inputs per
-    step; every step's y, the FIFO and the state against the oracle's chain."""
+    """Four consecutive steps, FIFO and state updated in place, fresh token inputs per
+    step, one workspace zeroed once and reused (its counters must come back to zero);
+    every step's y, the FIFO and the state against the oracle's chain.  Grouped heads up
+    to 8 v-heads per k-head: 32 CTAs count in on one k-head's FIFO."""
     import torch
     import gated_deltanet_linear_05_gb300 as gdn
     n = 6
@@ -68,7 +70,10 @@ def test_fused_decode_steps_in_place_against_the_oracle_chain(dt, hk, hv):
     s = to_dev(s_ref, "f32")
     cs_ref = None
     cs = None
-    for step in range(3):
+    shape = gdn.make_shape(n, n, hk, hv)
+    ws = torch.zeros(gdn.gdn_workspace_size(shape, gdn.GDN_OP_DECODE_BLOCK) + 256,
+                     dtype=torch.uint8, device="cuda")
+    for step in range(4):
         x = gi.make_block_inputs(wl, seed=17, step=step)
         if cs is None:
             cs_ref = x["conv_state0"]
@@ -77,7 +82,7 @@ def test_fused_decode_steps_in_place_against_the_oracle_chain(dt, hk, hv):
         o = torch.empty((n, hv, 128), dtype=torch.float32, device="cuda")
         y, _ = gdn.gdn_decode_block_step(d["q_raw"], d["k_raw"], d["v_raw"], d["a"], d["b"],
                                          d["conv_w"], d["A_log"], d["dt_bias"], cs, cs, s, s,
-                                         d["z"], d["norm_w"], o=o)
+                                         d["z"], d["norm_w"], o=o, workspace=ws)
         torch.cuda.synchronize()
         y_ref, s_ref, cs_ref, o_ref = _oracle_step(x, cs_ref, s_ref, dt)
         assert np.array_equal(to_np(cs), cs_ref), "FIFO step %d" % step
