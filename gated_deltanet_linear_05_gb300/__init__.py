@@ -25,6 +25,7 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_OP_PREFILL, GDN_OP_DECODE, GDN_OP_VERIFY, GDN_OP_DECODE_BLOCK = 0, 1, 2, 3
 GDN_ALGO_AUTO, GDN_ALGO_TWO_PASS, GDN_ALGO_SINGLE_PASS, GDN_ALGO_TENSOR_MEMORY = 0, 1, 2, 3
 GDN_ALGO_RECURRENT = 4
+GDN_ALGO_TWO_PASS_TENSOR = 5
 GDN_SINGLE_PASS_MIN_HEADS = 128
 
 GDN_CONV_WIDTH = 4

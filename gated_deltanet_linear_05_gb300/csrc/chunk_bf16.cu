@@ -8,24 +8,24 @@
 // The state-independent part of D is split off:  with T = (I + N)^-1,
 //   D = U - W S0,   U = T diag(beta) V,   W = T diag(beta exp G) K,
 // so the work falls in two passes:
-//   pass 1 (prep_kernel, one CTA per (block, v-head), all in parallel): G, the
-//     decay-masked Grams, the inverses T_ii = (I + N_ii)^-1 of the 16x16 diagonal blocks
-//     of I + N by forward substitution, and W and U by blocked forward substitution
-//     over the 16-token blocks, X_i = T_ii (R_i - sum_{j<i} N_ij X_j) -- the same
-//     triangular solve as the block inverse of the page, applied to the right-hand
-//     sides instead of forming (I + N)^-1.  Each block's -W, K~^T = (diag(e^(G_C - G)) K)^T,
-//     A, U and decays go to its own workspace slot, in the orientation pass 2 loads
-//     straight into its tensor-core fragments.
-//   pass 2 (chain_kernel, one CTA per (sequence, v-head, 16 value columns)): walks the
+//   pass 1 (prep_kernel, one CTA per (block, v-head), all in parallel): the block's q, k,
+//     v rows by tensor-map TMA, G, the decay-masked Grams, the inverses
+//     T_ii = (I + N_ii)^-1 of the 16x16 diagonal blocks of I + N by forward substitution,
+//     and W and U by blocked forward substitution over the 16-token blocks,
+//     X_i = T_ii (R_i - sum_{j<i} N_ij X_j) -- the same triangular solve as the block
+//     inverse of the page, applied to the right-hand sides instead of forming
+//     (I + N)^-1.  Each block's -W, A, U and decays go to its own workspace slot, -W and
+//     U in the fragment order pass 2 loads.
+//   pass 2 (recur_kernel, one CTA per (sequence, v-head, 16 value columns)): walks the
 //     blocks of the sequence in order with the state block S[:, cols] in fp32 registers
-//     (read from state_in once, written to state_out once): D = U - W S and
-//     S <- e^(G_C) S + K~^T D per block, exporting each block's S_c and D_c (fp16).
-//   pass 3 (out_kernel, one CTA per (v-head, block), all in parallel): the block outputs
-//     O = diag(e^G) Q S_c + A D_c.
-// Tensor-core products (mma.sync) take fp16 operands with fp32 accumulation: bf16 q, k
-// and v enter exactly (converted to fp16), the state, D, T, W, A and K~ are rounded to
-// fp16 (11 significant bits) for the products only; the state itself, the sums and every
-// decay are fp32.  Decay factors between two tokens are always the exp of a difference
+//     (read from state_in once, written to state_out once): per block
+//       D = U - W S,   O = diag(e^G) Q S + A D,
+//       S <- e^(G_C) S + K^T (diag(e^(G_C - G)) D)
+//     with q and k rows loaded from the inputs by tensor-map TMA.
+// Tensor-core products (mma.sync) take fp16 operands with fp32 accumulation (the Grams:
+// bf16): bf16 q, k and v enter exactly (converted to fp16), the state, D, T, W and A are
+// rounded to fp16 (11 significant bits) for the products only; the state itself, the
+// sums and every decay are fp32.  Decay factors between two tokens are always the exp of a difference
 // of cumsums.  A partly filled block is padded with g = 0, beta = 0 and zero q/k/v rows
 // (token_valid), which leaves the state exactly as after the sequence's last token.
 #include <cuda.h>
@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace gdn {
 
@@ -52,62 +53,63 @@ __device__ __forceinline__ void acc_to_f16(const float (&x)[4], const float (&y)
   a[3] = pack_f16(y[2] * t0, y[3] * t1);
 }
 
-// Contractions over the keys and over the tokens in pass 2 take the k index in a
-// permuted order: in every span of 32 (for C = 16: 16) indices, lane (gid, tig) supplies
-// the consecutive indices span + 8tig .. +7 (4tig .. +3), elements {4e, 4e+1} as the k
-// pair (2tig, 2tig+1) and {4e+2, 4e+3} as (2tig+8, 2tig+9) of the span's k-step e.  A and
-// B of every product use the same order, so the products are unchanged and each lane
-// reads one contiguous run per row.
-template <int C>
-struct TokSpan {
-  static constexpr int SPAN = C < 32 ? C : 32;  // tokens per span
-  static constexpr int NSP = C / SPAN;          // spans per block
-  static constexpr int KW = SPAN / 8;           // 32-bit words per lane and row run
-  static constexpr int KS = SPAN / 16;          // k-steps per span
-};
-
-// Fragment order of the slot's -W, K~^T and U: the chain kernel loads each group of 32
-// lane runs (512 bytes, or 256 for C = 16) with one coalesced warp instruction.  Groups,
-// lane = 4 gid + tig:
+// The contraction over the keys in pass 2's D = U - W S takes the keys in a permuted
+// order: in every span of 32 keys, lane (gid, tig) supplies the consecutive keys
+// span + 8tig .. +7, elements {4e, 4e+1} as the k pair (2tig, 2tig+1) and {4e+2, 4e+3} as
+// (2tig+8, 2tig+9) of the span's k-step e.  W and S use the same order, so the product is
+// unchanged and each lane reads one contiguous 16-byte run per row.
+//
+// Fragment order of the slot's -W and U: the chain kernel loads each group of 32 lane
+// runs (512 bytes) with one coalesced warp instruction.  Groups, lane = 4 gid + tig:
 //   WN (chain warp w < C/16, key span s < 4, row half rh): lane's run = -W row
 //      16w + gid + 8rh, keys 32s + 8tig .. +7                                   (16 B)
-//   KT (chain warp w < 4, key tile nt < 4, token span s): K~^T row 32w + 8nt + gid, the
-//      lane's token run of span s                                              (4 KW B)
 //   U  (value-column block b < 8, chain warp w < C/16): the words U[16w + gid + 8rh]
 //      [16b + 8nt + 2tig, +1] for (nt, rh) = (0,0), (0,1), (1,0), (1,1)       (16 B)
 __device__ __forceinline__ int wn_off(int w, int s, int rh, int lane) {
   return (((w * 4 + s) * 2 + rh) * 32 + lane) * 16;
 }
 template <int C>
-__device__ __forceinline__ int kt_off(int w, int nt, int s, int lane) {
-  using TS = TokSpan<C>;
-  return (((w * 4 + nt) * TS::NSP + s) * 32 + lane) * (4 * TS::KW);
-}
-template <int C>
 __device__ __forceinline__ int u_off(int b, int w, int lane) {
   return ((b * (C / 16) + w) * 32 + lane) * 16;
+}
+// Element `col` of row r of a 128-element-row tile of 16-bit values held as two halves
+// (columns 0-63 | 64-127) of `half` bytes, each with 128-byte rows in the TMA 128-byte
+// swizzle (16-byte granule g of row r at g ^ (r & 7)).
+__device__ __forceinline__ char *sw_el(char *tile, int half, int r, int col) {
+  return tile + (col >> 6) * half + swz<128>(r, 2 * (col & 63));
+}
+__device__ __forceinline__ const char *sw_el(const char *tile, int half, int r, int col) {
+  return tile + (col >> 6) * half + swz<128>(r, 2 * (col & 63));
 }
 // ================================================================== pass 1
 
 template <int C>
 struct PrepSmem {
-  alignas(16) char K[C * kP128];  // bf16 rows as loaded (rows past the end: zero)
-  alignas(16) char Q[C * kP128];
-  alignas(16) char V[C * kP128];
+  // bf16 rows as loaded by TMA (keys 0-63 | 64-127, 128-byte swizzle; rows past the end
+  // of the tensor: zero, past the end of the sequence: the next one's, never used)
+  char K[2][C * 128];
+  char Q[2][C * 128];
+  char V[2][C * 128];
   float Nd[C / 16][16][17];       // diagonal 16x16 blocks of N (fp32)
   alignas(16) char N16[C * row_c(C)];     // -N (fp16) [t][j], blocks below the diagonal
   alignas(16) char T16[C / 16][16 * 48];  // fp16 T_ii = (I + N_ii)^-1, rows of 48 B
   float G[C], EG[C], ED[C], B[C];
   float gRaw[C], bRaw[C];
+  alignas(8) uint64_t bar_kq, bar_v;  // the q/k tiles, the v tile have landed
 };
 
 constexpr int kPrepThreads = 256;
 
-template <int C>
-__global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, int per_head) {
-  constexpr int NT = kPrepThreads, MT = C / 16, RC = row_c(C);
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  PrepSmem<C> &sm = *reinterpret_cast<PrepSmem<C> *>(smem_raw);
+// LAYOUT 0: the slot layout of recur_kernel (slot_*_off); LAYOUT 1 (C = 64): the layout
+// of the tensor-memory pass 2 (kTs*), every operand stored straight from registers.
+template <int C, int LAYOUT>
+__global__ void __launch_bounds__(kPrepThreads, 3)
+    prep_kernel(ChunkParams p, int per_head, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap vmap) {
+  constexpr int NT = kPrepThreads, MT = C / 16, RC = row_c(C), HB = C * 128;
+  extern __shared__ unsigned char smem_raw[];
+  PrepSmem<C> &sm = *reinterpret_cast<PrepSmem<C> *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -116,48 +118,49 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
   const int n = nh / p.hv;
   const int h = nh - n * p.hv;
   const int kh = h / (p.hv / p.hk);
-  const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-  const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(p.k);
-  const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(p.v);
 
   int bos, eos;
   seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
   const int nchunks = (eos - bos + C - 1) / C;
+  if (tid == 0) {
+    mbar_init(&sm.bar_kq, 1);
+    mbar_init(&sm.bar_v, 1);
+    mbar_fence_init();
+  }
+  bool ok = true;
 
 #pragma unroll 1
-  for (int c = part; c < nchunks; c += per_head) {
+  for (int c = part, it = 0; c < nchunks; c += per_head, ++it) {
     const int tok0 = bos + c * C;
     const int L = min(C, eos - tok0);
-    char *slot = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, c)) * slot_bytes(C);
-    char *wn_out = slot, *kt_out = slot + slot_kt_off(C), *a_out = slot + slot_a_off(C);
+    char *slot = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, c)) * slot_stride(C);
+    char *wn_out = slot, *a_out = slot + slot_a_off(C);
     char *u_out = slot + slot_u_off(C);
     float *dec_out = reinterpret_cast<float *>(slot + slot_dec_off(C));
-    __syncthreads();  // the previous block is done with shared memory
+    __syncthreads();  // the previous block is done with shared memory (and the barriers set up)
 
-    // two copy groups: q, k and the gates (the Grams start on them), then v
-    for (int e = tid; e < C * 16; e += NT) {
-      const int r = e >> 4, gr = e & 15;
-      const bool ok = r < L;
-      const size_t tok = (size_t)tok0 + (ok ? r : 0);
-      const int nb = ok ? 16 : 0;
-      cp_async16(sm.K + r * kP128 + gr * 16, k + (tok * p.hk + kh) * kD + gr * 8, nb);
-      cp_async16(sm.Q + r * kP128 + gr * 16, q + (tok * p.hk + kh) * kD + gr * 8, nb);
+    // the q, k tiles (the Grams start on them) and the v tile by TMA on two barriers;
+    // the gates by 4-byte copies (zero past the sequence end: g = 0, beta = 0 padding)
+    if (tid == 0) {
+      fence_async_smem();  // the previous block's W and U stores before the tiles' overwrite
+      mbar_arrive_expect_tx(&sm.bar_kq, 4 * HB);
+      tma_load_3d(sm.K[0], &kmap, 0, kh, tok0, &sm.bar_kq);
+      tma_load_3d(sm.K[1], &kmap, 64, kh, tok0, &sm.bar_kq);
+      tma_load_3d(sm.Q[0], &qmap, 0, kh, tok0, &sm.bar_kq);
+      tma_load_3d(sm.Q[1], &qmap, 64, kh, tok0, &sm.bar_kq);
+      mbar_arrive_expect_tx(&sm.bar_v, 2 * HB);
+      tma_load_3d(sm.V[0], &vmap, 0, h, tok0, &sm.bar_v);
+      tma_load_3d(sm.V[1], &vmap, 64, h, tok0, &sm.bar_v);
     }
     for (int t = tid; t < C; t += NT) {
-      const bool ok = t < L;
-      const size_t gi = ((size_t)tok0 + (ok ? t : 0)) * p.hv + h;
-      cp_async4(&sm.gRaw[t], p.g + gi, ok ? 4 : 0);
-      cp_async4(&sm.bRaw[t], p.beta + gi, ok ? 4 : 0);
+      const bool in = t < L;
+      const size_t gi = ((size_t)tok0 + (in ? t : 0)) * p.hv + h;
+      cp_async4(&sm.gRaw[t], p.g + gi, in ? 4 : 0);
+      cp_async4(&sm.bRaw[t], p.beta + gi, in ? 4 : 0);
     }
     cp_async_commit();
-    for (int e = tid; e < C * 16; e += NT) {
-      const int r = e >> 4, gr = e & 15;
-      const bool ok = r < L;
-      const size_t tok = (size_t)tok0 + (ok ? r : 0);
-      cp_async16(sm.V + r * kP128 + gr * 16, v + (tok * p.hv + h) * kD + gr * 8, ok ? 16 : 0);
-    }
-    cp_async_commit();
-    cp_async_wait<1>();
+    cp_async_wait<0>();
+    ok = mbar_wait(&sm.bar_kq, it & 1) && ok;
     __syncthreads();
 
     // in-block inclusive cumsum of g (padding contributes 0), e^G, e^(G_C - G), beta --
@@ -217,17 +220,18 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
 #pragma unroll
       for (int e = 0; e < 4; ++e) ga[u][e] = 0.f;
     {
-      const char *Asrc = prod ? sm.Q : sm.K;
+      const char *Asrc = prod ? sm.Q[0] : sm.K[0];
 #pragma unroll
       for (int ks = 0; ks < kD / 16; ++ks) {
+        const int hf = ks >> 2, kk = 16 * (ks & 3);  // key half, key offset in it
         if (n0 > 0) {
           uint32_t a[4];
-          lda_p<kP128>(a, Asrc, 16 * mt0, 16 * ks, lane);
+          lda_tile<128>(a, Asrc + hf * HB, 16 * mt0, kk, lane);
 #pragma unroll
           for (int u = 0; u < 3; ++u) {
             if (u < n0) {
               uint32_t b[4];
-              ldb_nk_p<kP128>(b, sm.K, 16 * (np0 + u), 16 * ks, lane);
+              ldb_nk<128>(b, sm.K[hf], 16 * (np0 + u), kk, lane);
               mma_bf16(ga[2 * u], a, b[0], b[1]);
               mma_bf16(ga[2 * u + 1], a, b[2], b[3]);
             }
@@ -235,8 +239,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
         }
         if (mt1 >= 0) {
           uint32_t a[4], b[4];
-          lda_p<kP128>(a, Asrc, 16 * mt1, 16 * ks, lane);
-          ldb_nk_p<kP128>(b, sm.K, 0, 16 * ks, lane);
+          lda_tile<128>(a, Asrc + hf * HB, 16 * mt1, kk, lane);
+          ldb_nk<128>(b, sm.K[hf], 0, kk, lane);
           mma_bf16(ga[4], a, b[0], b[1]);
           mma_bf16(ga[5], a, b[2], b[3]);
         }
@@ -304,30 +308,29 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
               } else {
                 *reinterpret_cast<uint32_t *>(sm.N16 + t * RC + 2 * j) = pack_f16(-x0, -x1);
               }
-            } else {
+            } else if (LAYOUT == 0) {
               *reinterpret_cast<uint32_t *>(a_out + t * RC + 2 * j) = pack_f16(x0, x1);
+            } else {
+              *reinterpret_cast<uint32_t *>(slot + kTsAt + tc::at_off(t, j)) = pack_f16(x0, x1);
             }
           }
       }
     }
-    // the A tile's upper 16x16 blocks (never computed) are zero: MT (MT - 1) / 2 tiles of
-    // 16 rows x 8 column pairs
-    for (int e = tid; e < 64 * MT * (MT - 1); e += NT) {
-      const int tile = e >> 7, row = (e >> 3) & 15, pr = e & 7;
-      int mt = 0, np = 1, cnt = tile;  // tile -> (mt, np > mt), row-major over the upper part
-      while (cnt >= MT - 1 - mt) {
-        cnt -= MT - 1 - mt;
-        ++mt;
+    if (LAYOUT == 1) {
+      // the A tile's 16x16 blocks above the diagonal (never computed) are zero: 6 tiles of
+      // 16 rows x 8 column pairs
+      for (int e = tid; e < 6 * 128; e += NT) {
+        const int tile = e >> 7, row = (e >> 3) & 15, pr = e & 7;
+        const int mt = tile < 3 ? 0 : (tile < 5 ? 1 : 2);
+        const int np = tile < 3 ? 1 + tile : (tile < 5 ? tile - 1 : 3);
+        *reinterpret_cast<uint32_t *>(slot + kTsAt + tc::at_off(16 * mt + row, 16 * np + 2 * pr)) = 0u;
       }
-      np = mt + 1 + cnt;
-      *reinterpret_cast<uint32_t *>(a_out + (16 * mt + row) * RC + 2 * (16 * np + 2 * pr)) = 0u;
     }
     __syncthreads();
 
-    cp_async_wait<0>();  // v has landed (visible to all after the next barrier)
     // ---- T_ii = (I + N_ii)^-1 for the 16x16 diagonal blocks in fp32: one column per
-    //      thread, forward substitution.  Meanwhile the other threads write the slot's
-    //      K~^T = (diag(e^(G_C - G)) K)^T (fp16, in fragment order) and the decays.
+    //      thread, forward substitution.  Meanwhile the other threads write the decays
+    //      (and for LAYOUT 1 the fp16 operands K and diag(e^G) Q).
     if (tid < C) {
       const int blk = tid >> 4, cc = tid & 15;
       float x[16];
@@ -336,45 +339,30 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
       for (int r = 0; r < 16; ++r)
         *reinterpret_cast<__half *>(sm.T16[blk] + r * 48 + 2 * cc) = __float2half_rn(x[r]);
     } else {
-      const int t2 = tid - C, n2 = NT - C;
-      using TS = TokSpan<C>;
-      for (int e = t2; e < 4 * 4 * TS::NSP * 32; e += n2) {  // one lane run of K~^T each
-        const int lane_ = e & 31, sp = (e >> 5) % TS::NSP, wn = (e >> 5) / TS::NSP;
-        const int key = 8 * wn + (lane_ >> 2);  // 32w + 8nt + gid, wn = 4w + nt
-        const int t0 = TS::SPAN * sp + (TS::SPAN / 4) * (lane_ & 3);
-        // the token pairs are taken in an order rotated by the lane's token group, so that
-        // the four groups of a warp read rows in four different bank groups (their runs
-        // start 8 rows apart: with 272-byte rows, the same bank group)
-        const int rot = (lane_ & 3) & (TS::KW - 1);
-        uint32_t w[TS::KW];
-#pragma unroll
-        for (int u = 0; u < TS::KW; ++u) {
-          const int t = t0 + 2 * ((u + rot) & (TS::KW - 1));
-          const float k0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm.K + t * kP128 + 2 * key));
-          const float k1 =
-              __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm.K + (t + 1) * kP128 + 2 * key));
-          w[u] = pack_f16(k0 * sm.ED[t], k1 * sm.ED[t + 1]);
-        }
-        uint32_t wo[TS::KW];  // back in token order: pair j was computed at step (j - rot)
-#pragma unroll
-        for (int j = 0; j < TS::KW; ++j) {
-          uint32_t x = w[0];
-#pragma unroll
-          for (int u = 1; u < TS::KW; ++u)
-            if (((u + rot) & (TS::KW - 1)) == j) x = w[u];
-          wo[j] = x;
-        }
-        char *dst = kt_out + e * (4 * TS::KW);
-        if constexpr (TS::KW == 4)
-          *reinterpret_cast<uint4 *>(dst) = make_uint4(wo[0], wo[1], wo[2], wo[3]);
-        else
-          *reinterpret_cast<uint2 *>(dst) = make_uint2(wo[0], wo[1]);
+      float *dec = LAYOUT == 0 ? dec_out : reinterpret_cast<float *>(slot + kTsDec);
+      for (int t = tid - C; t < C; t += NT - C) {
+        dec[t] = sm.G[t];
+        dec[C + t] = sm.EG[t];
+        dec[2 * C + t] = sm.ED[t];
       }
-      for (int t = t2; t < C; t += n2) {
-        dec_out[t] = sm.G[t];
-        dec_out[C + t] = sm.EG[t];
+      if (LAYOUT == 1) {
+        // 16 bytes (8 keys of one token) per step, consecutive threads on consecutive
+        // tokens: each warp stores 512 contiguous bytes of the core-matrix layout
+        for (int e = tid - C; e < 2 * C * 16; e += NT - C) {
+          const int which = e >> 10, t = e & (C - 1), gq = (e >> 6) & 15;
+          const uint4 raw = *reinterpret_cast<const uint4 *>(sw_el(which ? sm.Q[0] : sm.K[0], HB, t, 8 * gq));
+          const float sc = which ? sm.EG[t] : 1.f;
+          const uint32_t in4[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t out4[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2)
+            out4[e2] = pack_f16(__uint_as_float(in4[e2] << 16) * sc, __uint_as_float(in4[e2] & 0xffff0000u) * sc);
+          *reinterpret_cast<uint4 *>(slot + (which ? kTsQt : kTsK) + tc::t64_off(t, 8 * gq)) =
+              make_uint4(out4[0], out4[1], out4[2], out4[3]);
+        }
       }
     }
+    ok = mbar_wait(&sm.bar_v, it & 1) && ok;  // v has landed
     __syncthreads();
 
     // ---- [W U] = (I + N)^-1 [diag(beta e^G) K  diag(beta) V] by blocked forward
@@ -386,8 +374,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
     //      over the rows of v it was solved from (only this warp reads those columns).
     {
       const int kind = warp >> 2, c0 = 32 * (warp & 3);
-      const char *X = kind ? sm.V : sm.K;
-      char *xo = kind ? sm.V : sm.Q;
+      const char *X = kind ? sm.V[0] : sm.K[0];
+      char *xo = kind ? sm.V[0] : sm.Q[0];
       const float sgn = kind ? 1.f : -1.f;
       uint32_t Xf[MT][2][4];  // fp16 A fragments of the solved blocks X_j^T
 #pragma unroll
@@ -407,8 +395,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
             uint32_t r4[4];  // (nt 0, cols lo), (nt 0, cols hi), (nt 1, lo), (nt 1, hi)
-            ldsm_x4_t(r4, X + (16 * i + (lane & 7) + 8 * (lane >> 4)) * kP128 +
-                              2 * (c0 + 16 * mt + 8 * ((lane >> 3) & 1)));
+            ldsm_x4_t(r4, sw_el(X, HB, 16 * i + (lane & 7) + 8 * (lane >> 4), c0 + 16 * mt + 8 * ((lane >> 3) & 1)));
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -443,21 +430,35 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
             for (int e = 0; e < 4; ++e) out[mt][nt][e] = 0.f;
             mma_f16(out[mt][nt], y[mt], bt[2 * nt], bt[2 * nt + 1]);
           }
-        __syncwarp();  // every lane's reads of R_i are done before the in-place stores
+        if (LAYOUT == 0) __syncwarp();  // every lane's reads of R_i are done before the in-place stores
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
-          // 8x8 matrices (columns c0 + 16mt + 8hr.., tokens 16i + 8nt..), m = 2nt + hr,
-          // stored transposed to rows 16i + 8nt + r, columns c0 + 16mt + 8hr
-          const int m = lane >> 3, r = lane & 7;
-          stsm_x4_t(xo + (16 * i + 8 * (m >> 1) + r) * kP128 + 2 * (c0 + 16 * mt + 8 * (m & 1)),
-                    pack_f16(sgn * out[mt][0][0], sgn * out[mt][0][1]),
-                    pack_f16(sgn * out[mt][0][2], sgn * out[mt][0][3]),
-                    pack_f16(sgn * out[mt][1][0], sgn * out[mt][1][1]),
-                    pack_f16(sgn * out[mt][1][2], sgn * out[mt][1][3]));
+          if (LAYOUT == 0) {
+            // 8x8 matrices (columns c0 + 16mt + 8hr.., tokens 16i + 8nt..), m = 2nt + hr,
+            // stored transposed to rows 16i + 8nt + r, columns c0 + 16mt + 8hr
+            const int m = lane >> 3, r = lane & 7;
+            stsm_x4_t(sw_el(xo, HB, 16 * i + 8 * (m >> 1) + r, c0 + 16 * mt + 8 * (m & 1)),
+                      pack_f16(sgn * out[mt][0][0], sgn * out[mt][0][1]),
+                      pack_f16(sgn * out[mt][0][2], sgn * out[mt][0][3]),
+                      pack_f16(sgn * out[mt][1][0], sgn * out[mt][1][1]),
+                      pack_f16(sgn * out[mt][1][2], sgn * out[mt][1][3]));
+          } else {
+            // W^T (wt_off) or U^T ([col][token], 144-byte rows) straight to the slot:
+            // lane (gid, tig) holds columns c0 + 16mt + gid (+8), tokens 16i + 8nt + 2tig, +1
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int hr = 0; hr < 2; ++hr) {
+                const int col = c0 + 16 * mt + gid + 8 * hr, t = 16 * i + 8 * nt + 2 * tig;
+                const uint32_t val = pack_f16(out[mt][nt][2 * hr], out[mt][nt][2 * hr + 1]);
+                *reinterpret_cast<uint32_t *>(slot + (kind ? kTsUt + col * 144 + 2 * t : kTsWt + tc::wt_off(t, col))) = val;
+              }
+          }
           if (i + 1 < MT) acc_to_f16(out[mt][0], out[mt][1], 1.f, 1.f, 1.f, 1.f, Xf[i][mt]);
         }
       }
     }
+    if (LAYOUT == 1) continue;  // (the next block's first barrier orders the smem reuse)
     __syncthreads();
     // ---- -W and U to the slot in fragment order (16-byte lane runs, coalesced stores)
     for (int e = tid; e < 2 * C * 16; e += NT) {
@@ -465,31 +466,32 @@ __global__ void __launch_bounds__(kPrepThreads, 3) prep_kernel(ChunkParams p, in
       uint4 x;
       if (!which) {  // WN group (w, s, rh) = (f >> 8, (f >> 6) & 3, (f >> 5) & 1)
         const int w = f >> 8, sp = (f >> 6) & 3, rh = (f >> 5) & 1;
-        x = *reinterpret_cast<const uint4 *>(sm.Q + (16 * w + g + 8 * rh) * kP128 + 2 * (32 * sp + 8 * tg));
+        x = *reinterpret_cast<const uint4 *>(sw_el(sm.Q[0], HB, 16 * w + g + 8 * rh, 32 * sp + 8 * tg));
       } else {       // U group (b, w) = ((f >> 5) / MT, (f >> 5) % MT)
-        const int w = (f >> 5) % MT, b = (f >> 5) / MT;
-        const char *r0 = sm.V + (16 * w + g) * kP128 + 2 * (16 * b + 2 * tg);
-        x.x = *reinterpret_cast<const uint32_t *>(r0);                  // nt 0, rh 0
-        x.y = *reinterpret_cast<const uint32_t *>(r0 + 8 * kP128);      // nt 0, rh 1
-        x.z = *reinterpret_cast<const uint32_t *>(r0 + 16);             // nt 1, rh 0
-        x.w = *reinterpret_cast<const uint32_t *>(r0 + 8 * kP128 + 16); // nt 1, rh 1
+        const int w = (f >> 5) % MT, b = (f >> 5) / MT, r0 = 16 * w + g, c0 = 16 * b + 2 * tg;
+        x.x = *reinterpret_cast<const uint32_t *>(sw_el(sm.V[0], HB, r0, c0));          // nt 0, rh 0
+        x.y = *reinterpret_cast<const uint32_t *>(sw_el(sm.V[0], HB, r0 + 8, c0));      // nt 0, rh 1
+        x.z = *reinterpret_cast<const uint32_t *>(sw_el(sm.V[0], HB, r0, c0 + 8));      // nt 1, rh 0
+        x.w = *reinterpret_cast<const uint32_t *>(sw_el(sm.V[0], HB, r0 + 8, c0 + 8));  // nt 1, rh 1
       }
       *reinterpret_cast<uint4 *>((which ? u_out : wn_out) + 16 * f) = x;
     }
   }
+  if (!ok) report_status(p.err, GDN_STATUS_WAIT_TIMEOUT);
 }
 
 // ================================================================== pass 2
 // One CTA per (sequence, v-head, 16 value columns) walks the sequence's blocks in order.
-//   producer warp: per block, bulk (TMA) copies of the slot's chain operands and, for the
-//     outputs, a tensor-map TMA of the block's q rows and a bulk copy of A, into a
-//     3-stage shared-memory ring signalled on mbarriers.
+//   producer warp: per block, bulk (TMA) copies of the slot's chain operands, a
+//     tensor-map TMA of the block's k rows and, for the outputs, of its q rows and a bulk
+//     copy of A, into a 3-stage shared-memory ring signalled on mbarriers.
 //   chain warps 0-3: the state block S[:, cols] in fp32 registers for the whole sequence
 //     (read from state_in once, written to state_out once), warp w holding keys
 //     32w .. 32w+31.  Per block, for tokens 16w .. 16w+15 (w < C/16),
 //       D = U - W S          (fragment-ordered -W and U, S from a shared fp16 snapshot),
-//     D goes to shared memory (transposed), then each warp updates its keys,
-//       S <- e^(G_C) S + K~^T D,
+//     D and D~ = diag(e^(G_C - G)) D go to shared memory (transposed), then each warp
+//     updates its keys from the k rows as loaded,
+//       S <- e^(G_C) S + K^T D~,
 //     and writes its part of the next snapshot.
 //   output warps 4-7: for tokens 16ow .. 16ow+15, O = diag(e^G) Q S + A D from the same
 //     snapshot and the exchanged D.
@@ -519,9 +521,13 @@ __device__ __forceinline__ int swz_row(int r, int RB, int b) {
 template <int C>
 struct ChainStage {
   alignas(128) char WN[C * 256];        // -W
-  alignas(128) char KT[C * 256];        // K~^T
   alignas(128) char U[(C / 16) * 512];  // U of this CTA's 16 value columns
-  alignas(16) float DEC[2 * C];         // G, e^G
+  alignas(16) float DEC[3 * C];         // G, e^G, e^(G_C - G)
+};
+// The block's k rows (the state update's operand).
+template <int C>
+struct alignas(1024) KStage {
+  char K[2][C * 128];    // keys 0-63 | 64-127 (bf16, TMA 128-byte swizzle)
 };
 // The outputs' operands of one block.
 template <int C>
@@ -534,15 +540,23 @@ template <int C, int MODE>
 struct RecSmem {
   static constexpr int NST = MODE == 0 ? 3 : 2;  // ring depth
   ChainStage<C> cs[NST];
-  alignas(128) char Sn[2][kDVB * 256];  // S^T (fp16) [16 value cols][128 keys], by parity
-  alignas(128) char Dt[2][kDVB * 128];  // D^T (fp16) [16 value cols][C tokens], by parity
-  alignas(16) float S32[kD][kDVB + 4];  // fp32 staging of the state block
+  alignas(128) char Sn[2][kDVB * 256];   // S^T (fp16) [16 value cols][128 keys], by parity
+  alignas(128) char Dt[2][kDVB * 128];   // D^T (fp16) [16 value cols][C tokens], by parity
+  alignas(128) char Dst[2][kDVB * 128];  // D~^T, D~ = diag(e^(G_C - G)) D, likewise
+  alignas(16) float S32[kD][kDVB + 4];   // fp32 staging of the state block
   alignas(8) uint64_t full[NST], empty[NST];
 };
+// Shared memory of pass 2: RecSmem, then NST KStages, then (MODE 0) NST OutStages, each
+// 1024-byte aligned from a 1024-aligned base.
+template <int C, int MODE>
+__host__ __device__ constexpr size_t rec_base_bytes() {
+  return (sizeof(RecSmem<C, MODE>) + 1023) / 1024 * 1024;
+}
 template <int C, int MODE>
 constexpr size_t rec_smem_bytes() {
-  const size_t base = (sizeof(RecSmem<C, MODE>) + 1023) / 1024 * 1024;
-  return 1024 + base + (MODE == 0 ? 3 * sizeof(OutStage<C>) : 0);  // + alignment slack
+  constexpr int NST = RecSmem<C, MODE>::NST;
+  return 1024 + rec_base_bytes<C, MODE>() + NST * sizeof(KStage<C>) +
+         (MODE == 0 ? NST * sizeof(OutStage<C>) : 0);  // + alignment slack
 }
 
 __device__ __forceinline__ void put4(uint32_t (&d)[4], uint4 x) {
@@ -551,32 +565,6 @@ __device__ __forceinline__ void put4(uint32_t (&d)[4], uint4 x) {
   d[2] = x.z;
   d[3] = x.w;
 }
-template <int KW>
-__device__ __forceinline__ void lds_words(uint32_t (&d)[KW], const char *p) {
-  if constexpr (KW == 4) {
-    put4(d, *reinterpret_cast<const uint4 *>(p));
-  } else {
-    const uint2 x = *reinterpret_cast<const uint2 *>(p);
-    d[0] = x.x;
-    d[1] = x.y;
-  }
-}
-// Lane (gid, tig)'s token run of span `span` in row r of the swizzled D^T tile.
-template <int KW>
-__device__ __forceinline__ void lds_run(uint32_t (&d)[KW], const char *tile, int r, int span, int tig) {
-  lds_words<KW>(d, tile + swz_row(r, 128, 2 * (KW == 4 ? 32 * span + 8 * tig : 16 * span + 4 * tig)));
-}
-
-// 3-D tensor-map TMA load (box of the map) into shared memory, completion on `bar`.
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
-                                            uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
-      "{%2, %3, %4}], [%5];\n" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // Chain warp w's snapshot part: S^T rows (value columns) 0-15, keys 32w .. 32w+31, fp16.
 __device__ __forceinline__ void write_snapshot(const float (&Sa)[4][4], char *Sn, int w, int lane) {
   const int m = lane >> 3, r = lane & 7;
@@ -590,10 +578,9 @@ __device__ __forceinline__ void write_snapshot(const float (&Sa)[4][4], char *Sn
 // One block of a chain warp: D for its tokens, the exchange, its keys' state update and
 // snapshot.  MODE 0: output warps share the snapshots and D through named barriers.
 template <int C, int MODE>
-__device__ __forceinline__ void chain_block(int c, const ChainStage<C> &st, float (&Sa)[4][4],
-                                            RecSmem<C, MODE> &sm, int w, int lane, bool dwork,
-                                            bool with_u) {
-  using TS = TokSpan<C>;
+__device__ __forceinline__ void chain_block(int c, const ChainStage<C> &st, const KStage<C> &kst,
+                                            float (&Sa)[4][4], RecSmem<C, MODE> &sm, int w, int lane,
+                                            bool dwork, bool with_u) {
   const int gid = lane >> 2, tig = lane & 3, par = c & 1;
   if (dwork) {
     // four independent accumulations per n-tile (key spans s), two products deep each
@@ -631,48 +618,50 @@ __device__ __forceinline__ void chain_block(int c, const ChainStage<C> &st, floa
         D[nt][2 * rh + 1] = uu.y + ((d[0][nt][2 * rh + 1] + d[1][nt][2 * rh + 1]) +
                                     (d[2][nt][2 * rh + 1] + d[3][nt][2 * rh + 1]));
       }
-    // D^T: matrices m = 2nt + rh (tokens 16w + 8rh.., columns 8nt..) stored transposed
+    // D^T and D~^T: matrices m = 2nt + rh (tokens 16w + 8rh.., columns 8nt..) stored
+    // transposed
     const int m = lane >> 3, r = lane & 7;
-    stsm_x4_t(sm.Dt[par] + swz_row(8 * (m >> 1) + r, 128, 32 * w + 16 * (m & 1)),
-              pack_f16(D[0][0], D[0][1]), pack_f16(D[0][2], D[0][3]), pack_f16(D[1][0], D[1][1]),
+    char *dt = sm.Dt[par] + swz_row(8 * (m >> 1) + r, 128, 32 * w + 16 * (m & 1));
+    stsm_x4_t(dt, pack_f16(D[0][0], D[0][1]), pack_f16(D[0][2], D[0][3]), pack_f16(D[1][0], D[1][1]),
               pack_f16(D[1][2], D[1][3]));
+    const float ed0 = st.DEC[2 * C + 16 * w + gid], ed1 = st.DEC[2 * C + 16 * w + gid + 8];
+    stsm_x4_t(dt + (sm.Dst[par] - sm.Dt[par]), pack_f16(ed0 * D[0][0], ed0 * D[0][1]),
+              pack_f16(ed1 * D[0][2], ed1 * D[0][3]), pack_f16(ed0 * D[1][0], ed0 * D[1][1]),
+              pack_f16(ed1 * D[1][2], ed1 * D[1][3]));
   }
   bar_sync(kBarChain, kChain);
   if (MODE == 0) bar_arrive(kBarDReady + par, kPair);
 
-  // S^T <- e^(G_C) S^T + D^T K~ over keys 32w .. 32w+31: one fresh accumulation per
-  // token span, summed with the scaled state at the end
-  float X[TS::NSP][4][4];
+  // S^T <- e^(G_C) S^T + D~^T K over keys 32w .. 32w+31 (the k rows as loaded, bf16 ->
+  // fp16 in registers): two accumulations by token step parity, summed with the scaled
+  // state at the end
+  float X[2][4][4];
 #pragma unroll
-  for (int s = 0; s < TS::NSP; ++s)
+  for (int s = 0; s < 2; ++s)
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) X[s][nt][i] = 0.f;
+  const char *Kh = kst.K[w >> 1];  // keys 64 (w >> 1) .. +63
 #pragma unroll
-  for (int s = 0; s < TS::NSP; ++s) {
-    uint32_t a0[TS::KW], a1[TS::KW], kt[4][TS::KW];
-    lds_run<TS::KW>(a0, sm.Dt[par], gid, s, tig);
-    lds_run<TS::KW>(a1, sm.Dt[par], gid + 8, s, tig);
+  for (int e = 0; e < C / 16; ++e) {
+    uint32_t a[4];
+    ldsm_x4(a, sm.Dst[par] + swz_row((lane & 7) + ((lane >> 3) & 1) * 8, 128, 2 * (16 * e + (lane >> 4) * 8)));
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) lds_words<TS::KW>(kt[nt], st.KT + kt_off<C>(w, nt, s, lane));
+    for (int pr = 0; pr < 2; ++pr) {
+      uint32_t b[4];  // n-tiles keys 32w + 16pr .. +7 (b[0], b[1]) and +8 .. +15 (b[2], b[3])
+      ldb_kn<128>(b, Kh, 16 * e, 32 * (w & 1) + 16 * pr, lane);
 #pragma unroll
-    for (int e = 0; e < TS::KS; ++e) {
-      const uint32_t a[4] = {a0[2 * e], a1[2 * e], a0[2 * e + 1], a1[2 * e + 1]};
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) mma_f16(X[s][nt], a, kt[nt][2 * e], kt[nt][2 * e + 1]);
+      for (int i = 0; i < 4; ++i) b[i] = bf16x2_to_f16x2(b[i]);
+      mma_f16(X[e & 1][2 * pr], a, b[0], b[1]);
+      mma_f16(X[e & 1][2 * pr + 1], a, b[2], b[3]);
     }
   }
   const float gam = st.DEC[2 * C - 1];
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float x = X[0][nt][i];
-#pragma unroll
-      for (int s = 1; s < TS::NSP; ++s) x += X[s][nt][i];
-      Sa[nt][i] = fmaf(gam, Sa[nt][i], x);
-    }
+    for (int i = 0; i < 4; ++i) Sa[nt][i] = fmaf(gam, Sa[nt][i], X[0][nt][i] + X[1][nt][i]);
   // S_{c+1} into the other snapshot buffer once the output warps are done with block c - 1
   if (MODE == 0 && c >= 1) bar_sync(kBarDone + (par ^ 1), kPair);
   write_snapshot(Sa, sm.Sn[par ^ 1], w, lane);
@@ -751,18 +740,20 @@ __device__ __forceinline__ void out_block(int c, const ChainStage<C> &cst, const
 // producer, no outputs.
 template <int C, typename TO, int MODE>
 __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 ? 1 : 2)
-    recur_kernel(ChunkParams p, const __grid_constant__ CUtensorMap qmap) {
+    recur_kernel(ChunkParams p, const __grid_constant__ CUtensorMap kmap,
+                 const __grid_constant__ CUtensorMap qmap) {
   constexpr int NB = kD / kDVB, MT = C / 16, RC = row_c(C);
   constexpr int NT = MODE == 0 ? kPair + 32 : kChain + 32;
   constexpr int NST = RecSmem<C, MODE>::NST, PW = NT / 32 - 1;  // ring depth, producer warp
-  constexpr size_t SB = slot_bytes(C);
-  constexpr uint32_t kChainTx = (uint32_t)(2 * C * 256 + MT * 512 + 8 * C);
+  constexpr size_t SB = slot_stride(C);
+  constexpr uint32_t kChainTx = (uint32_t)(C * 256 + MT * 512 + 12 * C + 2 * C * 128);
   constexpr uint32_t kOutTx = (uint32_t)(2 * C * 128 + C * RC);
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   RecSmem<C, MODE> &sm = *reinterpret_cast<RecSmem<C, MODE> *>(base);
-  OutStage<C> *os = reinterpret_cast<OutStage<C> *>(base + (sizeof(RecSmem<C, MODE>) + 1023) / 1024 * 1024);
+  KStage<C> *ks = reinterpret_cast<KStage<C> *>(base + rec_base_bytes<C, MODE>());
+  OutStage<C> *os = reinterpret_cast<OutStage<C> *>(ks + NST);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   long long b = blockIdx.x;
@@ -813,9 +804,10 @@ __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 
         ChainStage<C> &cs = sm.cs[s];
         mbar_arrive_expect_tx(&sm.full[s], kChainTx + (MODE == 0 ? kOutTx : 0));
         bulk_g2s(cs.WN, src, C * 256, &sm.full[s]);
-        bulk_g2s(cs.KT, src + slot_kt_off(C), C * 256, &sm.full[s]);
         bulk_g2s(cs.U, src + slot_u_off(C) + u_off<C>(blk, 0, 0), MT * 512, &sm.full[s]);
-        bulk_g2s(cs.DEC, src + slot_dec_off(C), 8 * C, &sm.full[s]);
+        bulk_g2s(cs.DEC, src + slot_dec_off(C), 12 * C, &sm.full[s]);
+        tma_load_3d(ks[s].K[0], &kmap, 0, kh, bos + c * C, &sm.full[s]);
+        tma_load_3d(ks[s].K[1], &kmap, 64, kh, bos + c * C, &sm.full[s]);
         if (MODE == 0) {
           tma_load_3d(os[s].Q[0], &qmap, 0, kh, bos + c * C, &sm.full[s]);
           tma_load_3d(os[s].Q[1], &qmap, 64, kh, bos + c * C, &sm.full[s]);
@@ -841,7 +833,7 @@ __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % NST;
       ok = mbar_wait(&sm.full[s], (c / NST) & 1) && ok;
-      chain_block<C, MODE>(c, sm.cs[s], Sa, sm, w, lane, dwork, !maps);
+      chain_block<C, MODE>(c, sm.cs[s], ks[s], Sa, sm, w, lane, dwork, !maps);
       if (tid == 0) mbar_arrive(&sm.empty[s]);  // all chain warps are past the barrier
     }
     if (MODE == 0 && nchunks >= 1) bar_sync(kBarDone + ((nchunks - 1) & 1), kPair);
@@ -892,35 +884,43 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// Tensor map of q [T, Hk, 128] bf16 for boxes of 64 keys x 1 head x C tokens, 128-byte
-// swizzle (rows past T read as zero).
-cudaError_t q_tensor_map(CUtensorMap *map, const void *q, int total_tokens, int hk, int C) {
+// Tensor map of a [T, H, 128] bf16 tensor (q, k or v) for boxes of 64 features x 1 head x
+// C tokens, 128-byte swizzle (rows past T read as zero).
+cudaError_t tile_map(CUtensorMap *map, const void *x, int total_tokens, int heads, int C) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)hk, (cuuint64_t)total_tokens};
-  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)hk * kD * 2};
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)total_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
   const cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides,
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(x), dims, strides,
                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The q, k, v tile maps of a call (left zero without tokens: no block, no load).
+struct TileMaps {
+  CUtensorMap q, k, v;
+};
+template <int C>
+cudaError_t make_tile_maps(TileMaps &m, const ChunkParams &p) {
+  memset(&m, 0, sizeof(m));
+  if (p.total_tokens <= 0) return cudaSuccess;
+  cudaError_t err = tile_map(&m.q, p.q, p.total_tokens, p.hk, C);
+  if (err == cudaSuccess) err = tile_map(&m.k, p.k, p.total_tokens, p.hk, C);
+  if (err == cudaSuccess) err = tile_map(&m.v, p.v, p.total_tokens, p.hv, C);
+  return err;
+}
+
 template <int C, typename TO, int MODE>
-cudaError_t launch_recur(const ChunkParams &p, long long heads, cudaStream_t stream) {
+cudaError_t launch_recur(const ChunkParams &p, const TileMaps &m, long long heads, cudaStream_t stream) {
   constexpr size_t smem = rec_smem_bytes<C, MODE>();
   cudaError_t err = cudaFuncSetAttribute(recur_kernel<C, TO, MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  CUtensorMap qmap;
-  memset(&qmap, 0, sizeof(qmap));
-  if (MODE == 0 && p.total_tokens > 0) {  // (no block, no q load, without tokens)
-    err = q_tensor_map(&qmap, p.q, p.total_tokens, p.hk, C);
-    if (err != cudaSuccess) return err;
-  }
   const unsigned grid = (unsigned)((MODE == 1 ? 2 : 1) * heads * (kD / kDVB));
-  recur_kernel<C, TO, MODE><<<grid, MODE == 0 ? kPair + 32 : kChain + 32, smem, stream>>>(p, qmap);
+  recur_kernel<C, TO, MODE><<<grid, MODE == 0 ? kPair + 32 : kChain + 32, smem, stream>>>(p, m.k, m.q);
   return cudaGetLastError();
 }
 
@@ -937,25 +937,40 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
   long long per_head = (8LL * sms + heads - 1) / heads;
   per_head = max(1LL, min(per_head, max(1LL, max_chunks)));
 
+  TileMaps maps;
+  err = make_tile_maps<C>(maps, p);
+  if (err != cudaSuccess) return err;
+  // both passes at C = 64 with tc_pass2: pass 2 on the tcgen05 tensor cores (one CTA per
+  // chain) over slots in its operand layout; else the mma.sync pass 2 (recur_kernel)
+  constexpr int LT = C == 64 ? 1 : 0;
+  const bool tc2 = C == 64 && p.passes == 0 && p.tc_pass2;
   if (p.total_tokens > 0 && p.passes != 2 && p.passes != 3) {
-    const size_t s1 = sizeof(PrepSmem<C>);
-    err = cudaFuncSetAttribute(prep_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
-    if (err != cudaSuccess) return err;
-    prep_kernel<C><<<(unsigned)(heads * per_head), kPrepThreads, s1, stream>>>(p, (int)per_head);
-    err = cudaGetLastError();
+    const size_t s1 = 1024 + sizeof(PrepSmem<C>);  // + alignment slack
+    const unsigned grid = (unsigned)(heads * per_head);
+    if (tc2) {
+      err = cudaFuncSetAttribute(prep_kernel<C, LT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+      if (err == cudaSuccess)
+        prep_kernel<C, LT><<<grid, kPrepThreads, s1, stream>>>(p, (int)per_head, maps.k, maps.q, maps.v);
+    } else {
+      err = cudaFuncSetAttribute(prep_kernel<C, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+      if (err == cudaSuccess)
+        prep_kernel<C, 0><<<grid, kPrepThreads, s1, stream>>>(p, (int)per_head, maps.k, maps.q, maps.v);
+    }
+    if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
+  if (tc2) return launch_tc_chain(p, stream);
   if (p.passes == 1) return cudaSuccess;
-  if (p.passes == 3) return launch_recur<C, float, 1>(p, heads, stream);
-  return p.o_fp32 ? launch_recur<C, float, 0>(p, heads, stream)
-                  : launch_recur<C, __nv_bfloat16, 0>(p, heads, stream);
+  if (p.passes == 3) return launch_recur<C, float, 1>(p, maps, heads, stream);
+  return p.o_fp32 ? launch_recur<C, float, 0>(p, maps, heads, stream)
+                  : launch_recur<C, __nv_bfloat16, 0>(p, maps, heads, stream);
 }
 
 }  // namespace
 
 size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk) {
   const size_t slots = (size_t)hv * ((size_t)total_tokens / chunk + num_seqs);
-  return 256 + slots * slot_bytes(chunk);
+  return 256 + slots * slot_stride(chunk);
 }
 
 cudaError_t launch_chunk_bf16(const ChunkParams &p, cudaStream_t stream) {

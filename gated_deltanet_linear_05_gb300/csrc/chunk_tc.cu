@@ -28,6 +28,8 @@
 // Precision: the Gram MMA takes the exact bf16 q, k; every other product takes fp16
 // operands (q, k, v exact; S, D, W, A rounded to 11 bits for the product) with fp32
 // accumulation, as in the mma.sync paths.
+#include <stddef.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -35,6 +37,10 @@
 namespace gdn {
 
 namespace {
+
+using tc::at_off;
+using tc::t64_off;
+using tc::wt_off;
 
 constexpr int kTcC = 64;                 // block length of this kernel
 constexpr int kTcThreads = 32 * 13;      // 4 E + 8 P warps + the MMA issuer warp
@@ -51,22 +57,10 @@ constexpr int kTmDT = 320;   // D^T fp16 pairs (A of P4)
 constexpr int kTmDD = 352;   // (D diag(e^(G_T - G)))^T fp16 pairs (A of P2)
 constexpr int kTmG = 384;    // Gram [K; Q] K^T fp32 [128 rows][64 tokens]
 
-// Byte offsets in the no-swizzle core-matrix layouts (8 rows x 16 B per core matrix):
-// [K; Q] bf16, 128 rows (tokens of k, then of q) x 128 keys, K-major
+// [K; Q] bf16, 128 rows (tokens of k, then of q) x 128 keys, K-major (no-swizzle
+// core-matrix layout, 8 rows x 16 B per core matrix)
 __device__ __forceinline__ int kq_off(int r, int key) {
   return (key >> 3) * 2048 + (r >> 3) * 128 + (r & 7) * 16 + (key & 7) * 2;
-}
-// 64 tokens x 128 keys fp16, K-major (diag(e^G) Q and K)
-__device__ __forceinline__ int t64_off(int t, int key) {
-  return (key >> 3) * 1024 + (t >> 3) * 128 + (t & 7) * 16 + (key & 7) * 2;
-}
-// W^T fp16, MN-major over tokens (B of P1 with N = tokens, K = keys)
-__device__ __forceinline__ int wt_off(int t, int key) {
-  return (key >> 3) * 1024 + (t >> 3) * 128 + (key & 7) * 16 + (t & 7) * 2;
-}
-// A fp16 [t][j] 64 x 64, K-major over j
-__device__ __forceinline__ int at_off(int t, int j) {
-  return (j >> 3) * 1024 + (t >> 3) * 128 + (t & 7) * 16 + (j & 7) * 2;
 }
 
 struct TcSmem {
@@ -627,6 +621,284 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_kernel(ChunkParams p) {
   }
 }
 
+// ============================================================ the chain over pass-1 slots
+// tc_chain_kernel: pass 2 of the two-pass path.  The state-free operands of every block
+// come from its workspace slot (written by pass 1 in the kTs* layout), so the CTA runs
+// only the state chain and the outputs, with the products of tc_kernel:
+//   P1: D^T  = -S^T W^T,  P3: R^T = S^T (diag(e^G) Q)^T,  P2: S^T += Dd^T K,  P4: O^T = R^T + D^T A^T
+// Warp roles:
+//   warps 0-3 (E, thread j = value column j = TMEM lane j): D = U + P1 into the fp16
+//     operands of P2 and P4; the state epilogue after P2: first the fp16 copy of S (the
+//     A operand of the next block's P1 and P3), then S pre-scaled by the next block's
+//     e^(G_C) (P2 accumulates on top of it).  Only these two steps sit on the chain.
+//   warps 4-7 (O, same lanes): the block's outputs O^T after P4 -> o.
+//   warp 8 lane 0: the producer, each block's slot into a ring stage with one bulk copy.
+//   warp 9 lane 0: issues every MMA and its commits.
+constexpr int kChNst = 2;                // ring depth
+constexpr int kChThreads = 32 * 10;
+constexpr int kBarO = 3;                 // named barrier of the O group
+
+struct alignas(128) ChainSlot {          // one block's operands, as in the slot (kTs*)
+  char Wt[16384], Qt[16384], K16[16384], At[8192], Ut[kD * 144];
+  float dec[3][kTcC];                    // G, e^G, e^(G_C - G)
+};
+static_assert(sizeof(ChainSlot) == kTsBytes && offsetof(ChainSlot, Qt) == kTsQt &&
+                  offsetof(ChainSlot, K16) == kTsK && offsetof(ChainSlot, At) == kTsAt &&
+                  offsetof(ChainSlot, Ut) == kTsUt && offsetof(ChainSlot, dec) == kTsDec,
+              "slot layout");
+struct ChainSmem {
+  ChainSlot st[kChNst];
+  alignas(8) uint64_t full[kChNst], empty[kChNst];
+  alignas(8) uint64_t p1_done, p2_done, p4_done, d_ready, s_ready, r_free;
+  uint32_t tmem;
+};
+
+template <typename TO>
+__global__ void __launch_bounds__(kChThreads, 1) tc_chain_kernel(ChunkParams p) {
+  constexpr int C = kTcC;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  ChainSmem &sm = *reinterpret_cast<ChainSmem *>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = blockIdx.x / p.hv, h = blockIdx.x - n * p.hv;
+  int bos, eos;
+  seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
+  const int nchunks = (eos - bos + C - 1) / C;
+  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD;
+  const char *slot0 = p.slot_ws + ((size_t)h * p.nslots + (size_t)(bos / C + n)) * slot_stride(C);
+
+  if (nchunks == 0) {  // empty sequence: the state passes through
+    for (int e = tid; e < kD * kD; e += kChThreads)
+      p.state_out[sbase + e] = p.state_in ? p.state_in[sbase + e] : 0.f;
+    return;
+  }
+  if (warp == 0) tc::alloc<512>(&sm.tmem);
+  if (tid == 32) {
+    for (int s = 0; s < kChNst; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 2);  // the last MMA reading the stage, the E group
+    }
+    mbar_init(&sm.p1_done, 1);
+    mbar_init(&sm.p2_done, 1);
+    mbar_init(&sm.p4_done, 1);
+    mbar_init(&sm.d_ready, 1);
+    mbar_init(&sm.s_ready, 1);
+    mbar_init(&sm.r_free, 1);
+    mbar_fence_init();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = sm.tmem;
+  bool ok = true;
+  auto wait = [&](uint64_t *bar, uint32_t par) { if (ok) ok = mbar_wait(bar, par); };
+
+  if (warp == 8) {
+    // ======================= producer: block c's slot into stage c % kChNst
+    if (lane == 0) {
+#pragma unroll 1
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kChNst;
+        if (c >= kChNst) wait(&sm.empty[s], ((c / kChNst) - 1) & 1);
+        mbar_arrive_expect_tx(&sm.full[s], (uint32_t)kTsBytes);
+        bulk_g2s(&sm.st[s], slot0 + (size_t)c * slot_stride(C), (uint32_t)kTsBytes, &sm.full[s]);
+      }
+    }
+  } else if (warp < 4) {
+    // ======================= E group: thread j owns value column j (TMEM lane j)
+    const int j = tid;
+    // initial state: S^T row j = S[:, j]; fp16 copy for P1/P3, fp32 scaled by e^(G_C) of
+    // block 0 (P2 accumulates on top of it)
+    wait(&sm.full[0], 0);
+    {
+      const float eg = sm.st[0].dec[1][C - 1];
+#pragma unroll 1
+      for (int s4 = 0; s4 < 4; ++s4) {
+        float x[32];
+        uint32_t r32[32], h16[16];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          x[i] = p.state_in ? p.state_in[sbase + (size_t)(32 * s4 + i) * kD + j] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) h16[i] = pack_f16(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r32[i] = __float_as_uint(x[i] * eg);
+        tc::st16(tc::lane_addr(tmem, warp, kTmST + 16 * s4), h16);
+        tc::st32(tc::lane_addr(tmem, warp, kTmS + 32 * s4), r32);
+      }
+      tc::wait_st();
+    }
+    tc::fence_before();
+    bar_sync(kBarE, kTcE);
+    if (tid == 0) mbar_arrive(&sm.s_ready);
+
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kChNst;
+      const ChainSlot &st = sm.st[s];
+      // ---- D = U + (-S W): fp16 D^T and (D diag(e^(G_C - G)))^T into tensor memory
+      wait(&sm.full[s], (c / kChNst) & 1);
+      wait(&sm.p1_done, c & 1);
+      tc::fence_after();
+      {
+        const float *ED = st.dec[2];
+        const uint4 *urow = reinterpret_cast<const uint4 *>(st.Ut + j * 144);
+        uint32_t a[64];
+        tc::ld32(tc::lane_addr(tmem, warp, kTmD), *reinterpret_cast<uint32_t(*)[32]>(a));
+        tc::ld32(tc::lane_addr(tmem, warp, kTmD + 32), *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+        tc::wait_ld();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {  // tokens 32 hh .. 32 hh + 31
+          uint32_t dt[16], dd[16];
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+            const uint4 u4 = urow[4 * hh + g8];
+            const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tl = 8 * g8 + 2 * e, t = 32 * hh + tl;
+              const float2 u = f16x2_to_float2(uw[e]);
+              const float d0 = u.x + __uint_as_float(a[t]), d1 = u.y + __uint_as_float(a[t + 1]);
+              dt[tl >> 1] = pack_f16(d0, d1);
+              dd[tl >> 1] = pack_f16(d0 * ED[t], d1 * ED[t + 1]);
+            }
+          }
+          tc::st16(tc::lane_addr(tmem, warp, kTmDT + 16 * hh), dt);
+          tc::st16(tc::lane_addr(tmem, warp, kTmDD + 16 * hh), dd);
+        }
+        tc::wait_st();
+      }
+      tc::fence_before();
+      bar_sync(kBarE, kTcE);
+      if (tid == 0) {
+        mbar_arrive(&sm.d_ready);
+        if (c + kChNst < nchunks) mbar_arrive(&sm.empty[s]);  // U^T and the decays of stage s are read
+      }
+
+      // ---- state: S after P2 -> fp16 copy for the next block (released first), then
+      //      pre-scaled by the next block's e^(G_C); after the last block, S -> state_out
+      wait(&sm.p2_done, c & 1);
+      tc::fence_after();
+      if (c + 1 == nchunks) {
+#pragma unroll 1
+        for (int s4 = 0; s4 < 4; ++s4) {
+          uint32_t r32[32];
+          tc::ld32(tc::lane_addr(tmem, warp, kTmS + 32 * s4), r32);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) p.state_out[sbase + (size_t)(32 * s4 + i) * kD + j] = __uint_as_float(r32[i]);
+        }
+      } else {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {  // keys 64 hf .. 64 hf + 63
+          uint32_t r[64], h16[32];
+          tc::ld32(tc::lane_addr(tmem, warp, kTmS + 64 * hf), *reinterpret_cast<uint32_t(*)[32]>(r));
+          tc::ld32(tc::lane_addr(tmem, warp, kTmS + 64 * hf + 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) h16[i] = pack_f16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          tc::st32(tc::lane_addr(tmem, warp, kTmST + 32 * hf), h16);
+        }
+        tc::wait_st();
+        tc::fence_before();
+        bar_sync(kBarE, kTcE);
+        if (tid == 0) mbar_arrive(&sm.s_ready);  // P1 and P3 of block c + 1 may start
+        const int s1 = (c + 1) % kChNst;
+        wait(&sm.full[s1], ((c + 1) / kChNst) & 1);
+        const float egn = sm.st[s1].dec[1][C - 1];
+#pragma unroll 1
+        for (int s4 = 0; s4 < 4; ++s4) {
+          uint32_t r32[32];
+          tc::ld32(tc::lane_addr(tmem, warp, kTmS + 32 * s4), r32);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r32[i] = __float_as_uint(__uint_as_float(r32[i]) * egn);
+          tc::st32(tc::lane_addr(tmem, warp, kTmS + 32 * s4), r32);
+        }
+        tc::wait_st();  // (ordered before P2 of block c + 1 by the d_ready hand-off)
+      }
+    }
+  } else if (warp < 8) {
+    // ======================= O group: the block's outputs, O^T row j -> o[t][h][j]
+    const int j = tid - 128;
+    TO *o = static_cast<TO *>(p.o);
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      const int tok0 = bos + c * C, L = min(C, eos - tok0);
+      wait(&sm.p4_done, c & 1);
+      tc::fence_after();
+      uint32_t r0[32], r1[32];
+      tc::ld32(tc::lane_addr(tmem, warp, kTmR), r0);
+      tc::ld32(tc::lane_addr(tmem, warp, kTmR + 32), r1);
+      tc::wait_ld();
+      tc::fence_before();
+      bar_sync(kBarO, kTcE);
+      if (j == 0) mbar_arrive(&sm.r_free);  // the accumulator is read: P3 of block c + 1 may start
+      TO *dst = o + ((size_t)tok0 * p.hv + h) * kD + j;
+      const size_t tstride = (size_t)p.hv * kD;
+#pragma unroll
+      for (int t = 0; t < C; ++t) {
+        if (t < L) Elem<TO>::store(dst, __uint_as_float(t < 32 ? r0[t & 31] : r1[t & 31]));
+        dst += tstride;
+      }
+    }
+  } else if (warp == 9 && lane == 0) {
+    // ======================= MMA issuer
+    constexpr uint32_t idP1 = tc::idesc(128, 64, 0, 1, 1);  // -S^T W^T, W^T MN-major
+    constexpr uint32_t idP3 = tc::idesc(128, 64, 0, 0, 0);  // S^T (diag(e^G) Q)^T
+    constexpr uint32_t idP2 = tc::idesc(128, 128, 0, 0, 1); // Dd^T K, K MN-major over keys
+    constexpr uint32_t idP4 = tc::idesc(128, 64, 0, 0, 0);  // D^T A^T
+#pragma unroll 1
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kChNst;
+      const uint32_t sWt = smem_u32(sm.st[s].Wt), sQt = smem_u32(sm.st[s].Qt);
+      const uint32_t sK = smem_u32(sm.st[s].K16), sAt = smem_u32(sm.st[s].At);
+      wait(&sm.full[s], (c / kChNst) & 1);
+      wait(&sm.s_ready, c & 1);
+      tc::fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc::mma_ts(tmem + kTmD, tmem + kTmST + 8 * kk, tc::sdesc(sWt + kk * 2048, 1024, 128), idP1, kk > 0);
+      tc::commit(&sm.p1_done);
+      if (c >= 1) wait(&sm.r_free, (c - 1) & 1);
+      tc::fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc::mma_ts(tmem + kTmR, tmem + kTmST + 8 * kk, tc::sdesc(sQt + kk * 2048, 1024, 128), idP3, kk > 0);
+      wait(&sm.d_ready, c & 1);
+      tc::fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // 16 tokens per step
+        tc::mma_ts(tmem + kTmS, tmem + kTmDD + 8 * kk, tc::sdesc(sK + kk * 256, 128, 1024), idP2, 1);
+      tc::commit(&sm.p2_done);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_ts(tmem + kTmR, tmem + kTmDT + 8 * kk, tc::sdesc(sAt + kk * 2048, 1024, 128), idP4, 1);
+      tc::commit(&sm.p4_done);
+      // every MMA reading stage s is done (only where the producer refills it: no arrive
+      // may land after the CTA has finished)
+      if (c + kChNst < nchunks) tc::commit(&sm.empty[s]);
+    }
+  }
+
+  if (!ok) report_status(p.err, GDN_STATUS_WAIT_TIMEOUT);
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after();
+    tc::dealloc<512>(tmem);
+  }
+}
+
+template <typename TO>
+cudaError_t launch_tc_chain_t(const ChunkParams &p, cudaStream_t stream) {
+  const size_t smem = sizeof(ChainSmem);
+  cudaError_t err =
+      cudaFuncSetAttribute(tc_chain_kernel<TO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  tc_chain_kernel<TO><<<(unsigned)((long long)p.num_seqs * p.hv), kChThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <typename TO>
 cudaError_t launch_tc_t(const ChunkParams &p, cudaStream_t stream) {
   const size_t smem = sizeof(TcSmem);
@@ -638,6 +910,11 @@ cudaError_t launch_tc_t(const ChunkParams &p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_tc_chain(const ChunkParams &p, cudaStream_t stream) {
+  if ((long long)p.num_seqs * p.hv == 0) return cudaSuccess;
+  return p.o_fp32 ? launch_tc_chain_t<float>(p, stream) : launch_tc_chain_t<__nv_bfloat16>(p, stream);
+}
 
 cudaError_t launch_chunk_tc(const ChunkParams &p, cudaStream_t stream) {
   if ((long long)p.num_seqs * p.hv == 0) return cudaSuccess;

@@ -130,6 +130,21 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) 
   }
   return done != 0;
 }
+// Orders this thread's (and, after a barrier, the CTA's) generic-proxy accesses to shared
+// memory before later async-proxy ones (a bulk or tensor copy into the same bytes).
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+// 3-D tensor-map (TMA) load of the map's box at coordinates (x, y, z) into shared memory
+// (1024-byte aligned for a 128-byte swizzle), completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, int y, int z,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4}], [%5];\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
 // Bulk (TMA) copy global -> shared of `bytes` (multiple of 16, both ends 16-byte
 // aligned); completion is counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,

@@ -56,9 +56,10 @@ gdn_status check_shape(const gdn_shape *s, bool needs_chunk) {
   if (s->qkv_dtype != GDN_F32 && s->qkv_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if (s->o_fp32 != 0 && s->o_fp32 != 1) return GDN_ERR_INVALID_ARG;
   if (s->algo != GDN_ALGO_AUTO && s->algo != GDN_ALGO_TWO_PASS && s->algo != GDN_ALGO_SINGLE_PASS &&
-      s->algo != GDN_ALGO_TENSOR_MEMORY && s->algo != GDN_ALGO_RECURRENT)
+      s->algo != GDN_ALGO_TENSOR_MEMORY && s->algo != GDN_ALGO_RECURRENT &&
+      s->algo != GDN_ALGO_TWO_PASS_TENSOR)
     return GDN_ERR_INVALID_ARG;
-  if (s->algo == GDN_ALGO_TENSOR_MEMORY && needs_chunk &&
+  if ((s->algo == GDN_ALGO_TENSOR_MEMORY || s->algo == GDN_ALGO_TWO_PASS_TENSOR) && needs_chunk &&
       (s->chunk != 64 || s->qkv_dtype != GDN_BF16))
     return GDN_ERR_UNSUPPORTED;
   if (needs_chunk && s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return GDN_ERR_UNSUPPORTED;
@@ -109,7 +110,7 @@ gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_E
 // bf16 chunked pass: one CTA per (sequence, v-head) without workspace, or two passes
 bool single_pass(const gdn_shape *s) {
   if (s->algo == GDN_ALGO_SINGLE_PASS || s->algo == GDN_ALGO_TENSOR_MEMORY) return true;
-  if (s->algo == GDN_ALGO_TWO_PASS) return false;
+  if (s->algo == GDN_ALGO_TWO_PASS || s->algo == GDN_ALGO_TWO_PASS_TENSOR) return false;
   return (long long)s->num_seqs * s->num_v_heads >= GDN_SINGLE_PASS_MIN_HEADS;
 }
 
@@ -146,6 +147,7 @@ gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes,
   p.err = status_word();
   p.delta = delta;
   p.passes = passes;
+  p.tc_pass2 = s->algo == GDN_ALGO_TWO_PASS_TENSOR;
   p.state_in2 = state_in2;
   p.state_out2 = state_out2;
   p.num_seqs = s->num_seqs;

@@ -34,14 +34,14 @@ struct ChunkParams {
   // Workspace of the two-pass bf16 path (chunk_bf16.cu): one slot per (v-head, block);
   // block c of sequence n uses slot bos_n / C + n + c, which is unique and below
   // nslots = total_tokens / C + num_seqs.  A slot holds the block's state-free operands,
-  // each region one bulk copy for pass 2 (chunk_bf16.cu; rows past the sequence end are
-  // zero).  WN, KT and U are in the fragment order pass 2's chain warps read (each warp's
-  // 32 lane runs contiguous):
+  // each region one bulk copy for pass 2 (chunk_bf16.cu; rows of W and U past the
+  // sequence end are zero, A's are never used).  WN and U are in the fragment order pass
+  // 2's chain warps read (each warp's 32 lane runs contiguous):
   //   WN  fp16, C x 128       -W, W = (I+N)^-1 diag(beta e^G) K (rows: tokens)
-  //   KT  fp16, 128 x C       (diag(e^(G_C - G)) K)^T (rows: keys)
-  //   A   fp16 [C][2C + 16 B] decay-masked causal Q K^T, padded rows
+  //   A   fp16 [C][2C + 16 B] decay-masked causal Q K^T, padded rows (the 16x16 blocks
+  //                           above the diagonal are never written nor read)
   //   U   fp16, C x 128       U = (I+N)^-1 diag(beta) V (rows: tokens), per 16-column block
-  //   DEC fp32 [2][C]         G (in-block cumsum), e^G
+  //   DEC fp32 [3][C]         G (in-block cumsum), e^G, e^(G_C - G)
   int nslots;
   char *slot_ws;      // Hv * nslots slots of slot_bytes(C) bytes, 128-byte aligned
   unsigned int *err;  // the library's device status word (GDN_STATUS_* bits), or NULL
@@ -49,6 +49,7 @@ struct ChunkParams {
   // split's state chains -- from state_in, and with U = 0 from state_in2 -- on the slots
   // of a pass 1 run with these q, k, v, g, beta; else both passes)
   int passes;
+  bool tc_pass2;  // both passes at C = 64: pass 2 on the tensor cores (chunk_tc.cu)
   const float *state_in2;
   float *state_out2;
 };
@@ -58,12 +59,22 @@ struct ChunkParams {
 constexpr int kP128 = 272;
 __host__ __device__ constexpr int row_c(int C) { return 2 * C + 16; }
 // Slot layout offsets (bytes) for block length C.
-__host__ __device__ constexpr size_t slot_kt_off(int C) { return (size_t)C * 256; }
-__host__ __device__ constexpr size_t slot_a_off(int C) { return slot_kt_off(C) + (size_t)C * 256; }
+__host__ __device__ constexpr size_t slot_a_off(int C) { return (size_t)C * 256; }
 __host__ __device__ constexpr size_t slot_u_off(int C) { return slot_a_off(C) + (size_t)C * row_c(C); }
 __host__ __device__ constexpr size_t slot_dec_off(int C) { return slot_u_off(C) + (size_t)C * 256; }
 __host__ __device__ constexpr size_t slot_bytes(int C) {
-  return (slot_dec_off(C) + (size_t)8 * C + 127) / 128 * 128;
+  return (slot_dec_off(C) + (size_t)12 * C + 127) / 128 * 128;
+}
+// Slot layout of the tensor-memory pass 2 (block length 64, chunk_tc.cu): the chain's
+// operands in the shared-memory layouts of its MMAs (tc.cuh), copied by one bulk copy:
+//   Wt  W^T fp16, MN-major over tokens (wt_off)      Qt  diag(e^G) Q fp16 (t64_off)
+//   K   k fp16 (t64_off)                             At  A fp16, zero above the diagonal (at_off)
+//   Ut  U^T fp16 [value col][token], 144-byte rows   DEC fp32 [3][64] G, e^G, e^(G_C - G)
+constexpr size_t kTsWt = 0, kTsQt = 16384, kTsK = 32768, kTsAt = 49152, kTsUt = 57344,
+                 kTsDec = 75776, kTsBytes = 76544;
+// Distance between slots: room for either layout at C = 64.
+__host__ __device__ constexpr size_t slot_stride(int C) {
+  return C == 64 && kTsBytes > slot_bytes(C) ? kTsBytes : slot_bytes(C);
 }
 
 // The block's input prologue (block_io.cu): causal conv + SiLU over [q | k | v] raw
@@ -166,6 +177,9 @@ size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk);
 
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_chunk_bf16(const ChunkParams &p, cudaStream_t stream);
+// Pass 2 of the two-pass path on the tcgen05 tensor cores (chunk_tc.cu): one CTA per
+// (sequence, v-head) over slots in the kTs* layout written by pass 1.
+cudaError_t launch_tc_chain(const ChunkParams &p, cudaStream_t stream);
 cudaError_t launch_chunk_fused(const ChunkParams &p, cudaStream_t stream);
 cudaError_t launch_chunk_tc(const ChunkParams &p, cudaStream_t stream);
 cudaError_t launch_chunk_f32(const ChunkParams &p, cudaStream_t stream);

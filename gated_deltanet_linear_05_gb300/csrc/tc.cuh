@@ -83,6 +83,22 @@ __device__ __forceinline__ void dealloc(uint32_t base) {
                : "memory");
 }
 
+// Byte offsets of the 64-token operands in the no-swizzle core-matrix layouts (8 rows x
+// 16 B per core matrix), shared by the tensor-memory kernels and the two-pass path's
+// pass 1, which writes them to its workspace slots:
+// 64 tokens x 128 keys fp16, K-major over keys (diag(e^G) Q and K)
+__device__ __forceinline__ int t64_off(int t, int key) {
+  return (key >> 3) * 1024 + (t >> 3) * 128 + (t & 7) * 16 + (key & 7) * 2;
+}
+// W^T fp16, MN-major over tokens (B of D^T = -S^T W^T with N = tokens, K = keys)
+__device__ __forceinline__ int wt_off(int t, int key) {
+  return (key >> 3) * 1024 + (t >> 3) * 128 + (key & 7) * 16 + (t & 7) * 2;
+}
+// A fp16 [t][j] 64 x 64, K-major over j
+__device__ __forceinline__ int at_off(int t, int j) {
+  return (j >> 3) * 1024 + (t >> 3) * 128 + (t & 7) * 16 + (j & 7) * 2;
+}
+
 // Address of column `col` of this warp's 32-lane quarter (warp % 4).
 __device__ __forceinline__ uint32_t lane_addr(uint32_t base, int warp, int col) {
   return base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)col;

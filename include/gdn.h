@@ -113,13 +113,19 @@ typedef enum {
  *                accurate schedule and the slowest: the per-token reductions over the keys
  *                cost several times the chunk schedules' tensor-core work from 16 tokens
  *                up.  AUTO never picks it.
+ *   TWO_PASS_TENSOR the two-pass schedule with its second pass on the tcgen05 tensor
+ *                cores: the first pass writes each block's operands in the layouts of the
+ *                tensor-core products (a larger workspace slot), the second runs one CTA
+ *                per (sequence, v-head) with the state in tensor memory.  Block length 64
+ *                and bf16 q/k/v only (else GDN_ERR_UNSUPPORTED).  AUTO does not pick it.
  * All give results within the same bounds; they are not bit-identical to each other. */
 typedef enum {
   GDN_ALGO_AUTO = 0,
   GDN_ALGO_TWO_PASS = 1,
   GDN_ALGO_SINGLE_PASS = 2,
   GDN_ALGO_TENSOR_MEMORY = 3,
-  GDN_ALGO_RECURRENT = 4
+  GDN_ALGO_RECURRENT = 4,
+  GDN_ALGO_TWO_PASS_TENSOR = 5
 } gdn_algo;
 #define GDN_SINGLE_PASS_MIN_HEADS 128
 

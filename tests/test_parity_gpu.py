@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 # the schedules of the bf16 chunked pass (f32 q/k/v: the fp32 kernel, or the token loop)
-ALGOS = {"two_pass": 1, "single_pass": 2, "tensor_memory": 3, "recurrent": 4}
+ALGOS = {"two_pass": 1, "single_pass": 2, "tensor_memory": 3, "recurrent": 4, "two_pass_tensor": 5}
 # schedules built for every block length (tensor_memory: 64-token blocks only)
 ALGOS_ANY_C = ["two_pass", "single_pass", "recurrent"]
 
