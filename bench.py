@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "GDN prefill tokens/s (%TC roofline); decode state GB/s (%HBM peak)"
 D = 128
 EXTRA_ROWS = ("decode", "decode_block", "verify", "varlen", "prologue", "gated_rmsnorm", "accept",
-              "split")
+              "split", "schedules")
 
 
 def parse():
@@ -242,6 +242,7 @@ def run_gdn(args):
                 "decode_block": lambda: bench_decode_block(torch, gdn, gi, device, pk, args),
                 "verify": lambda: bench_verify(torch, gdn, gi, device, pk, args, flush),
                 "varlen": lambda: bench_varlen(torch, gdn, gi, device, pk, args, flush),
+                "schedules": lambda: bench_schedules(torch, gdn, gi, device, pk, args, flush),
                 "prologue": lambda: bench_prologue(torch, gdn, gi, device, pk, args, flush),
                 "gated_rmsnorm": lambda: bench_gated_rmsnorm(torch, gdn, gi, device, pk, args, flush),
                 "accept": lambda: bench_accept(torch, gdn, gi, device, pk, args, flush),
@@ -264,11 +265,11 @@ def run_gdn(args):
                    "l2": "flushed (512 MiB write) before every timed step",
                    "parallelism": "dp%d (independent batches per GPU)" % world},
         # traffic: DRAM bytes of the step's two kernels from the committed ncu capture
-        # (pass 1 58.6 MB + pass 2 80.3 MB; ncu flushes caches between kernels, so the
+        # (pass 1 54.0 MB + pass 2 80.3 MB; ncu flushes caches between kernels, so the
         # workspace round trip counts as DRAM traffic there)
-        "roofline": roofline("hbm", gbs, pk["hbm"], "GB/s", traffic=138.9e6),
+        "roofline": roofline("hbm", gbs, pk["hbm"], "GB/s", traffic=134.3e6),
         "roofline_scope": "one gdn_prefill_chunked call (pass 1 + pass 2); the dominant "
-                          "kernel, pass 2, takes ~62 of its ~99 us",
+                          "kernel, pass 2, takes ~61 of its ~93 us",
         "tensor": {"achieved": round(tfs, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                    "frac": round(tfs / pk["bf16"], 4), "algorithmic_flops": flops},
         "algorithmic_bytes": byts,
@@ -423,7 +424,7 @@ def bench_decode_block(torch, gdn, gi, device, pk, args):
 
 
 SCHEDULES = (("two_pass", 1), ("single_pass", 2), ("tensor_memory", 3),  # C = 64 only
-             ("recurrent", 4))
+             ("recurrent", 4), ("two_pass_tensor", 5))                  # C = 64 only
 
 
 def bench_chunked_schedules(torch, gdn, d, wl, chunk, fn, op, n, flush):
@@ -432,7 +433,7 @@ def bench_chunked_schedules(torch, gdn, d, wl, chunk, fn, op, n, flush):
     o = torch.empty_like(d["v"])
     res = {}
     for name, algo in SCHEDULES:
-        if algo == 3 and chunk != 64:
+        if algo in (3, 5) and chunk != 64:
             continue
         shape = gdn.make_shape(wl.num_seqs, wl.total_tokens, wl.num_k_heads, wl.num_v_heads,
                                chunk=chunk, algo=algo)
@@ -449,6 +450,19 @@ def bench_chunked_schedules(torch, gdn, d, wl, chunk, fn, op, n, flush):
     many = wl.num_seqs * wl.num_v_heads >= gdn.GDN_SINGLE_PASS_MIN_HEADS
     auto = ("tensor_memory" if chunk == 64 else "single_pass") if many else "two_pass"
     return res, auto
+
+
+def bench_schedules(torch, gdn, gi, device, pk, args, flush):
+    """The headline prefill (B=1, H=16, T=4096, C=64) under every bf16 schedule, L2 flushed
+    before each step; AUTO takes the two-pass one for these 16 (sequence, head) pairs."""
+    wl = gi.prefill_t4096_h16()
+    d = dev_inputs(gi.make_inputs(wl), torch, device)
+    n = max(5, min(args.steps, 30))
+    res, auto = bench_chunked_schedules(torch, gdn, d, wl, 64, gdn.gdn_prefill_chunked,
+                                        gdn.GDN_OP_PREFILL, n, flush)
+    return {"workload": wl.name, "schedule": auto,
+            "us_per_step_by_schedule": {k: round(v * 1e3, 2) for k, v in res.items()},
+            "gpu_launches": n * (len(res) + 2)}
 
 
 def bench_verify(torch, gdn, gi, device, pk, args, flush):
