@@ -494,7 +494,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
 //       S <- e^(G_C) S + K^T D~,
 //     and writes its part of the next snapshot.
 //   output warps 4-7: for tokens 16ow .. 16ow+15, O = diag(e^G) Q S + A D from the same
-//     snapshot and the exchanged D.
+//     snapshot and the exchanged D, once D is published (so that their reads overlap the
+//     state update, not the D product).
 // Hand-offs between chain and output warps are named barriers; the ring's are mbarriers
 // with bounded waits (a wait that gives up reports GDN_STATUS_WAIT_TIMEOUT).
 constexpr int kDVB = 16;  // value columns per CTA
@@ -677,6 +678,10 @@ __device__ __forceinline__ void out_block(int c, const ChainStage<C> &cst, const
   const int gid = lane >> 2, tig = lane & 3, par = c & 1;
   const bool work = 16 * ow < C;
   bar_sync(kBarSReady + par, kPair);
+  // Q S only once D is formed: the chain's D = U - W S reads the same snapshot and the
+  // block's operands, and the two would otherwise share shared memory on the chain's
+  // critical phase; after it the output warps overlap the state update instead
+  bar_sync(kBarDReady + par, kPair);
   float R[2][4];
   if (work) {
     float r2[2][2][4];  // [k-step parity][n-tile][fragment]
@@ -703,7 +708,6 @@ __device__ __forceinline__ void out_block(int c, const ChainStage<C> &cst, const
 #pragma unroll
       for (int i = 0; i < 4; ++i) R[nt][i] = (r2[0][nt][i] + r2[1][nt][i]) * (i < 2 ? e0 : e1);
   }
-  bar_sync(kBarDReady + par, kPair);
   if (work) {
     // O += A D over the causal part (A is zero above the diagonal)
     for (int ks = 0; ks <= ow; ++ks) {
