@@ -243,23 +243,42 @@ __global__ void __launch_bounds__(kDBThreads, 14) decode_block_kernel(DecodeBloc
   oss += __shfl_xor_sync(0xffffffffu, oss, 2);
   oss += __shfl_xor_sync(0xffffffffu, oss, 4);
   const size_t rowh = (size_t)n * p.hv + h;
-  if (warp == 0 && rsub == 0) {
-    const float4 ov = make_float4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<float4 *>(p.ws_o + rowh * kD + col0) = ov;
-    if (p.o) *reinterpret_cast<float4 *>(p.o + rowh * kD + col0) = ov;
-    if (lane == 0) p.ws_part[rowh * 4 + quarter] = oss;
-  }
-  // o, the sum and every FIFO read of the CTA are done (the barrier) and visible on the GPU
-  // (the fence, cumulative over what the barrier ordered) before the counts below
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    unsigned int *cv = p.ws_cnt + rowh, *ck = p.ws_cnt + (size_t)p.num_seqs * p.hv + (size_t)n * p.hk + kh;
-    const unsigned int gv = atomicAdd(cv, 1u), gk = atomicAdd(ck, 1u);
-    s_last[0] = gv == 3u;
-    s_last[1] = gk == 4u * (unsigned int)ratio - 1u;
-    if (gv == 3u) *cv = 0u;  // every quarter has counted in: ready for the next call
-    if (gk == 4u * (unsigned int)ratio - 1u) *ck = 0u;
+  // ---- S' = d S + k delta^T for this warp's rows, written straight from the update
+  auto store_rows = [&]() {
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      const int i = s * 8 + warp * 4 + rsub;
+      float4 x = s < 8 ? S[s & 7] : s_S[i - 64][cg];
+      const float ki = s_k[i];
+      x.x = d * x.x + ki * delta[0];
+      x.y = d * x.y + ki * delta[1];
+      x.z = d * x.z + ki * delta[2];
+      x.w = d * x.w + ki * delta[3];
+      *reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)i * kD + 4 * cg) = x;
+    }
+  };
+  if (warp == 1) store_rows();  // warp 1's rows go out while warp 0 counts in
+  if (warp == 0) {
+    // this quarter's o and sum of o^2 to the workspace (lanes 0-7 hold the 32 columns)
+    if (rsub == 0) {
+      const float4 ov = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4 *>(p.ws_o + rowh * kD + col0) = ov;
+      if (p.o) *reinterpret_cast<float4 *>(p.o + rowh * kD + col0) = ov;
+      if (lane == 0) p.ws_part[rowh * 4 + quarter] = oss;
+    }
+    // warp 0 wrote o, the sum and the v FIFO entries, and every FIFO read of the CTA was
+    // done before the prologue's barrier: after this warp's barrier and one fence (its
+    // writes visible on the GPU), count in
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      unsigned int *cv = p.ws_cnt + rowh, *ck = p.ws_cnt + (size_t)p.num_seqs * p.hv + (size_t)n * p.hk + kh;
+      const unsigned int gv = atomicAdd(cv, 1u), gk = atomicAdd(ck, 1u);
+      s_last[0] = gv == 3u;
+      s_last[1] = gk == 4u * (unsigned int)ratio - 1u;
+      if (gv == 3u) *cv = 0u;  // every quarter has counted in: ready for the next call
+      if (gk == 4u * (unsigned int)ratio - 1u) *ck = 0u;
+    }
   }
   __syncthreads();
   // ---- the last CTA of the k-head advances its q/k FIFO entries (every CTA that reads them
@@ -281,18 +300,7 @@ __global__ void __launch_bounds__(kDBThreads, 14) decode_block_kernel(DecodeBloc
     yy[1] = ov.y * sc * nw.y * silu_f(raw_hi<T>(zr));
     st_pair<T>(static_cast<T *>(p.y) + rowh * kD + 2 * tid, yy);
   }
-  // ---- S' = d S + k delta^T, written straight from the update
-#pragma unroll
-  for (int s = 0; s < 16; ++s) {
-    const int i = s * 8 + warp * 4 + rsub;
-    float4 x = s < 8 ? S[s & 7] : s_S[i - 64][cg];
-    const float ki = s_k[i];
-    x.x = d * x.x + ki * delta[0];
-    x.y = d * x.y + ki * delta[1];
-    x.z = d * x.z + ki * delta[2];
-    x.w = d * x.w + ki * delta[3];
-    *reinterpret_cast<float4 *>(p.state_out + sbase + (size_t)i * kD + 4 * cg) = x;
-  }
+  if (warp == 0) store_rows();
 }
 
 template <typename T>
