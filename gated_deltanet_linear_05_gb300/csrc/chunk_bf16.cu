@@ -775,12 +775,6 @@ __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 
   const float *s_in = maps ? p.state_in2 : p.state_in;
   float *s_out = maps ? p.state_out2 : p.state_out;
 
-  int bos, eos;
-  seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
-  const int nchunks = (eos - bos + C - 1) / C;
-  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD + blk * kDVB;
-  const char *slot0 = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, 0)) * SB;
-
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -788,6 +782,16 @@ __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 
     }
     mbar_fence_init();
   }
+  // Launched as a programmatic dependent of the kernel before it (pass 1): the set-up above
+  // overlaps that kernel's tail; nothing in global memory is read before it has completed
+  // and its writes are visible.
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
+  int bos, eos;
+  seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
+  const int nchunks = (eos - bos + C - 1) / C;
+  const size_t sbase = ((size_t)n * p.hv + h) * kD * kD + blk * kDVB;
+  const char *slot0 = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, 0)) * SB;
   // state block S[:, blk*16 .. +16) -> fp32 staging (coalesced 64-byte rows)
   for (int e = tid; e < kD * kDVB / 4; e += NT) {
     const int i = e / (kDVB / 4), c4 = e % (kDVB / 4);
@@ -924,8 +928,19 @@ cudaError_t launch_recur(const ChunkParams &p, const TileMaps &m, long long head
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const unsigned grid = (unsigned)((MODE == 1 ? 2 : 1) * heads * (kD / kDVB));
-  recur_kernel<C, TO, MODE><<<grid, MODE == 0 ? kPair + 32 : kChain + 32, smem, stream>>>(p, m.k, m.q);
-  return cudaGetLastError();
+  // a programmatic dependent launch: the CTAs may start (and set up their barriers) as
+  // the kernel before them drains; the kernel waits for its completion before any read
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(MODE == 0 ? kPair + 32 : kChain + 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, recur_kernel<C, TO, MODE>, p, m.k, m.q);
 }
 
 template <int C>
