@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   for (int c = part, it = 0; c < nchunks; c += per_head, ++it) {
     const int tok0 = bos + c * C;
     const int L = min(C, eos - tok0);
-    char *slot = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, c)) * slot_stride(C);
+    char *slot = p.slot_ws + ((size_t)h * p.nslots + slot_index(bos, C, n, c)) * slot_stride(C, LAYOUT == 1);
     char *wn_out = slot, *a_out = slot + slot_a_off(C);
     char *u_out = slot + slot_u_off(C);
     float *dec_out = reinterpret_cast<float *>(slot + slot_dec_off(C));
@@ -749,7 +749,7 @@ __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 
   constexpr int NB = kD / kDVB, MT = C / 16, RC = row_c(C);
   constexpr int NT = MODE == 0 ? kPair + 32 : kChain + 32;
   constexpr int NST = RecSmem<C, MODE>::NST, PW = NT / 32 - 1;  // ring depth, producer warp
-  constexpr size_t SB = slot_stride(C);
+  constexpr size_t SB = slot_stride(C, false);
   constexpr uint32_t kChainTx = (uint32_t)(C * 256 + MT * 512 + 12 * C + 2 * C * 128);
   constexpr uint32_t kOutTx = (uint32_t)(2 * C * 128 + C * RC);
   extern __shared__ unsigned char smem_raw[];
@@ -987,9 +987,9 @@ cudaError_t launch_c(const ChunkParams &p, cudaStream_t stream) {
 
 }  // namespace
 
-size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk) {
+size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk, bool tc) {
   const size_t slots = (size_t)hv * ((size_t)total_tokens / chunk + num_seqs);
-  return 256 + slots * slot_stride(chunk);
+  return 256 + slots * slot_stride(chunk, tc);
 }
 
 cudaError_t launch_chunk_bf16(const ChunkParams &p, cudaStream_t stream) {

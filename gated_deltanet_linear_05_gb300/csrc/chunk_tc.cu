@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(kChThreads, 1) tc_chain_kernel(ChunkParams p) 
   seq_range(p.cu_seqlens, n, p.total_tokens, bos, eos);
   const int nchunks = (eos - bos + C - 1) / C;
   const size_t sbase = ((size_t)n * p.hv + h) * kD * kD;
-  const char *slot0 = p.slot_ws + ((size_t)h * p.nslots + (size_t)(bos / C + n)) * slot_stride(C);
+  const char *slot0 = p.slot_ws + ((size_t)h * p.nslots + (size_t)(bos / C + n)) * kTsBytes;
 
   if (nchunks == 0) {  // empty sequence: the state passes through
     for (int e = tid; e < kD * kD; e += kChThreads)
@@ -700,7 +700,7 @@ __global__ void __launch_bounds__(kChThreads, 1) tc_chain_kernel(ChunkParams p) 
         const int s = c % kChNst;
         if (c >= kChNst) wait(&sm.empty[s], ((c / kChNst) - 1) & 1);
         mbar_arrive_expect_tx(&sm.full[s], (uint32_t)kTsBytes);
-        bulk_g2s(&sm.st[s], slot0 + (size_t)c * slot_stride(C), (uint32_t)kTsBytes, &sm.full[s]);
+        bulk_g2s(&sm.st[s], slot0 + (size_t)c * kTsBytes, (uint32_t)kTsBytes, &sm.full[s]);
       }
     }
   } else if (warp < 4) {

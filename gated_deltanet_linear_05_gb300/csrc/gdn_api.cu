@@ -116,7 +116,8 @@ bool single_pass(const gdn_shape *s) {
 
 size_t chunked_workspace(const gdn_shape *s) {
   if (s->qkv_dtype == GDN_F32 || s->algo == GDN_ALGO_RECURRENT || single_pass(s)) return 0;
-  return gdn::chunk_workspace_bytes(s->total_tokens, s->num_seqs, s->num_v_heads, s->chunk);
+  return gdn::chunk_workspace_bytes(s->total_tokens, s->num_seqs, s->num_v_heads, s->chunk,
+                                    s->algo == GDN_ALGO_TWO_PASS_TENSOR);
 }
 
 gdn_status run_chunked(const Common &c, void *workspace, size_t workspace_bytes, void *stream,

@@ -72,9 +72,9 @@ __host__ __device__ constexpr size_t slot_bytes(int C) {
 //   Ut  U^T fp16 [value col][token], 144-byte rows   DEC fp32 [3][64] G, e^G, e^(G_C - G)
 constexpr size_t kTsWt = 0, kTsQt = 16384, kTsK = 32768, kTsAt = 49152, kTsUt = 57344,
                  kTsDec = 75776, kTsBytes = 76544;
-// Distance between slots: room for either layout at C = 64.
-__host__ __device__ constexpr size_t slot_stride(int C) {
-  return C == 64 && kTsBytes > slot_bytes(C) ? kTsBytes : slot_bytes(C);
+// Distance between slots: the tensor-memory layout's (tc, C = 64) or slot_bytes(C).
+__host__ __device__ constexpr size_t slot_stride(int C, bool tc) {
+  return tc && C == 64 ? kTsBytes : slot_bytes(C);
 }
 
 // The block's input prologue (block_io.cu): causal conv + SiLU over [q | k | v] raw
@@ -173,7 +173,7 @@ cudaError_t launch_identity(float *state, long long states, cudaStream_t stream)
 cudaError_t launch_split_combine(const SplitCombineParams &p, cudaStream_t stream);
 
 // Workspace bytes of the bf16 chunk path: a 256-byte reserved header + slots.
-size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk);
+size_t chunk_workspace_bytes(int total_tokens, int num_seqs, int hv, int chunk, bool tc);
 
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_chunk_bf16(const ChunkParams &p, cudaStream_t stream);

@@ -56,14 +56,15 @@ def test_status_strings(L):
 def test_workspace_size(L):
     sh = gdn.make_shape(8, 4096, 16, 32, chunk=64, algo=gdn.GDN_ALGO_TWO_PASS)
     n = gdn.gdn_workspace_size(sh, gdn.GDN_OP_PREFILL)
-    # a 256-byte header, then one slot per (v-head, block) for T / C + N blocks per head,
-    # room for either pass-2 layout: the mma.sync one (-W and U 64 x 128 fp16, A in 64
-    # rows of 2 x 64 + 16 bytes, 3 x 64 fp32 decays) or, larger, the tensor-memory one
-    # (W^T, diag(e^G) Q and K 64 x 128 fp16, A 64 x 64 fp16, U^T in 128 rows of 144 bytes,
-    # the decays)
+    # a 256-byte header, then one slot per (v-head, block) for T / C + N blocks per head:
+    # -W and U (64 x 128 fp16 each), A in 64 rows of 2 x 64 + 16 bytes, 3 x 64 fp32 decays
     mma_slot = -(-(2 * 64 * 128 * 2 + 64 * (2 * 64 + 16) + 3 * 64 * 4) // 128) * 128
+    assert n == 256 + 32 * (4096 // 64 + 8) * mma_slot
+    # with the tensor-memory second pass the slot holds its operand layouts instead: W^T,
+    # diag(e^G) Q and K (64 x 128 fp16), A (64 x 64 fp16), U^T in 128 rows of 144 bytes
     tc_slot = 3 * 64 * 128 * 2 + 64 * 64 * 2 + 128 * 144 + 3 * 64 * 4
-    assert n == 256 + 32 * (4096 // 64 + 8) * max(mma_slot, tc_slot)
+    sh5 = gdn.make_shape(8, 4096, 16, 32, chunk=64, algo=gdn.GDN_ALGO_TWO_PASS_TENSOR)
+    assert gdn.gdn_workspace_size(sh5, gdn.GDN_OP_PREFILL) == 256 + 32 * (4096 // 64 + 8) * tc_slot
     assert n == gdn.gdn_workspace_size(sh, gdn.GDN_OP_VERIFY)
     assert gdn.gdn_workspace_size(sh, gdn.GDN_OP_DECODE) == 0
     assert gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, chunk=16, dtype=gdn.GDN_F32),
@@ -88,11 +89,11 @@ def test_workspace_size_follows_the_schedule(L):
         assert auto == (0 if n * hv >= gdn.GDN_SINGLE_PASS_MIN_HEADS else two)
     with pytest.raises(gdn.GdnError):
         gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, algo=6), gdn.GDN_OP_PREFILL)
-    # the two-pass schedule with the tensor-memory second pass: the same slots (room for
-    # either layout), 64-token blocks only
+    # the two-pass schedule with the tensor-memory second pass: larger slots, 64-token
+    # blocks only
     sh2 = gdn.make_shape(3, 700, 2, 4, chunk=64, algo=gdn.GDN_ALGO_TWO_PASS)
     sh5 = gdn.make_shape(3, 700, 2, 4, chunk=64, algo=gdn.GDN_ALGO_TWO_PASS_TENSOR)
-    assert gdn.gdn_workspace_size(sh5, gdn.GDN_OP_PREFILL) == gdn.gdn_workspace_size(sh2, gdn.GDN_OP_PREFILL)
+    assert gdn.gdn_workspace_size(sh5, gdn.GDN_OP_PREFILL) > gdn.gdn_workspace_size(sh2, gdn.GDN_OP_PREFILL)
     with pytest.raises(gdn.GdnError):
         gdn.gdn_workspace_size(gdn.make_shape(1, 64, 1, 1, chunk=16,
                                               algo=gdn.GDN_ALGO_TWO_PASS_TENSOR), gdn.GDN_OP_PREFILL)
