@@ -266,11 +266,11 @@ def run_gdn(args):
                    "l2": "flushed (512 MiB write) before every timed step",
                    "parallelism": "dp%d (independent batches per GPU)" % world},
         # traffic: DRAM bytes of the step's two kernels from the committed ncu capture
-        # (pass 1 54.1 MB + pass 2 80.4 MB; ncu flushes caches between kernels, so the
+        # (pass 1 53.9 MB + pass 2 80.1 MB; ncu flushes caches between kernels, so the
         # workspace round trip counts as DRAM traffic there)
-        "roofline": roofline("hbm", gbs, pk["hbm"], "GB/s", traffic=134.5e6),
+        "roofline": roofline("hbm", gbs, pk["hbm"], "GB/s", traffic=134.0e6),
         "roofline_scope": "one gdn_prefill_chunked call (pass 1 + pass 2); the dominant "
-                          "kernel, pass 2, takes ~59 of its ~89 us",
+                          "kernel, pass 2, takes ~57 of its ~87 us",
         "tensor": {"achieved": round(tfs, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                    "frac": round(tfs / pk["bf16"], 4), "algorithmic_flops": flops},
         "algorithmic_bytes": byts,

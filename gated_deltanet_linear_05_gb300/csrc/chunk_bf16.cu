@@ -504,10 +504,12 @@ constexpr int kChain = 32 * kChainWarps;
 constexpr int kPair = 32 * (kChainWarps + kOutWarps);
 
 // Named barriers of pass 2 (0 is __syncthreads)
+constexpr int kOutBufs = 3;    // snapshot and D^T buffers shared with the output warps
 constexpr int kBarChain = 1;   // the chain warps among themselves
-constexpr int kBarSReady = 2;  // +parity: snapshot S_c published (chain arrives, output waits)
-constexpr int kBarDone = 4;    // +parity: output warps done with block c (output arrives, chain waits)
-constexpr int kBarDReady = 6;  // +parity: D_c published (chain arrives, output waits)
+constexpr int kBarSReady = 2;  // +c mod kOutBufs: snapshot S_c published (chain arrives, output waits)
+constexpr int kBarDone = kBarSReady + kOutBufs;  // +c mod kOutBufs: output warps done with block c
+constexpr int kBarDReady = kBarDone + kOutBufs;  // +c mod kOutBufs: D_c published (chain arrives)
+static_assert(kBarDReady + kOutBufs <= 16, "named barriers 0-15");
 
 // Byte offset of byte b of row r in a shared tile of RB-byte rows whose 16-byte granules
 // are permuted per row (granule g stored at g ^ f(r), f(r) = 4 (r & 1) + ((r >> 1) & 3)):
@@ -541,9 +543,12 @@ template <int C, int MODE>
 struct RecSmem {
   static constexpr int NST = MODE == 0 ? 3 : 2;  // ring depth
   ChainStage<C> cs[NST];
-  alignas(128) char Sn[2][kDVB * 256];   // S^T (fp16) [16 value cols][128 keys], by parity
-  alignas(128) char Dt[2][kDVB * 128];   // D^T (fp16) [16 value cols][C tokens], by parity
-  alignas(128) char Dst[2][kDVB * 128];  // D~^T, D~ = diag(e^(G_C - G)) D, likewise
+  // snapshot and D^T buffers: kOutBufs with output warps (the chain overwrites those of
+  // block c + 1 - kOutBufs while the output warps may still be on a later block), else two
+  static constexpr int NSB = MODE == 0 ? kOutBufs : 2;
+  alignas(128) char Sn[NSB][kDVB * 256];  // S^T (fp16) [16 value cols][128 keys], by c mod NSB
+  alignas(128) char Dt[NSB][kDVB * 128];  // D^T (fp16) [16 value cols][C tokens], by c mod NSB
+  alignas(128) char Dst[2][kDVB * 128];  // D~^T, D~ = diag(e^(G_C - G)) D (chain only), by parity
   alignas(16) float S32[kD][kDVB + 4];   // fp32 staging of the state block
   alignas(8) uint64_t full[NST], empty[NST];
 };
@@ -582,7 +587,8 @@ template <int C, int MODE>
 __device__ __forceinline__ void chain_block(int c, const ChainStage<C> &st, const KStage<C> &kst,
                                             float (&Sa)[4][4], RecSmem<C, MODE> &sm, int w, int lane,
                                             bool dwork, bool with_u) {
-  const int gid = lane >> 2, tig = lane & 3, par = c & 1;
+  constexpr int NSB = RecSmem<C, MODE>::NSB;
+  const int gid = lane >> 2, tig = lane & 3, par = c & 1, cur = c % NSB, nxt = (c + 1) % NSB;
   if (dwork) {
     // four independent accumulations per n-tile (key spans s), two products deep each
     float d[4][2][4];  // [key span][n-tile: value columns 8nt..][fragment]
@@ -592,7 +598,7 @@ __device__ __forceinline__ void chain_block(int c, const ChainStage<C> &st, cons
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) d[g][nt][i] = 0.f;
-    const char *Sn = sm.Sn[par];
+    const char *Sn = sm.Sn[cur];
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       uint32_t b0[4], b1[4], w0[4], w1[4];
@@ -622,16 +628,16 @@ __device__ __forceinline__ void chain_block(int c, const ChainStage<C> &st, cons
     // D^T and D~^T: matrices m = 2nt + rh (tokens 16w + 8rh.., columns 8nt..) stored
     // transposed
     const int m = lane >> 3, r = lane & 7;
-    char *dt = sm.Dt[par] + swz_row(8 * (m >> 1) + r, 128, 32 * w + 16 * (m & 1));
-    stsm_x4_t(dt, pack_f16(D[0][0], D[0][1]), pack_f16(D[0][2], D[0][3]), pack_f16(D[1][0], D[1][1]),
-              pack_f16(D[1][2], D[1][3]));
+    const int doff = swz_row(8 * (m >> 1) + r, 128, 32 * w + 16 * (m & 1));
+    stsm_x4_t(sm.Dt[cur] + doff, pack_f16(D[0][0], D[0][1]), pack_f16(D[0][2], D[0][3]),
+              pack_f16(D[1][0], D[1][1]), pack_f16(D[1][2], D[1][3]));
     const float ed0 = st.DEC[2 * C + 16 * w + gid], ed1 = st.DEC[2 * C + 16 * w + gid + 8];
-    stsm_x4_t(dt + (sm.Dst[par] - sm.Dt[par]), pack_f16(ed0 * D[0][0], ed0 * D[0][1]),
+    stsm_x4_t(sm.Dst[par] + doff, pack_f16(ed0 * D[0][0], ed0 * D[0][1]),
               pack_f16(ed1 * D[0][2], ed1 * D[0][3]), pack_f16(ed0 * D[1][0], ed0 * D[1][1]),
               pack_f16(ed1 * D[1][2], ed1 * D[1][3]));
   }
   bar_sync(kBarChain, kChain);
-  if (MODE == 0) bar_arrive(kBarDReady + par, kPair);
+  if (MODE == 0) bar_arrive(kBarDReady + cur, kPair);
 
   // S^T <- e^(G_C) S^T + D~^T K over keys 32w .. 32w+31 (the k rows as loaded, bf16 ->
   // fp16 in registers): two accumulations by token step parity, summed with the scaled
@@ -663,11 +669,11 @@ __device__ __forceinline__ void chain_block(int c, const ChainStage<C> &st, cons
   for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) Sa[nt][i] = fmaf(gam, Sa[nt][i], X[0][nt][i] + X[1][nt][i]);
-  // S_{c+1} into the other snapshot buffer once the output warps are done with block c - 1
-  if (MODE == 0 && c >= 1) bar_sync(kBarDone + (par ^ 1), kPair);
-  write_snapshot(Sa, sm.Sn[par ^ 1], w, lane);
+  // S_{c+1} into the buffer of S_{c+1-NSB} once the output warps are done with that block
+  if (MODE == 0 && c + 1 >= NSB) bar_sync(kBarDone + nxt, kPair);
+  write_snapshot(Sa, sm.Sn[nxt], w, lane);
   bar_sync(kBarChain, kChain);
-  if (MODE == 0) bar_arrive(kBarSReady + (par ^ 1), kPair);
+  if (MODE == 0) bar_arrive(kBarSReady + nxt, kPair);
 }
 
 template <int C, typename TO>
@@ -675,13 +681,13 @@ __device__ __forceinline__ void out_block(int c, const ChainStage<C> &cst, const
                                           RecSmem<C, 0> &sm, int ow, int lane, TO *o, int tok0,
                                           int L, int hv, int h, int blk) {
   constexpr int RC = row_c(C);
-  const int gid = lane >> 2, tig = lane & 3, par = c & 1;
+  const int gid = lane >> 2, tig = lane & 3, cur = c % kOutBufs;
   const bool work = 16 * ow < C;
-  bar_sync(kBarSReady + par, kPair);
+  bar_sync(kBarSReady + cur, kPair);
   // Q S only once D is formed: the chain's D = U - W S reads the same snapshot and the
   // block's operands, and the two would otherwise share shared memory on the chain's
   // critical phase; after it the output warps overlap the state update instead
-  bar_sync(kBarDReady + par, kPair);
+  bar_sync(kBarDReady + cur, kPair);
   float R[2][4];
   if (work) {
     float r2[2][2][4];  // [k-step parity][n-tile][fragment]
@@ -691,7 +697,7 @@ __device__ __forceinline__ void out_block(int c, const ChainStage<C> &cst, const
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) r2[e][nt][i] = 0.f;
-    const char *Sn = sm.Sn[par];
+    const char *Sn = sm.Sn[cur];
 #pragma unroll
     for (int ks = 0; ks < kD / 16; ++ks) {
       uint32_t a[4], b[4];
@@ -713,7 +719,7 @@ __device__ __forceinline__ void out_block(int c, const ChainStage<C> &cst, const
     for (int ks = 0; ks <= ow; ++ks) {
       uint32_t a[4], b[4];
       lda_p<RC>(a, ost.A, 16 * ow, 16 * ks, lane);
-      ldsm_x4(b, sm.Dt[par] + swz_row((lane & 7) + (lane >> 4) * 8, 128, 2 * (16 * ks + ((lane >> 3) & 1) * 8)));
+      ldsm_x4(b, sm.Dt[cur] + swz_row((lane & 7) + (lane >> 4) * 8, 128, 2 * (16 * ks + ((lane >> 3) & 1) * 8)));
       mma_f16(R[0], a, b[0], b[1]);
       mma_f16(R[1], a, b[2], b[3]);
     }
@@ -735,7 +741,7 @@ __device__ __forceinline__ void out_block(int c, const ChainStage<C> &cst, const
     }
   }
   __syncwarp();
-  bar_arrive(kBarDone + par, kPair);
+  bar_arrive(kBarDone + cur, kPair);
 }
 
 // MODE 0: pass 2 (state chain and outputs): 4 chain + 4 output warps + 1 producer warp.
@@ -844,7 +850,8 @@ __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 
       chain_block<C, MODE>(c, sm.cs[s], ks[s], Sa, sm, w, lane, dwork, !maps);
       if (tid == 0) mbar_arrive(&sm.empty[s]);  // all chain warps are past the barrier
     }
-    if (MODE == 0 && nchunks >= 1) bar_sync(kBarDone + ((nchunks - 1) & 1), kPair);
+    if (MODE == 0)  // the output warps' last blocks
+      for (int c = max(0, nchunks + 1 - kOutBufs); c < nchunks; ++c) bar_sync(kBarDone + c % kOutBufs, kPair);
     if (!ok && lane == 0) report_status(p.err, GDN_STATUS_WAIT_TIMEOUT);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
@@ -863,7 +870,7 @@ __global__ void __launch_bounds__(MODE == 0 ? kPair + 32 : kChain + 32, C == 64 
                        min(C, eos - tok0), p.hv, h, blk);
       if (lane == 0) mbar_arrive(&sm.empty[s]);
     }
-    bar_sync(kBarSReady + (nchunks & 1), kPair);
+    bar_sync(kBarSReady + nchunks % kOutBufs, kPair);
     if (!ok && lane == 0) report_status(p.err, GDN_STATUS_WAIT_TIMEOUT);
   }
   __syncthreads();
