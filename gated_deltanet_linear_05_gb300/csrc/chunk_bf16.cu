@@ -496,8 +496,11 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
 //   output warps 4-7: for tokens 16ow .. 16ow+15, O = diag(e^G) Q S + A D from the same
 //     snapshot and the exchanged D, once D is published (so that their reads overlap the
 //     state update, not the D product).
-// Hand-offs between chain and output warps are named barriers; the ring's are mbarriers
-// with bounded waits (a wait that gives up reports GDN_STATUS_WAIT_TIMEOUT).
+// Hand-offs between chain and output warps are named barriers over kOutBufs snapshot and
+// D^T buffers, so that the output warps may trail the chain by up to two blocks (the
+// chain overwrites the buffers of block c - 2 once their outputs are done); the ring's
+// hand-offs are mbarriers with bounded waits (a wait that gives up reports
+// GDN_STATUS_WAIT_TIMEOUT).
 constexpr int kDVB = 16;  // value columns per CTA
 constexpr int kChainWarps = 4, kOutWarps = 4;
 constexpr int kChain = 32 * kChainWarps;
