@@ -87,6 +87,22 @@ def test_chunked_form_slow_decay_dk128():
         assert _rel(o2, o1) < 1e-11 and _rel(s2, s1) < 1e-11
 
 
+def test_chunked_form_strong_decay():
+    """g ~ -28 per token: e^G of a 64-token block underflows to zero in float64 long before
+    its end.  The chunk form takes every decay as the exp of a difference of cumsums, so it
+    stays finite and equal to the token loop (a product e^G_t e^-G_j would be 0 * inf)."""
+    wl = gi.Workload("s", [150, 7, 64], 1, 2, dk=16, dv=8, dtype="f32", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=5, gate_scale=40.0)
+    G = np.cumsum(x["g"][:64, 0].astype(np.float64))
+    assert np.exp(G[-1]) == 0.0  # the regime the pin is about
+    o1, s1 = _run(x)
+    for C in (16, 64):
+        o2, s2 = oracle.chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state0"],
+                                x["cu_seqlens"], C, "doubling")
+        assert np.isfinite(o2).all() and np.isfinite(s2).all()
+        assert _rel(o2, o1) < 1e-12 and _rel(s2, s1) < 1e-12
+
+
 # ---------------------------------------------------------------- closed forms
 
 def test_beta_zero_is_pure_decay():

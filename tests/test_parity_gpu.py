@@ -138,6 +138,20 @@ def test_prefill_slow_decay_bf16(algo):
 
 
 @pytest.mark.parametrize("algo", list(ALGOS))
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_prefill_strong_decay_bf16(algo, chunk):
+    """g ~ -28 per token: the in-block decays underflow to zero within a few tokens, which
+    only the exp of a difference of cumsums survives (a product of e^G_t and e^-G_j would
+    give 0 * inf); every schedule must stay finite and match the oracle."""
+    if algo not in ALGOS_ANY_C and chunk != 64:
+        pytest.skip("64-token blocks only")
+    wl = gi.Workload("strong", [200, 37, 64], 1, 2, chunk=chunk, dtype="bf16", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=13, gate_scale=40.0)
+    o_ref, s_ref = _oracle(x)
+    _run_and_check(x, wl, o_ref, s_ref, "strong decay C=%d" % chunk, algo=ALGOS[algo])
+
+
+@pytest.mark.parametrize("algo", list(ALGOS))
 def test_prefill_T4096_H16_full(algo):
     wl = gi.prefill_t4096_h16()
     x = gi.make_inputs(wl)
