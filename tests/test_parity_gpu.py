@@ -152,6 +152,16 @@ def test_prefill_strong_decay_bf16(algo, chunk):
 
 
 @pytest.mark.parametrize("algo", list(ALGOS))
+@pytest.mark.parametrize("hk,hv", [(1, 8), (2, 16)])
+def test_prefill_wide_head_groups_bf16(algo, hk, hv):
+    """8 v-heads per k-head: every v-head of a group reads the same q, k rows (h / 8)."""
+    wl = gi.Workload("gqa8", [90, 1, 130], hk, hv, chunk=64, dtype="bf16", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=17 + hv)
+    o_ref, s_ref = _oracle(x)
+    _run_and_check(x, wl, o_ref, s_ref, "Hk=%d Hv=%d" % (hk, hv), algo=ALGOS[algo])
+
+
+@pytest.mark.parametrize("algo", list(ALGOS))
 def test_prefill_T4096_H16_full(algo):
     wl = gi.prefill_t4096_h16()
     x = gi.make_inputs(wl)
@@ -224,11 +234,12 @@ def test_verify_B128_H32_T16_full(algo):
 # ------------------------------------------------------------------ decode
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_decode_one_token_per_sequence(dtype):
+@pytest.mark.parametrize("hk,hv", [(1, 3), (2, 16)])
+def test_decode_one_token_per_sequence(dtype, hk, hv):
     import torch
     import gated_deltanet_linear_05_gb300 as gdn
-    wl = gi.Workload("dec", [1] * 5, 1, 3, dtype=dtype, s0_scale=0.1)
-    x = gi.make_inputs(wl, seed=2)
+    wl = gi.Workload("dec", [1] * 5, hk, hv, dtype=dtype, s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=2 + hv)
     d = device_inputs(x, dtype)
     s_out = torch.empty_like(d["state0"])
     o32 = torch.empty(d["v"].shape, dtype=torch.float32, device="cuda")
