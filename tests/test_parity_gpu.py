@@ -151,6 +151,17 @@ def test_prefill_strong_decay_bf16(algo, chunk):
     _run_and_check(x, wl, o_ref, s_ref, "strong decay C=%d" % chunk, algo=ALGOS[algo])
 
 
+@pytest.mark.parametrize("algo", [None, "recurrent"])
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_prefill_strong_decay_f32(algo, chunk):
+    """As above for fp32 q/k/v (the fp32 chunk kernel, and the token loop)."""
+    kw = {"algo": ALGOS[algo]} if algo else {}
+    wl = gi.Workload("strong", [200, 37, 64], 1, 2, chunk=chunk, dtype="f32", s0_scale=0.1)
+    x = gi.make_inputs(wl, seed=14, gate_scale=40.0)
+    o_ref, s_ref = _oracle(x)
+    _run_and_check(x, wl, o_ref, s_ref, "strong decay f32 C=%d" % chunk, **kw)
+
+
 @pytest.mark.parametrize("algo", list(ALGOS))
 @pytest.mark.parametrize("hk,hv", [(1, 8), (2, 16)])
 def test_prefill_wide_head_groups_bf16(algo, hk, hv):

@@ -68,9 +68,11 @@ def test_varlen_batch_with_empty_and_short_sequences(chunk, seg):
     assert np.array_equal(s[1], x["state0"][1].astype(np.float64))
 
 
-@pytest.mark.parametrize("algo", [1, 2, 3])
+@pytest.mark.parametrize("algo", [1, 2, 3, 5])
 def test_each_inner_schedule(algo):
-    """The three passes run on the chunked schedule the shape asks for."""
+    """The three passes run on the chunked schedule the shape asks for (with
+    GDN_ALGO_TWO_PASS_TENSOR the shared pass 1 and the chain-only and output runs of the
+    mma.sync second pass, in that schedule's larger workspace)."""
     wl = gi.Workload("split3", [700, 300], 1, 2, chunk=64, dtype="bf16", s0_scale=0.1)
     x = gi.make_inputs(wl, seed=33)
     o, s = _split(x, wl, 192, algo=algo)
