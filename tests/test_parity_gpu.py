@@ -99,7 +99,8 @@ def test_prefill_small_shapes_bf16(algo, chunk, lengths, hk, hv):
 
 @pytest.mark.parametrize("dtype,algo", [("f32", None), ("bf16", "two_pass"),
                                         ("bf16", "single_pass"), ("bf16", "tensor_memory"),
-                                        ("bf16", "recurrent"), ("f32", "recurrent")])
+                                        ("bf16", "recurrent"), ("f32", "recurrent"),
+                                        ("bf16", "two_pass_tensor")])
 def test_prefill_zero_initial_state_and_in_place(dtype, algo):
     kw = {"algo": ALGOS[algo]} if algo else {}
     chunk = 32 if algo in (None, *ALGOS_ANY_C) else 64
